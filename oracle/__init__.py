@@ -1,0 +1,136 @@
+"""fp64 CPU oracle for masked space attention and windowed causal time attention.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's CPU
+baseline may import this package; the CUDA library never calls it, and it shares
+no code with the CUDA path.  The arithmetic lives in od_oracle.c (plain loops,
+double precision); this module compiles it with gcc and marshals numpy arrays.
+
+Every function takes float64 arrays in the library's layouts
+(Q/O/dO/dQ [B,T,S,Hq,D], K/V/dK/dV [B,T,S,Hkv,D], LSE [B,T,S,Hq]) and returns
+float64 results.  Use `from_bf16` to widen the bf16 inputs exactly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "od_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile od_oracle.c into liboracle.so (gcc -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c99", "-fno-fast-math",
+                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            dp = ctypes.POINTER(ctypes.c_double)
+            i = ctypes.c_int
+            fwd = [dp, dp, dp, dp, dp, i, i, i, i, i, i, i, ctypes.c_double, i]
+            bwd = [dp, dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, i, ctypes.c_double, i]
+            for name, args in (("oracle_space_fwd", fwd), ("oracle_time_fwd", fwd),
+                               ("oracle_space_bwd", bwd), ("oracle_time_bwd", bwd)):
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = ctypes.c_int
+            lib.oracle_num_threads.argtypes = [i]
+            lib.oracle_num_threads.restype = i
+            _lib = lib
+    return _lib
+
+
+def num_threads(requested: int = 0) -> int:
+    return _load().oracle_num_threads(int(requested))
+
+
+def from_bf16(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) exactly to float64."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(
+        np.float32).astype(np.float64)
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _prep(q, k, v):
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    if q.ndim != 5 or k.shape != v.shape or q.shape[:3] != k.shape[:3] or q.shape[4] != k.shape[4]:
+        raise ValueError("expected Q [B,T,S,Hq,D] and K, V [B,T,S,Hkv,D]")
+    return q, k, v
+
+
+def _fwd(name, q, k, v, extra, scale, nthreads):
+    q, k, v = _prep(q, k, v)
+    B, T, S, Hq, D = q.shape
+    Hkv = k.shape[3]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, T, S, Hq), dtype=np.float64)
+    rc = getattr(_load(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                B, T, S, Hq, Hkv, D, int(extra), float(scale), int(nthreads))
+    if rc:
+        raise ValueError("oracle rejected the arguments")
+    return o, lse
+
+
+def _bwd(name, q, k, v, dout, extra, scale, nthreads):
+    q, k, v = _prep(q, k, v)
+    dout = np.ascontiguousarray(dout, dtype=np.float64)
+    if dout.shape != q.shape:
+        raise ValueError("dO must have Q's shape")
+    B, T, S, Hq, D = q.shape
+    Hkv = k.shape[3]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, T, S, Hq), dtype=np.float64)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    rc = getattr(_load(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(o), _ptr(lse),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, T, S, Hq, Hkv, D, int(extra),
+                                float(scale), int(nthreads))
+    if rc:
+        raise ValueError("oracle rejected the arguments")
+    return o, lse, dq, dk, dv
+
+
+def space_fwd(q, k, v, agent=-1, scale=None, nthreads=0):
+    """Masked space attention forward. Returns (O, LSE)."""
+    return _fwd("oracle_space_fwd", q, k, v, agent, scale, nthreads)
+
+
+def time_fwd(q, k, v, window, scale=None, nthreads=0):
+    """Windowed causal time attention forward. Returns (O, LSE)."""
+    return _fwd("oracle_time_fwd", q, k, v, window, scale, nthreads)
+
+
+def space_bwd(q, k, v, dout, agent=-1, scale=None, nthreads=0):
+    """Space attention backward. Returns (O, LSE, dQ, dK, dV)."""
+    return _bwd("oracle_space_bwd", q, k, v, dout, agent, scale, nthreads)
+
+
+def time_bwd(q, k, v, dout, window, scale=None, nthreads=0):
+    """Time attention backward. Returns (O, LSE, dQ, dK, dV)."""
+    return _bwd("oracle_time_bwd", q, k, v, dout, window, scale, nthreads)
