@@ -1,0 +1,381 @@
+"""Benchmark of the block-causal attention hot path on one B300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch of the Minecraft 1.6B dynamics
+layer shapes (B=1, T=256, S=290, 30 Q / 3 KV heads, head_dim 64, window 192, agent 289):
+space attention forward, time attention forward, and (when enabled) both backward passes.
+Metric: algorithmic TFLOP/s (allowed query-key pairs only; a backward counts 2.5 forward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this project has) on a
+bounded sample of the same workload.  Under torchrun each rank runs an independent replica
+(the operator has no cross-GPU exchange); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_causal_video_attention_b300 import synth  # noqa: E402
+
+METRIC = "space/time attention TFLOP/s (fwd, fwd+bwd) and % of B300 bf16 roofline"
+UNIT = "TFLOP/s"
+
+
+def pairs_space(w):
+    n = w.S * w.S - (w.S - 1 if w.agent >= 0 else 0)
+    return n * w.B * w.T * w.Hq
+
+
+def pairs_time(w):
+    n = sum(min(t + 1, w.window) for t in range(w.T))
+    return n * w.B * w.S * w.Hq
+
+
+def flops(w):
+    """Algorithmic FLOPs per op: 4*D per allowed (query, key) pair and head; bwd = 2.5x."""
+    f = {"space_fwd": 4.0 * w.D * pairs_space(w), "time_fwd": 4.0 * w.D * pairs_time(w)}
+    f["space_bwd"] = 2.5 * f["space_fwd"]
+    f["time_bwd"] = 2.5 * f["time_fwd"]
+    return f
+
+
+def fwd_bytes(w):
+    rows = w.B * w.T * w.S
+    return rows * (2 * w.Hq * w.D * 2 + 2 * w.Hkv * w.D * 2 + 4 * w.Hq)
+
+
+def bwd_bytes(w):
+    rows = w.B * w.T * w.S
+    # read Q, K, V, O, dO, LSE; write dQ, dK, dV
+    return rows * (3 * w.Hq * w.D * 2 + 2 * w.Hkv * w.D * 2 + 4 * w.Hq + w.Hq * w.D * 2
+                   + 2 * w.Hkv * w.D * 2)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+class Clocks:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for n, val in zip(names, r[5:9]):
+                    if val.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                pass
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, nunits, with_bwd):
+    """Time the fp64 oracle on `nunits` whole units of each op; returns (flop, seconds,
+    threads, description)."""
+    import oracle
+    oracle.build()
+    q, k, v, dout = synth.make_inputs(w, with_dout=True)
+    G = w.G
+    rng = np.random.default_rng(1234)
+    f = flops(w)
+    tot_flop, tot_s = 0.0, 0.0
+    units_space = w.B * w.T * w.Hkv
+    units_time = w.B * w.S * w.Hkv
+    per_unit = {"space_fwd": f["space_fwd"] / units_space, "time_fwd": f["time_fwd"] / units_time,
+                "space_bwd": f["space_bwd"] / units_space, "time_bwd": f["time_bwd"] / units_time}
+    # gather sub-problems: nunits space units stacked as B, same for time
+    sb = [(int(rng.integers(w.B)), int(rng.integers(w.T)), int(rng.integers(w.Hkv))) for _ in range(nunits)]
+    tb = [(int(rng.integers(w.B)), int(rng.integers(w.S)), int(rng.integers(w.Hkv))) for _ in range(nunits)]
+    X = oracle.from_bf16
+    sq = np.concatenate([X(q[b:b+1, t:t+1, :, h*G:(h+1)*G]) for b, t, h in sb])
+    sk = np.concatenate([X(k[b:b+1, t:t+1, :, h:h+1]) for b, t, h in sb])
+    sv = np.concatenate([X(v[b:b+1, t:t+1, :, h:h+1]) for b, t, h in sb])
+    sd = np.concatenate([X(dout[b:b+1, t:t+1, :, h*G:(h+1)*G]) for b, t, h in sb])
+    tq = np.concatenate([X(q[b:b+1, :, s:s+1, h*G:(h+1)*G]) for b, s, h in tb])
+    tk = np.concatenate([X(k[b:b+1, :, s:s+1, h:h+1]) for b, s, h in tb])
+    tv = np.concatenate([X(v[b:b+1, :, s:s+1, h:h+1]) for b, s, h in tb])
+    td = np.concatenate([X(dout[b:b+1, :, s:s+1, h*G:(h+1)*G]) for b, s, h in tb])
+    nth = oracle.num_threads(0)
+    t0 = time.perf_counter()
+    if with_bwd:
+        oracle.space_bwd(sq, sk, sv, sd, w.agent, w.scale)
+        oracle.time_bwd(tq, tk, tv, td, w.window, w.scale)
+        tot_flop = nunits * (per_unit["space_fwd"] + per_unit["space_bwd"] + per_unit["time_fwd"]
+                             + per_unit["time_bwd"])
+    else:
+        oracle.space_fwd(sq, sk, sv, w.agent, w.scale)
+        oracle.time_fwd(tq, tk, tv, w.window, w.scale)
+        tot_flop = nunits * (per_unit["space_fwd"] + per_unit["time_fwd"])
+    tot_s = time.perf_counter() - t0
+    desc = "%d space units (b,t,kv head) + %d time units (b,s,kv head) of %s, %s" % (
+        nunits, nunits, w.name, "fwd+bwd" if with_bwd else "fwd")
+    return tot_flop, tot_s, nth, desc
+
+
+def run_reference(args, w, with_bwd):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    nunits = args.ref_units
+    vals = []
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample(w, max(1, nunits // 8), with_bwd)
+    for _ in range(args.steps):
+        fl, s, nth, desc = oracle_sample(w, nunits, with_bwd)
+        vals.append((fl, s))
+    fl = sum(v[0] for v in vals)
+    s = sum(v[1] for v in vals)
+    value = fl / s / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nth, "kind": "oracle",
+                             "sample": desc + " per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU path
+def run_ours(args, w, with_bwd):
+    import torch
+    import torch.distributed as dist
+    from block_causal_video_attention_b300 import api
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    q, k, v, dout = synth.make_inputs(w, with_dout=True)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    hq, hk, hv, hd = (to(a).pin_memory() for a in (q, k, v, dout))
+    dq, dk, dv, dd = (t.to(dev) for t in (hq, hk, hv, hd))
+    stream = torch.cuda.current_stream()
+    o_s = torch.empty_like(dq)
+    o_t = torch.empty_like(dq)
+    l_s = torch.empty(dq.shape[:4], dtype=torch.float32, device=dev)
+    l_t = torch.empty_like(l_s)
+    ops = ["space_fwd", "time_fwd"]
+    if with_bwd:
+        ops += ["space_bwd", "time_bwd"]
+        g = [torch.empty_like(x) for x in (dq, dk, dv, dq, dk, dv)]
+        ws_s = torch.empty(max(api.bwd_workspace_bytes(0, w.B, w.T, w.S, w.Hq, w.Hkv), 16),
+                           dtype=torch.uint8, device=dev)
+        ws_t = torch.empty(max(api.bwd_workspace_bytes(1, w.B, w.T, w.S, w.Hq, w.Hkv), 16),
+                           dtype=torch.uint8, device=dev)
+
+    ev = {op: [] for op in ops}
+
+    def step(record, Q=dq, K=dk, V=dv, DO=dd):
+        def timed(op, fn):
+            if record:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ev[op].append((a, b))
+            else:
+                fn()
+        timed("space_fwd", lambda: api.space_attn_fwd(Q, K, V, w.agent, w.scale, o_s, l_s, stream))
+        timed("time_fwd", lambda: api.time_attn_fwd(Q, K, V, w.window, w.scale, o_t, l_t, stream))
+        if with_bwd:
+            timed("space_bwd", lambda: api.space_attn_bwd(Q, K, V, o_s, l_s, DO, w.agent, w.scale,
+                                                          workspace=ws_s, out=g[:3], stream=stream))
+            timed("time_bwd", lambda: api.time_attn_bwd(Q, K, V, o_t, l_t, DO, w.window, w.scale,
+                                                        workspace=ws_t, out=g[3:], stream=stream))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    if api.get_device_status() != 0:
+        raise RuntimeError("device timeout during warm-up")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        end.record(stream)
+        torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if api.get_device_status() != 0:
+        raise RuntimeError("device timeout during the timed region")
+    f = flops(w)
+    step_flop = sum(f[o] for o in ops)
+    value = world * step_flop * args.steps / (ms * 1e-3) / 1e12
+    per_op = {}
+    for op in ops:
+        t_ms = float(np.mean([a.elapsed_time(b) for a, b in ev[op]]))
+        per_op[op] = {"ms": t_ms, "tflops": f[op] / (t_ms * 1e-3) / 1e12}
+
+    # end to end: pinned host inputs -> device, the step, results back to pinned host memory
+    outs = [o_s, l_s, o_t, l_t] + (g if with_bwd else [])
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    hin = [hq, hk, hv] + ([hd] if with_bwd else [])
+    din = [torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv), torch.empty_like(dd)]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step():
+        for h, d in zip(hin, din):
+            d.copy_(h, non_blocking=True)
+        step(False, din[0], din[1], din[2], din[3])
+        for d, h in zip(outs, hout):
+            h.copy_(d, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = world * step_flop * args.steps / (e2e_ms * 1e-3) / 1e12
+
+    hbm, tc, tc_sus, src = load_peaks()
+    # dominant kernel: the op with the largest share of device time
+    dom = max(ops, key=lambda o: per_op[o]["ms"])
+    fwd_b, bwd_b = fwd_bytes(w), bwd_bytes(w)
+    op_bytes = {"space_fwd": fwd_b, "time_fwd": fwd_b, "space_bwd": bwd_b, "time_bwd": bwd_b}
+    for op in ops:
+        t_s = per_op[op]["ms"] * 1e-3
+        bound = "tensor" if f[op] / (tc * 1e12) >= op_bytes[op] / (hbm * 1e9) else "hbm"
+        per_op[op]["bound"] = bound
+        per_op[op]["gbs"] = op_bytes[op] / t_s / 1e9
+        per_op[op]["frac"] = (per_op[op]["tflops"] / tc) if bound == "tensor" else (per_op[op]["gbs"] / hbm)
+    d = per_op[dom]
+    if d["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": d["tflops"], "peak": tc, "unit": "TFLOP/s",
+                "frac": d["tflops"] / tc, "traffic": None, "kernel": dom,
+                "peak_source": "%s bf16 burst" % src}
+    else:
+        roof = {"bound": "hbm", "achieved": d["gbs"], "peak": hbm, "unit": "GB/s",
+                "frac": d["gbs"] / hbm, "traffic": None, "kernel": dom,
+                "peak_source": "%s HBM copy" % src}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, s, nth, desc = oracle_sample(w, args.ref_units, with_bwd)
+        cpu = {"value": fl / s / 1e12, "unit": UNIT, "cores": nth, "kind": "oracle", "sample": desc}
+
+    launches_per_step = {"space_fwd": 1, "time_fwd": 1, "space_bwd": api.BWD_LAUNCHES,
+                         "time_bwd": api.BWD_LAUNCHES}
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "T": w.T, "S": w.S, "Hq": w.Hq,
+                           "Hkv": w.Hkv, "head_dim": w.D, "window": w.window, "agent": w.agent,
+                           "ops": ops, "l2": "inputs larger than L2 (Q alone %.0f MB)" %
+                           (w.B * w.T * w.S * w.Hq * w.D * 2 / 1e6),
+                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "per_op": per_op, "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h},
+                "gpu_launches": args.steps * sum(launches_per_step[o] for o in ops),
+                "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--ref-units", type=int, default=6)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    name = args.workload or ("minecraft_fwd" if args.fwd_only else "minecraft_fwd_bwd")
+    w = synth.WORKLOADS[name]
+    with_bwd = w.backward and not args.fwd_only
+    if args.impl == "reference":
+        run_reference(args, w, with_bwd)
+    else:
+        run_ours(args, w, with_bwd)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+"""Python binding of the C ABI in include/od_attn.h (argument marshalling only).
+
+Tensors are torch CUDA tensors: Q, O, dO, dQ [B,T,S,Hq,D] bf16; K, V, dK, dV
+[B,T,S,Hkv,D] bf16; LSE [B,T,S,Hq] fp32.  Every call enqueues on the current torch
+stream (or the `stream` given) and returns without synchronising.  All computation
+happens in the CUDA library; there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+_LIB_PATH = os.path.join(_PKG, "libod_attn.so")
+_HEADER = os.path.join(_ROOT, "include", "od_attn.h")
+_lock = threading.Lock()
+_lib = None
+
+# kernels one backward call launches (row statistics, main kernel, dQ conversion)
+BWD_LAUNCHES = 3
+
+STATUS = {0: "OD_OK", 1: "OD_ERR_INVALID_ARG", 2: "OD_ERR_UNSUPPORTED", 3: "OD_ERR_CUDA",
+          4: "OD_ERR_TIMEOUT", 5: "OD_ERR_WORKSPACE"}
+
+
+class ODError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = code
+        super().__init__("%s: %s%s" % (what, STATUS.get(code, code),
+                                       "" if _lib is None else
+                                       " (%s)" % _lib.od_status_string(code).decode()))
+
+
+def _declared_symbols():
+    src = open(_HEADER).read()
+    return re.findall(r"^\s*(?:od_status|size_t|const char\*)\s+(od_\w+)\s*\(", src, re.M)
+
+
+EXPORTED_SYMBOLS = tuple(_declared_symbols()) if os.path.exists(_HEADER) else ()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library():
+    """Load libod_attn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ODError(3, "libod_attn.so is not built (run __graft_entry__.build())")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            fwd = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+            bwd = [P] * 12 + [I] * 7 + [F, P, Z, P]
+            for name, args in (("od_space_attn_fwd", fwd), ("od_time_attn_fwd", fwd),
+                               ("od_space_attn_bwd", bwd), ("od_time_attn_bwd", bwd)):
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = I
+            lib.od_attn_bwd_workspace_bytes.argtypes = [I] * 7
+            lib.od_attn_bwd_workspace_bytes.restype = Z
+            lib.od_get_device_status.argtypes = [P]
+            lib.od_get_device_status.restype = I
+            lib.od_status_string.argtypes = [I]
+            lib.od_status_string.restype = ctypes.c_char_p
+            lib.od_version.argtypes = []
+            lib.od_version.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError("%s must be a CUDA tensor" % name)
+        if t.dtype != torch.bfloat16:
+            raise TypeError("%s must be bfloat16" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+        if t.dim() != 5:
+            raise ValueError("%s must be [B,T,S,H,D]" % name)
+    if k.shape != v.shape or q.shape[:3] != k.shape[:3] or q.shape[4] != k.shape[4]:
+        raise ValueError("shape mismatch: q %s, k %s, v %s" % (tuple(q.shape), tuple(k.shape),
+                                                               tuple(v.shape)))
+    B, T, S, Hq, D = q.shape
+    return B, T, S, Hq, k.shape[3], D
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _fwd(name, q, k, v, extra, scale, out, lse, stream):
+    B, T, S, Hq, Hkv, D = _check_qkv(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, T, S, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if l.shape != (B, T, S, Hq) or l.dtype != torch.float32 or not l.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,T,S,Hq]")
+    st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, T, S, Hq,
+                                  Hkv, D, int(extra), float(scale), _stream(stream))
+    if st:
+        raise ODError(st, name)
+    return o, l
+
+
+def space_attn_fwd(q, k, v, agent_idx=-1, scale=None, out=None, lse=None, stream=None):
+    """Masked space attention forward -> (O bf16, LSE fp32)."""
+    return _fwd("od_space_attn_fwd", q, k, v, agent_idx, scale, out, lse, stream)
+
+
+def time_attn_fwd(q, k, v, window, scale=None, out=None, lse=None, stream=None):
+    """Sliding-window causal time attention forward -> (O bf16, LSE fp32)."""
+    return _fwd("od_time_attn_fwd", q, k, v, window, scale, out, lse, stream)
+
+
+def bwd_workspace_bytes(which, B, T, S, Hq, Hkv, D=64):
+    return int(library().od_attn_bwd_workspace_bytes(int(which), B, T, S, Hq, Hkv, D))
+
+
+def _bwd(name, which, q, k, v, o, lse, dout, extra, scale, fp32_grads, workspace, out, stream):
+    B, T, S, Hq, Hkv, D = _check_qkv(q, k, v)
+    for nm, t in (("o", o), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("%s must be a contiguous bf16 CUDA tensor shaped like q" % nm)
+    if lse.shape != (B, T, S, Hq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,T,S,Hq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = out
+    f32 = (None, None, None)
+    if fp32_grads:
+        f32 = (torch.empty(q.shape, dtype=torch.float32, device=q.device),
+               torch.empty(k.shape, dtype=torch.float32, device=q.device),
+               torch.empty(v.shape, dtype=torch.float32, device=q.device))
+    need = bwd_workspace_bytes(which, B, T, S, Hq, Hkv, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(f32[0]), _ptr(f32[1]),
+                                  _ptr(f32[2]), B, T, S, Hq, Hkv, D, int(extra), float(scale),
+                                  _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                  _stream(stream))
+    if st:
+        raise ODError(st, name)
+    if fp32_grads:
+        return dq, dk, dv, f32
+    return dq, dk, dv
+
+
+def space_attn_bwd(q, k, v, o, lse, dout, agent_idx=-1, scale=None, fp32_grads=False,
+                   workspace=None, out=None, stream=None):
+    """Space attention backward -> (dQ, dK, dV) bf16 [, (dQ, dK, dV) fp32]."""
+    return _bwd("od_space_attn_bwd", 0, q, k, v, o, lse, dout, agent_idx, scale, fp32_grads,
+                workspace, out, stream)
+
+
+def time_attn_bwd(q, k, v, o, lse, dout, window, scale=None, fp32_grads=False,
+                  workspace=None, out=None, stream=None):
+    """Time attention backward -> (dQ, dK, dV) bf16 [, (dQ, dK, dV) fp32]."""
+    return _bwd("od_time_attn_bwd", 1, q, k, v, o, lse, dout, window, scale, fp32_grads,
+                workspace, out, stream)
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status (0 = OK)."""
+    return int(library().od_get_device_status(_stream(stream)))

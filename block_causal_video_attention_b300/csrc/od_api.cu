@@ -1,0 +1,260 @@
+// od_api.cu -- host side of the C ABI declared in include/od_attn.h.
+//
+// Validates arguments, encodes the TMA tensor maps for the [B,T,S,H,D] tensors, sizes the
+// persistent grid to the SM count and launches on the caller's stream.  No allocation,
+// no synchronisation on the launch path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "od_attn.h"
+#include "od_fwd.cuh"
+#include "od_bwd.cuh"
+
+// Device status word: bit OD_DEV_TIMEOUT is set by any kernel whose bounded wait expired.
+__device__ unsigned int g_od_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned int* status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+od_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return OD_ERR_CUDA;
+    void* sp = nullptr;
+    if (cudaGetSymbolAddress(&sp, g_od_status) != cudaSuccess) return OD_ERR_CUDA;
+    d.status = static_cast<unsigned int*>(sp);
+    if (cudaFuncSetAttribute(od::od_attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(od::kFwdSmemBytes)) != cudaSuccess)
+      return OD_ERR_CUDA;
+    // The forward kernel redistributes its launch registers between warpgroups
+    // (setmaxnreg); that split is only valid for the register count it was designed for.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, od::od_attn_fwd_kernel) != cudaSuccess ||
+        fa.numRegs != od::kFwdLaunchRegs)
+      return OD_ERR_CUDA;
+    if (od::bwd_setup() != cudaSuccess) return OD_ERR_CUDA;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return OD_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return OD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+od_status check_shape(int B, int T, int S, int Hq, int Hkv, int D, float scale) {
+  if (B <= 0 || T <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return OD_ERR_INVALID_ARG;
+  if (Hq % Hkv) return OD_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return OD_ERR_INVALID_ARG;
+  if (D != 64) return OD_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 128) return OD_ERR_UNSUPPORTED;
+  const long long rows = 1LL * B * T * S;
+  // tensor-map coordinates are 32-bit and the element count of one tensor must stay
+  // addressable with 64-bit strides below 2^40 bytes
+  if (rows * Hq * D * 2 >= (1LL << 40)) return OD_ERR_UNSUPPORTED;
+  if (B > 65535 || T > (1 << 24) || S > (1 << 24) || Hq > 65535) return OD_ERR_UNSUPPORTED;
+  return OD_OK;
+}
+
+// 5-D tensor map over a [B,T,S,H,D] tensor of `elem` bytes per element.
+od_status make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem, int B,
+                   int T, int S, int H, int D, const uint32_t box[5],
+                   CUtensorMapSwizzle swizzle) {
+  cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)T,
+                        (cuuint64_t)B};
+  cuuint64_t strides[4];
+  strides[0] = (cuuint64_t)D * elem;
+  strides[1] = strides[0] * H;
+  strides[2] = strides[1] * S;
+  strides[3] = strides[2] * T;
+  cuuint32_t bx[5] = {box[0], box[1], box[2], box[3], box[4]};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(m, dt, 5, const_cast<void*>(ptr), dims, strides, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? OD_OK : OD_ERR_CUDA;
+}
+
+od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int T, int S, int Hq, int Hkv, int D, int agent, int window,
+                     float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return OD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return OD_ERR_INVALID_ARG;
+  od_status st = check_shape(B, T, S, Hq, Hkv, D, scale);
+  if (st != OD_OK) return st;
+  if (is_time) {
+    if (window < 1) return OD_ERR_INVALID_ARG;
+  } else {
+    if (agent < -1 || agent >= S) return OD_ERR_INVALID_ARG;
+  }
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != OD_OK) return st;
+
+  od::FwdParams p{};
+  p.B = B; p.T = T; p.S = S; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv;
+  p.is_time = is_time;
+  p.L = is_time ? T : S;
+  p.F = is_time ? S : T;
+  p.agent = is_time ? -1 : agent;
+  p.window = is_time ? window : 1;
+  p.sl = scale * 1.4426950408889634f;
+  p.nTok = od::kBM / p.G;
+  p.rows = p.nTok * p.G;
+  p.ntiles = (p.L + p.nTok - 1) / p.nTok;
+  p.npairs = (p.ntiles + 1) / 2;
+  p.nitems = 1LL * B * p.F * Hkv * p.npairs;
+  p.nkb = (p.L + od::kBN - 1) / od::kBN;
+  p.resident = p.nkb <= od::kStages;
+  p.lse = lse;
+  p.status = dev->status;
+
+  const uint32_t qbox_space[5] = {64, (uint32_t)p.G, (uint32_t)p.nTok, 1, 1};
+  const uint32_t qbox_time[5] = {64, (uint32_t)p.G, 1, (uint32_t)p.nTok, 1};
+  const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kBN, 1, 1};
+  const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kBN, 1};
+  CUtensorMap tq, tk, tv, to;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, is_time ? qbox_time : qbox_space, sw)) ||
+      (st = make_map(&to, o, bf, 2, B, T, S, Hq, D, is_time ? qbox_time : qbox_space, sw)) ||
+      (st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw)) ||
+      (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw)))
+    return st;
+
+  const long long grid = p.nitems < dev->num_sms ? p.nitems : dev->num_sms;
+  od::od_attn_fwd_kernel<<<(unsigned)grid, od::kFwdThreads, od::kFwdSmemBytes,
+                           static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, p);
+  return cudaGetLastError() == cudaSuccess ? OD_OK : OD_ERR_CUDA;
+}
+
+od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S, int Hq,
+                     int Hkv, int D, int agent, int window, float scale, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return OD_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return OD_ERR_INVALID_ARG;
+  od_status st = check_shape(B, T, S, Hq, Hkv, D, scale);
+  if (st != OD_OK) return st;
+  if (is_time) {
+    if (window < 1) return OD_ERR_INVALID_ARG;
+  } else {
+    if (agent < -1 || agent >= S) return OD_ERR_INVALID_ARG;
+  }
+  if (workspace_bytes < od::bwd_workspace_bytes(B, T, S, Hq, D)) return OD_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != OD_OK) return st;
+  od::BwdArgs a;
+  a.is_time = is_time;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout; a.lse = lse;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dq_f32 = dq_f32; a.dk_f32 = dk_f32; a.dv_f32 = dv_f32;
+  a.B = B; a.T = T; a.S = S; a.Hq = Hq; a.Hkv = Hkv; a.D = D;
+  a.agent = is_time ? -1 : agent;
+  a.window = is_time ? window : 1;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = dev->status;
+  a.num_sms = dev->num_sms;
+  const int r = od::launch_bwd(a);
+  return r == 0 ? OD_OK : (r == 2 ? OD_ERR_UNSUPPORTED : OD_ERR_CUDA);
+}
+
+}  // namespace
+
+extern "C" {
+
+od_status od_space_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                            float scale, void* stream) {
+  return launch_fwd(0, q, k, v, o, lse, B, T, S, Hq, Hkv, D, agent_idx, 1, scale, stream);
+}
+
+od_status od_time_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
+                           void* stream) {
+  return launch_fwd(1, q, k, v, o, lse, B, T, S, Hq, Hkv, D, -1, window, scale, stream);
+}
+
+size_t od_attn_bwd_workspace_bytes(int which, int B, int T, int S, int Hq, int Hkv, int D) {
+  if ((which != 0 && which != 1) || check_shape(B, T, S, Hq, Hkv, D, 1.f) != OD_OK) return 0;
+  return od::bwd_workspace_bytes(B, T, S, Hq, D);
+}
+
+od_status od_space_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S,
+                            int Hq, int Hkv, int D, int agent_idx, float scale, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  return launch_bwd(0, q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
+                    Hkv, D, agent_idx, 1, scale, workspace, workspace_bytes, stream);
+}
+
+od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                           float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S,
+                           int Hq, int Hkv, int D, int window, float scale, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  return launch_bwd(1, q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
+                    Hkv, D, -1, window, scale, workspace, workspace_bytes, stream);
+}
+
+od_status od_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return OD_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_od_status, sizeof(v)) != cudaSuccess) return OD_ERR_CUDA;
+  if (v) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_od_status, &zero, sizeof(zero)) != cudaSuccess) return OD_ERR_CUDA;
+  }
+  return (v & OD_DEV_TIMEOUT) ? OD_ERR_TIMEOUT : OD_OK;
+}
+
+const char* od_status_string(od_status s) {
+  switch (s) {
+    case OD_OK: return "ok";
+    case OD_ERR_INVALID_ARG: return "invalid argument";
+    case OD_ERR_UNSUPPORTED: return "unsupported shape or head dimension";
+    case OD_ERR_CUDA: return "CUDA error";
+    case OD_ERR_TIMEOUT: return "device-side wait timed out";
+    case OD_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+const char* od_version(void) { return "od_attn 0.1 (sm_103a)"; }
+
+}  // extern "C"

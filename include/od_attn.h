@@ -1,0 +1,115 @@
+/*
+ * od_attn.h -- C ABI of the block-causal video attention library (B300, sm_103a).
+ *
+ * Two attention operators of the block-causal transformer backbone that the Open
+ * Dreamer tokenizer and dynamics model share (7minutos.es page, section
+ * "Arquitectura: una columna vertebral, dos modelos"; edgex es-LA page, section
+ * "Arquitectura"): space attention inside one timestep block, where world-model tokens
+ * cannot read the agent token, and causal time attention across timesteps at each token
+ * position, limited to a sliding window (192 steps in the Minecraft configuration, edgex
+ * es-LA page, section "Configuracion de entrenamiento"), with grouped-query heads
+ * (30 query heads sharing 3 KV heads in that configuration).
+ *
+ * Notation: B batch, T timesteps, S tokens per timestep block, Hq query heads, Hkv KV
+ * heads, G = Hq / Hkv, D head dimension (64), W time window, a agent token index
+ * (-1 = none), scale = softmax scale (1/sqrt(D) in the pages' configs).
+ * Query head h reads KV head floor(h / G).
+ *
+ * Space attention, for each (b, t, h) and query token s:
+ *   keys s' of the same (b, t), except s' = a when s != a (the agent reads everything).
+ * Time attention, for each (b, s, h) and query step t:
+ *   keys t' of the same (b, s) with max(0, t - W + 1) <= t' <= t (W keys including t).
+ * Per query row with logits l_j = scale * <q, k_j> over its allowed keys:
+ *   LSE = ln sum_j exp(l_j),  O = sum_j exp(l_j - LSE) v_j.
+ * Backward: dV_j += p_j dO, dP_j = <dO, v_j>, dS_j = p_j (dP_j - <dO, O>),
+ *   dQ = scale sum_j dS_j k_j, dK_j += scale dS_j q, with dK and dV summed over the G
+ *   query heads of a group.
+ *
+ * Layouts (row-major, contiguous, caller-owned device memory):
+ *   Q, O, dO, dQ : [B, T, S, Hq, D]  bf16 (raw __nv_bfloat16 bits)
+ *   K, V, dK, dV : [B, T, S, Hkv, D] bf16
+ *   LSE          : [B, T, S, Hq]     fp32, natural log
+ * Mixed precision follows the pages' stability notes (bf16 attention inputs, fp32
+ * statistics; edgex es-LA page, section "Ingenieria de estabilidad", item 3): inputs and
+ * outputs bf16, accumulation and softmax statistics fp32.
+ *
+ * Calls are asynchronous: they validate their arguments on the host, enqueue kernels on
+ * `stream` (a cudaStream_t passed as void*, NULL = legacy default stream) and return.
+ * They never synchronise, allocate or free.  Outputs are fully overwritten (never
+ * accumulated into).  Every device pointer must be 16-byte aligned.
+ *
+ * Errors: OD_ERR_INVALID_ARG for a null pointer, a non-positive size, Hq % Hkv != 0,
+ * agent outside [-1, S), window < 1, a misaligned pointer, a scale that is not finite and
+ * positive, or a workspace that is too small; OD_ERR_UNSUPPORTED for D != 64, G > 128 or
+ * sizes beyond 32-bit tensor coordinates; OD_ERR_CUDA when a CUDA call or a launch
+ * fails.  Nothing is enqueued when an error is returned.  Device-side timeouts (a bounded
+ * wait that gave up) are reported later by od_get_device_status.
+ */
+#ifndef OD_ATTN_H
+#define OD_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OD_OK = 0,
+  OD_ERR_INVALID_ARG = 1,
+  OD_ERR_UNSUPPORTED = 2,
+  OD_ERR_CUDA = 3,
+  OD_ERR_TIMEOUT = 4,
+  OD_ERR_WORKSPACE = 5
+} od_status;
+
+/* Space attention forward.  Writes O [B,T,S,Hq,D] (bf16) and LSE [B,T,S,Hq] (fp32). */
+od_status od_space_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                            float scale, void* stream);
+
+/* Time attention forward (window >= 1; keys t-window+1 .. t).  Writes O and LSE. */
+od_status od_time_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int T, int S, int Hq, int Hkv, int D, int window,
+                           float scale, void* stream);
+
+/* Space attention backward.  Inputs: Q, K, V, the forward's O and LSE, and dO.  Outputs
+ * dQ [B,T,S,Hq,D], dK and dV [B,T,S,Hkv,D] in bf16 (overwritten).  `workspace` is
+ * caller-owned device scratch of at least od_attn_bwd_workspace_bytes(0, ...) bytes
+ * (fp32 row statistics and the fp32 dQ accumulator); its contents on entry do not matter.
+ * If dq_f32/dk_f32/dv_f32 are non-NULL, the gradients are also written there in fp32
+ * (same layouts), before rounding to bf16. */
+od_status od_space_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S,
+                            int Hq, int Hkv, int D, int agent_idx, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Time attention backward; as od_space_attn_bwd with `window` in place of agent_idx. */
+od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                           float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S,
+                           int Hq, int Hkv, int D, int window, float scale, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace the backward needs (which: 0 = space, 1 = time). Returns 0
+ * for invalid sizes. */
+size_t od_attn_bwd_workspace_bytes(int which, int B, int T, int S, int Hq, int Hkv, int D);
+
+/* Synchronises `stream`, then reads and clears the device status word of the current
+ * device.  Returns OD_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * call, OD_ERR_CUDA if the synchronisation failed, OD_OK otherwise. */
+od_status od_get_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* od_status_string(od_status s);
+
+/* Library version string. */
+const char* od_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OD_ATTN_H */

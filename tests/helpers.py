@@ -1,0 +1,37 @@
+"""Shared test helpers: seeded inputs on both sides, comparison against the oracle."""
+import numpy as np
+import torch
+
+from block_causal_video_attention_b300 import synth
+
+MAX_ERR = 1e-2      # max |gpu - oracle| for O (and fp32 gradients)
+MEAN_REL = 2e-3     # mean |gpu - oracle| / mean |oracle|
+LSE_ERR = 1e-3      # max |gpu - oracle| for the logsumexp
+
+
+def to_dev(bits):
+    """uint16 bf16 bit patterns (numpy) -> CUDA bf16 tensor."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def to_f64(t):
+    """CUDA tensor (bf16 or fp32) -> float64 numpy."""
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def inputs(B, T, S, Hq, Hkv, seed, with_dout=False):
+    w = synth.custom(B, T, S, Hq, Hkv, seed=seed)
+    return synth.make_inputs(w, with_dout=with_dout)
+
+
+def errors(gpu, ref):
+    d = np.abs(gpu - ref)
+    return float(d.max()), float(d.mean() / max(np.abs(ref).mean(), 1e-30))
+
+
+def assert_close(gpu, ref, what, max_err=MAX_ERR, mean_rel=MEAN_REL):
+    assert np.isfinite(gpu).all(), "%s: non-finite values" % what
+    m, r = errors(gpu, ref)
+    assert m <= max_err and r <= mean_rel, "%s: max|err| %.3g (<= %.3g), mean rel %.3g (<= %.3g)" % (
+        what, m, max_err, r, mean_rel)
+    return m, r

@@ -1,0 +1,86 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared symbol,
+and rejects invalid arguments before touching the device."""
+import ctypes
+import re
+
+import pytest
+
+from block_causal_video_attention_b300 import api
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_causal_video_attention_b300 import build
+    build.build()
+    return api.library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    src = open(api._HEADER).read()
+    declared = set(re.findall(r"\b(od_\w+)\s*\(", src))
+    assert {"od_space_attn_fwd", "od_time_attn_fwd", "od_space_attn_bwd", "od_time_attn_bwd",
+            "od_attn_bwd_workspace_bytes", "od_get_device_status", "od_status_string",
+            "od_version"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(api.EXPORTED_SYMBOLS) == declared
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.od_status_string(code)
+    assert b"sm_103a" in lib.od_version()
+
+
+P = ctypes.c_void_p
+GOOD = P(4096)  # aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("fn", ["od_space_attn_fwd", "od_time_attn_fwd"])
+def test_forward_rejects_invalid_arguments(lib, fn):
+    f = getattr(lib, fn)
+    extra_ok = 0 if fn == "od_space_attn_fwd" else 4
+    base = dict(B=1, T=4, S=8, Hq=4, Hkv=2, D=64, extra=extra_ok, scale=0.125)
+
+    def call(ptrs=None, **kw):
+        a = dict(base, **kw)
+        q, k, v, o, l = ptrs or (GOOD, GOOD, GOOD, GOOD, GOOD)
+        return f(q, k, v, o, l, a["B"], a["T"], a["S"], a["Hq"], a["Hkv"], a["D"], a["extra"],
+                 a["scale"], P(0))
+    assert call(ptrs=(P(0), GOOD, GOOD, GOOD, GOOD)) == 1
+    assert call(ptrs=(GOOD, GOOD, GOOD, P(4097), GOOD)) == 1      # misaligned
+    assert call(B=0) == 1
+    assert call(S=-3) == 1
+    assert call(Hq=5, Hkv=2) == 1                                  # Hq % Hkv
+    assert call(scale=float("nan")) == 1
+    assert call(scale=-0.1) == 1
+    assert call(D=128) == 2                                         # unsupported head dim
+    assert call(Hq=258, Hkv=1) == 2                                 # group too large
+    if fn == "od_space_attn_fwd":
+        assert call(extra=8) == 1 and call(extra=-2) == 1           # agent index out of range
+    else:
+        assert call(extra=0) == 1                                   # window < 1
+
+
+@pytest.mark.parametrize("fn", ["od_space_attn_bwd", "od_time_attn_bwd"])
+def test_backward_rejects_invalid_arguments(lib, fn):
+    f = getattr(lib, fn)
+    extra = 0 if fn == "od_space_attn_bwd" else 4
+    ptrs = [GOOD] * 9 + [P(0)] * 3
+    ws = lib.od_attn_bwd_workspace_bytes(0 if "space" in fn else 1, 1, 4, 8, 4, 2, 64)
+    assert ws > 0
+    assert f(*ptrs, 1, 4, 8, 4, 2, 64, extra, 0.125, GOOD, ws - 16, P(0)) == 5  # too small
+    bad = list(ptrs)
+    bad[5] = P(0)                                                   # null dO
+    assert f(*bad, 1, 4, 8, 4, 2, 64, extra, 0.125, GOOD, ws, P(0)) == 1
+    assert f(*ptrs, 1, 4, 8, 4, 3, 64, extra, 0.125, GOOD, ws, P(0)) == 1           # Hq % Hkv
+    assert lib.od_attn_bwd_workspace_bytes(2, 1, 4, 8, 4, 2, 64) == 0
+    assert lib.od_attn_bwd_workspace_bytes(0, 1, 4, 8, 4, 3, 64) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 2, 3, 4, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 3, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        api.space_attn_fwd(q, k, k, agent_idx=-1)
