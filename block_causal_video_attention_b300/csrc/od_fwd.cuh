@@ -18,7 +18,7 @@
 //   warps 4-7   softmax warpgroup for Q tile B
 //   warp  8     TMA producer (one thread)
 //   warp  9     TMEM allocator + tcgen05.mma issuer (one thread)
-//   warps 10-11 idle
+//   warps 10-11 convert each V tile to fp16 in shared memory (P V runs in fp16)
 // The kernel launches with kFwdLaunchRegs registers per thread; the softmax warpgroups
 // then raise their limit to kFwdSoftmaxRegs and the control warpgroup lowers its own to
 // kFwdCtrlRegs.  2*128*kFwdSoftmaxRegs + 128*kFwdCtrlRegs equals the launch allocation, and
@@ -75,7 +75,9 @@ struct FwdSmem {
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2], p_full[2], o_done[2];
   uint64_t st_full[2], st_free[2];
+  uint64_t v16_ready[kStages];
   uint64_t drain;
+  uint8_t vfmt[kStages][4];  // per 32-key chunk of a V stage: 0 = fp16, 1 = bf16
   uint32_t tmem_base;
   Ctl ctl;
 };
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v16_ready[s], 2);
       mbar_init(&sm.kv_empty[s], 1);
     }
     mbar_init(&sm.drain, 1);
@@ -296,7 +299,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t tS[2] = {tmem + 0, tmem + 128};
       const uint32_t tP[2] = {tmem + 256, tmem + 320};
       const uint32_t tO[2] = {tmem + 384, tmem + 448};
-      const uint32_t idesc_pv = idesc_bf16(128, 64, 0, 1);
+      const uint32_t idesc_pv_bf16 = idesc_bf16(128, 64, 0, 1);
+      const uint32_t idesc_pv_fp16 = idesc_fp16(128, 64, 0, 1);
       long long prev_unit = -1;
       uint32_t unit_loads = 0, stream_cnt = 0, qn[2] = {0, 0}, jS[2] = {0, 0}, jP[2] = {0, 0};
       bool ok = true;
@@ -333,13 +337,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         };
         auto issue_pv = [&](int x, int bi) -> bool {
           const KvSlot ks = kv_slot(p, it, bi, unit_loads, stream_cnt);
-          if (!wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status)) return false;
+          if (!wait_bar(&sm.v16_ready[ks.stage], ks.parity, ctl, status)) return false;
           if (!wait_bar(&sm.p_full[x], jP[x] & 1u, ctl, status)) return false;
           tc_fence_after();
           const int ksteps = round16(block_ncols(it, it.kb_lo + bi)) >> 4;
-          const uint64_t b = sdesc_sw128(smem_u32(sV + ks.stage * kTile), 16, 1024);
-          for (int k = 0; k < ksteps; ++k)
-            mma_ts(tO[x], tP[x] + 8 * k, b + (2048 >> 4) * k, idesc_pv, (bi > 0 || k > 0));
+          const uint64_t b = sdesc_sw128(smem_u32(sV + ks.stage * kTile), 1024, 1024);
+          for (int k = 0; k < ksteps; ++k) {
+            const uint32_t idesc = sm.vfmt[ks.stage][k >> 1] ? idesc_pv_bf16 : idesc_pv_fp16;
+            mma_ts(tO[x], tP[x] + 8 * k, b + (2048 >> 4) * k, idesc, (bi > 0 || k > 0));
+          }
           mma_commit(&sm.o_done[x]);
           ++jP[x];
           return true;
@@ -363,6 +369,71 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mma_commit(&sm.drain);
       drain_wait(&sm.drain, 0);
     }
+   } else {
+    // ------------------------------------------------------------ V converter (warps 10-11)
+    // P V runs in fp16: P in [0, 256] loses 8x less to rounding than in bf16.  Each fill
+    // of a V stage is converted in place, per 32-key chunk, when the chunk's magnitude
+    // is inside a safe fp16 range (2^-10 <= max|v| <= 2^15, or all zero); otherwise the
+    // chunk stays bf16 and the softmax and MMA use bf16 for those keys.
+    const int cw = warp - 10;
+    long long prev_unit = -1;
+    uint32_t unit_loads = 0, stream_cnt = 0;
+    bool ok = true;
+    auto convert = [&](int stage, uint32_t parity) -> bool {
+      bool w = wait_bar(&sm.v_full[stage], parity, ctl, status);
+      if (!__all_sync(0xffffffffu, w)) return false;
+#pragma unroll 1
+      for (int cc = 2 * cw; cc < 2 * cw + 2; ++cc) {
+        uint4* chunk = reinterpret_cast<uint4*>(sV + stage * kTile + cc * 32 * 128);
+        float mx = 0.f;
+#pragma unroll 2
+        for (int j = 0; j < 8; ++j) {
+          const uint4 d = chunk[lane + 32 * j];
+          const uint32_t wv[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            mx = fmaxf(mx, fabsf(__uint_as_float(wv[h] << 16)));
+            mx = fmaxf(mx, fabsf(__uint_as_float(wv[h] & 0xFFFF0000u)));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const bool fp16_ok = (mx == 0.f) || (mx >= 0.0009765625f && mx <= 32768.f);
+        if (fp16_ok) {
+#pragma unroll 2
+          for (int j = 0; j < 8; ++j) {
+            const uint4 d = chunk[lane + 32 * j];
+            uint32_t wv[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+              wv[h] = pack_f16x2(__uint_as_float(wv[h] << 16), __uint_as_float(wv[h] & 0xFFFF0000u));
+            chunk[lane + 32 * j] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
+        if (lane == 0) sm.vfmt[stage][cc] = fp16_ok ? 0 : 1;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.v16_ready[stage]);
+      return true;
+    };
+    for (long long i = i0; i < i1 && ok; ++i) {
+      const FwdItem it = fwd_decode(p, i);
+      if (p.resident) {
+        if (it.unit != prev_unit) {
+          ++unit_loads;
+          prev_unit = it.unit;
+          for (int st = 0; st < p.nkb && ok; ++st) ok = convert(st, (unit_loads - 1) & 1u);
+        }
+      } else {
+        const int nb = it.kb_hi - it.kb_lo + 1;
+        for (int bi = 0; bi < nb && ok; ++bi) {
+          const uint32_t c = stream_cnt + bi;
+          ok = convert(static_cast<int>(c % kStages), (c / kStages) & 1u);
+        }
+        stream_cnt += nb;
+      }
+    }
    }
   } else {
     regs_inc<kFwdSoftmaxRegs>();
@@ -377,9 +448,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int tok = r / G;
     const int g = r - tok * G;
     uint32_t jS = 0, jP = 0, e = 0;
+    long long prev_unit = -1;
+    uint32_t unit_loads = 0, stream_next = 0;
     bool ok = true;
     for (long long i = i0; i < i1 && ok; ++i) {
       const FwdItem it = fwd_decode(p, i);
+      if (p.resident && it.unit != prev_unit) {
+        ++unit_loads;
+        prev_unit = it.unit;
+      }
+      const uint32_t stream_cnt = stream_next;
+      stream_next += it.kb_hi - it.kb_lo + 1;
       if (x == 1 && !it.validB) continue;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
       const int pos = mytok0 + tok;
@@ -465,16 +544,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+        // V of this block must be converted before P's format can be chosen
+        const KvSlot ks = kv_slot(p, it, bi, unit_loads, stream_cnt);
+        ok = wait_bar(&sm.v16_ready[ks.stage], ks.parity, ctl, status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           if (c < nch) {
+            const bool as_bf16 = sm.vfmt[ks.stage][c] != 0;
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
               const float p0 = ex2(fmaf(s[32 * c + j], p.sl, -msub));
               const float p1 = ex2(fmaf(s[32 * c + j + 1], p.sl, -msub));
               l += p0 + p1;
-              pk[j >> 1] = pack_bf16x2(p0, p1);
+              pk[j >> 1] = as_bf16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
             }
             tmem_st16(tP + 16 * c, pk);
           }

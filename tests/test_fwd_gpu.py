@@ -161,3 +161,23 @@ def test_full_size_sampled_units(oracle_mod, name):
                 gl = to_f64(lse[b:b+1, :, f:f+1, hs])
             assert_close(go, ro, "%s %s unit %s" % (name, kind, (b, f, h)))
             assert np.abs(gl - rl).max() <= LSE_ERR
+
+
+@pytest.mark.parametrize("vscale", [2.0 ** 17, 2.0 ** -14])
+def test_v_outside_fp16_range_uses_bf16(oracle_mod, vscale):
+    """V chunks whose magnitude is outside the safe fp16 range fall back to bf16 P V.
+    Keys 32..63 of every frame are scaled; the rest stay N(0,1).  Errors are measured
+    relative to the output scale.  The fallback carries bf16 accuracy for P (8 significant
+    bits): with |v| ~ 1e5 the worst element is ~3% of mean|O| in an exact simulation of
+    bf16-P arithmetic, so it is held to 5e-2 (worst) and 3e-3 (mean) of mean|O|."""
+    B, T, S, Hq, Hkv = 1, 4, 70, 4, 2
+    q, k, v = inputs(B, T, S, Hq, Hkv, seed=31)
+    vf = oracle_mod.from_bf16(v)
+    vf[:, :, 32:64] *= vscale
+    v2 = synth.f64_to_bf16_bits(vf)
+    go, gl, ro, rl = run_both(oracle_mod, "space", (q, k, v2), 5)
+    sc = np.abs(ro).mean()
+    assert np.isfinite(go).all()
+    assert np.abs(go - ro).max() / sc <= 5e-2
+    assert np.abs(go - ro).mean() / sc <= 3e-3
+    assert np.abs(gl - rl).max() <= LSE_ERR
