@@ -85,10 +85,13 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()
+            while not self.rows and time.time() - t0 < 5.0:   # wait for the first sample
+                time.sleep(0.02)
         except OSError:
             self.proc = None
         return self
@@ -246,6 +249,7 @@ def run_ours(args, w, with_bwd):
             timed("time_bwd", lambda: api.time_attn_bwd(Q, K, V, o_t, l_t, DO, w.window, w.scale,
                                                         workspace=ws_t, out=g[3:], stream=stream))
 
+    clk = Clocks(local).__enter__()
     for _ in range(args.warmup):
         step(False)
     torch.cuda.synchronize()
@@ -255,12 +259,11 @@ def run_ours(args, w, with_bwd):
         dist.barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
-        start.record(stream)
-        for _ in range(args.steps):
-            step(True)
-        end.record(stream)
-        torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    end.record(stream)
+    torch.cuda.synchronize()
     ms = start.elapsed_time(end)
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -302,6 +305,7 @@ def run_ours(args, w, with_bwd):
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b)
+    clk.__exit__()
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -360,7 +364,7 @@ def run_ours(args, w, with_bwd):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None)

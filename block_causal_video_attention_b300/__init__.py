@@ -13,7 +13,7 @@ from __future__ import annotations
 
 _API = (
     "space_attn_fwd", "space_attn_bwd", "time_attn_fwd", "time_attn_bwd",
-    "bwd_workspace_bytes", "get_device_status", "library", "library_path",
+    "bwd_workspace_bytes", "get_device_status", "get_device_status_detail", "library", "library_path",
     "ODError", "EXPORTED_SYMBOLS",
 )
 

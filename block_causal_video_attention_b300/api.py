@@ -69,6 +69,8 @@ def library():
             lib.od_attn_bwd_workspace_bytes.restype = Z
             lib.od_get_device_status.argtypes = [P]
             lib.od_get_device_status.restype = I
+            lib.od_get_device_status_detail.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+            lib.od_get_device_status_detail.restype = I
             lib.od_status_string.argtypes = [I]
             lib.od_status_string.restype = ctypes.c_char_p
             lib.od_version.argtypes = []
@@ -185,3 +187,10 @@ def time_attn_bwd(q, k, v, o, lse, dout, window, scale=None, fp32_grads=False,
 def get_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status (0 = OK)."""
     return int(library().od_get_device_status(_stream(stream)))
+
+
+def get_device_status_detail(stream=None):
+    """(status, site word) -- the site word names the first expired wait (0 if none)."""
+    w = ctypes.c_uint(0)
+    st = library().od_get_device_status_detail(_stream(stream), ctypes.byref(w))
+    return int(st), int(w.value)

@@ -16,8 +16,9 @@
 #include "od_fwd.cuh"
 #include "od_bwd.cuh"
 
-// Device status word: bit OD_DEV_TIMEOUT is set by any kernel whose bounded wait expired.
-__device__ unsigned int g_od_status;
+// Device status words: [0] has bit OD_DEV_TIMEOUT set by any kernel whose bounded wait
+// expired; [1] holds the first such wait's site word (site << 24 | parity << 23 | block).
+__device__ unsigned int g_od_status[2];
 
 namespace {
 
@@ -132,6 +133,7 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   p.ntiles = (p.L + p.nTok - 1) / p.nTok;
   p.npairs = (p.ntiles + 1) / 2;
   p.nitems = 1LL * B * p.F * Hkv * p.npairs;
+  if (p.nitems >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
   p.nkb = (p.L + od::kBN - 1) / od::kBN;
   p.resident = p.nkb <= od::kStages;
   p.lse = lse;
@@ -141,18 +143,18 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   const uint32_t qbox_time[5] = {64, (uint32_t)p.G, 1, (uint32_t)p.nTok, 1};
   const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kBN, 1, 1};
   const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kBN, 1};
-  CUtensorMap tq, tk, tv, to;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  CUtensorMap tq, tk, tv;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, is_time ? qbox_time : qbox_space, sw)) ||
-      (st = make_map(&to, o, bf, 2, B, T, S, Hq, D, is_time ? qbox_time : qbox_space, sw)) ||
       (st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw)) ||
       (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw)))
     return st;
 
   const long long grid = p.nitems < dev->num_sms ? p.nitems : dev->num_sms;
   od::od_attn_fwd_kernel<<<(unsigned)grid, od::kFwdThreads, od::kFwdSmemBytes,
-                           static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, p);
+                           static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? OD_OK : OD_ERR_CUDA;
 }
 
@@ -232,16 +234,19 @@ od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const vo
                     Hkv, D, -1, window, scale, workspace, workspace_bytes, stream);
 }
 
-od_status od_get_device_status(void* stream) {
+od_status od_get_device_status_detail(void* stream, unsigned int* site_word) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return OD_ERR_CUDA;
-  unsigned int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_od_status, sizeof(v)) != cudaSuccess) return OD_ERR_CUDA;
-  if (v) {
-    const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(g_od_status, &zero, sizeof(zero)) != cudaSuccess) return OD_ERR_CUDA;
+  unsigned int v[2] = {0, 0};
+  if (cudaMemcpyFromSymbol(v, g_od_status, sizeof(v)) != cudaSuccess) return OD_ERR_CUDA;
+  if (v[0] || v[1]) {
+    const unsigned int zero[2] = {0, 0};
+    if (cudaMemcpyToSymbol(g_od_status, zero, sizeof(zero)) != cudaSuccess) return OD_ERR_CUDA;
   }
-  return (v & OD_DEV_TIMEOUT) ? OD_ERR_TIMEOUT : OD_OK;
+  if (site_word) *site_word = v[1];
+  return (v[0] & OD_DEV_TIMEOUT) ? OD_ERR_TIMEOUT : OD_OK;
 }
+
+od_status od_get_device_status(void* stream) { return od_get_device_status_detail(stream, nullptr); }
 
 const char* od_status_string(od_status s) {
   switch (s) {

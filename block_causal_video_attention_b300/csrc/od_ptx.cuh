@@ -55,34 +55,66 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// As mbar_try_wait, but the thread may sleep up to `ns` nanoseconds waiting for the phase.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 
 // Shared control block of a CTA: the abort flag every bounded wait checks.
 struct Ctl {
   volatile int abort;
 };
 
+// Record a timeout: status[0] |= OD_DEV_TIMEOUT; status[1] keeps the first site as
+// (site << 24) | (parity << 23) | block index.
+__device__ __forceinline__ void record_timeout(unsigned int* status, int site, uint32_t parity) {
+  atomicOr(status, OD_DEV_TIMEOUT);
+  atomicCAS(status + 1, 0u,
+            (static_cast<uint32_t>(site) << 24) | ((parity & 1u) << 23) | (blockIdx.x & 0x7FFFFFu));
+}
+
 // Wait until the phase with the given parity of `bar` has completed.  Returns false (and
 // leaves the CTA in abort mode) if the CTA was aborted or the wait exceeded the limit.
 __device__ __forceinline__ bool wait_bar_slow(uint32_t a, uint32_t parity, Ctl* ctl,
-                                           unsigned int* status) {
+                                           unsigned int* status, int site) {
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((i & 15u) == 15u) {
+    if (mbar_try_wait_sleep(a, parity, 20000u)) return true;
+    if ((i & 3u) == 3u) {
       if (ctl->abort) return false;
       if (globaltimer() - t0 > OD_WAIT_LIMIT_NS) {
         ctl->abort = 1;
-        atomicOr(status, OD_DEV_TIMEOUT);
+        record_timeout(status, site, parity);
         return false;
       }
     }
   }
 }
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl* ctl,
-                                         unsigned int* status) {
+                                         unsigned int* status, int site) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  return wait_bar_slow(a, parity, ctl, status);
+  return wait_bar_slow(a, parity, ctl, status, site);
 }
 
 // ---------------------------------------------------------------- proxies / fences
@@ -179,6 +211,25 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
+// Wait for this thread's outstanding TMEM loads; the 16 registers passed are tied to the
+// wait so the compiler cannot schedule their uses before it.
+__device__ __forceinline__ void tmem_wait_ld_dep16(float* v) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+        "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]),
+        "+f"(v[13]), "+f"(v[14]), "+f"(v[15])::"memory");
+}
+__device__ __forceinline__ void tmem_wait_ld_dep32(float* v) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+        "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]),
+        "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]),
+        "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]),
+        "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]),
+        "+f"(v[31])::"memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -199,6 +250,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
         "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+// 32 lanes x 32 bit, 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }
@@ -287,6 +350,11 @@ __device__ __forceinline__ void regs_dec() {
 }
 
 // ---------------------------------------------------------------- math
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

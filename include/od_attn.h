@@ -102,6 +102,11 @@ size_t od_attn_bwd_workspace_bytes(int which, int B, int T, int S, int Hq, int H
  * call, OD_ERR_CUDA if the synchronisation failed, OD_OK otherwise. */
 od_status od_get_device_status(void* stream);
 
+/* As od_get_device_status; if site_word is non-NULL it receives the first expired wait's
+ * site word since the last call (0 if none): bits 31-24 name the wait site inside the
+ * kernel, bit 23 the phase parity waited for, bits 22-0 the CTA index.  For diagnosis. */
+od_status od_get_device_status_detail(void* stream, unsigned int* site_word);
+
 /* Static description of a status code. */
 const char* od_status_string(od_status s);
 

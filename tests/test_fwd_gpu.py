@@ -27,7 +27,8 @@ def run_both(oracle_mod, kind, bits, extra, scale=0.125):
         ro, rl = oracle_mod.time_fwd(oracle_mod.from_bf16(q), oracle_mod.from_bf16(k),
                                      oracle_mod.from_bf16(v), extra, scale)
     torch.cuda.synchronize()
-    assert api.get_device_status() == 0
+    st, site = api.get_device_status_detail()
+    assert st == 0, "device timeout at site word %#x" % site
     return to_f64(o), to_f64(lse), ro, rl
 
 
@@ -53,7 +54,7 @@ SHAPES = [
     (1, 300, 3, 10, 1, 0, 192),    # G=10 time with 3 key blocks and a window edge
     (2, 70, 11, 8, 2, 5, 64),      # G=4
     (1, 33, 130, 2, 2, -1, 200),   # G=1, window >= T, no agent
-    (1, 4, 600, 4, 4, 599, 2),     # S > 4 key blocks: K/V streamed through the ring
+    (1, 4, 800, 4, 4, 799, 2),     # S > 7 key blocks: K/V streamed through the ring
     (3, 7, 1, 4, 2, 0, 1),         # S = 1 (agent reads itself only), W = 1
     (1, 1, 17, 16, 2, 0, 9),       # T = 1, agent at 0, G = 8
     (1, 260, 2, 128, 1, 1, 130),   # G = 128: one token per tile
