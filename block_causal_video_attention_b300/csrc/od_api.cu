@@ -191,8 +191,82 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = dev->status;
   a.num_sms = dev->num_sms;
-  const int r = od::launch_bwd(a);
-  return r == 0 ? OD_OK : (r == 2 ? OD_ERR_UNSUPPORTED : OD_ERR_CUDA);
+  cudaStream_t strm = a.stream;
+
+  // shapes shared by both gradient kernels (forward tiling)
+  od::FwdParams f{};
+  f.B = B; f.T = T; f.S = S; f.Hq = Hq; f.Hkv = Hkv; f.G = Hq / Hkv;
+  f.is_time = is_time;
+  f.L = is_time ? T : S;
+  f.F = is_time ? S : T;
+  f.agent = is_time ? -1 : agent;
+  f.window = is_time ? window : 1;
+  f.sl = scale * 1.4426950408889634f;
+  f.nTok = od::kBM / f.G;
+  f.rows = f.nTok * f.G;
+  f.ntiles = (f.L + f.nTok - 1) / f.nTok;
+  f.npairs = (f.ntiles + 1) / 2;
+  f.nitems = 1LL * B * f.F * Hkv * f.npairs;
+  f.nkb = (f.L + od::kBN - 1) / od::kBN;
+  f.resident = 0;
+  f.status = dev->status;
+  if (f.nitems >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
+
+  float* delta = static_cast<float*>(workspace);
+  const uint32_t qbox_space[5] = {64, (uint32_t)f.G, (uint32_t)f.nTok, 1, 1};
+  const uint32_t qbox_time[5] = {64, (uint32_t)f.G, 1, (uint32_t)f.nTok, 1};
+  const uint32_t* qbox = is_time ? qbox_time : qbox_space;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap tq, tdo, tk, tv;
+  if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, qbox, sw)) ||
+      (st = make_map(&tdo, dout, bf, 2, B, T, S, Hq, D, qbox, sw)))
+    return st;
+  {
+    const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kBN, 1, 1};
+    const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kBN, 1};
+    const uint32_t* kbox = is_time ? kbox_time : kbox_space;
+    if ((st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, kbox, sw)) ||
+        (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, kbox, sw)))
+      return st;
+    od::DqParams dp{};
+    dp.f = f;
+    dp.lse = lse;
+    dp.delta = delta;
+    dp.scale = scale;
+    dp.dq = static_cast<__nv_bfloat16*>(dq);
+    dp.dq_f32 = dq_f32;
+    const long long grid = f.nitems < dev->num_sms ? f.nitems : dev->num_sms;
+    // 1. Delta pass, 2. dQ
+    od::od_bwd_dq_kernel<true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+    if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
+    od::od_bwd_dq_kernel<false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+    if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
+  }
+  // 3. dK, dV
+  {
+    const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kKvBN, 1, 1};
+    const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kKvBN, 1};
+    const uint32_t* kbox = is_time ? kbox_time : kbox_space;
+    if ((st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, kbox, sw)) ||
+        (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, kbox, sw)))
+      return st;
+    od::KvParams kp{};
+    kp.f = f;
+    kp.lse = lse;
+    kp.delta = delta;
+    kp.scale = scale;
+    kp.nkb = (f.L + od::kKvBN - 1) / od::kKvBN;
+    kp.nitems = 1LL * B * f.F * Hkv * kp.nkb;
+    kp.dk = static_cast<__nv_bfloat16*>(dk);
+    kp.dv = static_cast<__nv_bfloat16*>(dv);
+    kp.dk_f32 = dk_f32;
+    kp.dv_f32 = dv_f32;
+    const long long grid = kp.nitems < dev->num_sms ? kp.nitems : dev->num_sms;
+    od::od_bwd_dkdv_kernel<<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
+    if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
+  }
+  return OD_OK;
 }
 
 }  // namespace

@@ -365,10 +365,21 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Split two floats into bf16 high parts (packed, returned) and bf16 residuals (packed into
+// *res): x = hi + lo to about 16 significant bits.
+__device__ __forceinline__ uint32_t split_bf16x2(float a, float b, uint32_t* res);
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+__device__ __forceinline__ uint32_t split_bf16x2(float a, float b, uint32_t* res) {
+  const uint32_t hi = pack_bf16x2(a, b);
+  const float ha = __uint_as_float(hi << 16);
+  const float hb = __uint_as_float(hi & 0xFFFF0000u);
+  *res = pack_bf16x2(a - ha, b - hb);
+  return hi;
 }
 
 }  // namespace od

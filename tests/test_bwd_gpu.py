@@ -1,0 +1,124 @@
+"""Backward parity: CUDA library vs the fp64 oracle.
+
+Gates (the fp32 gradient outputs carry the stated tolerance; bf16 outputs add one rounding):
+  fp32 dQ/dK/dV : max |err| <= 1e-2 and mean |err| / mean |ref| <= 2e-3
+  bf16 dQ/dK/dV : per element |err| <= max(1e-2, one bf16 ulp of |ref|), and
+                  mean |err| / mean |ref| <= 3e-3 (bf16 rounding of the output alone is ~1.4e-3)
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_causal_video_attention_b300 import api, synth
+from helpers import assert_close, inputs, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_bwd(oracle_mod, kind, bits, extra, scale=0.125):
+    q, k, v, do = bits
+    Q, K, V, DO = to_dev(q), to_dev(k), to_dev(v), to_dev(do)
+    X = oracle_mod.from_bf16
+    if kind == "space":
+        o, l = api.space_attn_fwd(Q, K, V, extra, scale)
+        dq, dk, dv, (fq, fk, fv) = api.space_attn_bwd(Q, K, V, o, l, DO, extra, scale, fp32_grads=True)
+        ref = oracle_mod.space_bwd(X(q), X(k), X(v), X(do), extra, scale)
+    else:
+        o, l = api.time_attn_fwd(Q, K, V, extra, scale)
+        dq, dk, dv, (fq, fk, fv) = api.time_attn_bwd(Q, K, V, o, l, DO, extra, scale, fp32_grads=True)
+        ref = oracle_mod.time_bwd(X(q), X(k), X(v), X(do), extra, scale)
+    torch.cuda.synchronize()
+    st, site = api.get_device_status_detail()
+    assert st == 0, "device timeout at site word %#x" % site
+    return (to_f64(dq), to_f64(dk), to_f64(dv)), (to_f64(fq), to_f64(fk), to_f64(fv)), ref[2:]
+
+
+def check_bwd(oracle_mod, kind, bits, extra, scale=0.125, what=""):
+    bf, f32, ref = run_bwd(oracle_mod, kind, bits, extra, scale)
+    for name, g, gb, r in zip(("dQ", "dK", "dV"), f32, bf, ref):
+        assert_close(g, r, "%s %s %s fp32" % (what, kind, name), bf16_out=False)
+        assert_close(gb, r, "%s %s %s bf16" % (what, kind, name), mean_rel=3e-3)
+
+
+def test_tiny_config_backward(oracle_mod):
+    w = synth.WORKLOADS["tiny"]
+    bits = synth.make_inputs(w, with_dout=True)
+    check_bwd(oracle_mod, "space", bits, w.agent, w.scale, "tiny")
+    check_bwd(oracle_mod, "time", bits, w.window, w.scale, "tiny")
+
+
+SHAPES = [
+    # B, T, S, Hq, Hkv, agent, window
+    (2, 9, 37, 6, 2, 36, 5),
+    (1, 5, 290, 30, 3, 289, 3),
+    (1, 300, 3, 10, 1, 0, 192),
+    (2, 70, 11, 8, 2, 5, 64),
+    (1, 33, 130, 2, 2, -1, 200),
+    (1, 3, 800, 4, 4, 799, 2),
+    (3, 7, 1, 4, 2, 0, 1),
+    (1, 1, 17, 16, 2, 0, 9),
+    (1, 140, 2, 128, 1, 1, 130),
+]
+
+
+@pytest.mark.parametrize("B,T,S,Hq,Hkv,agent,window", SHAPES)
+def test_backward_shapes(oracle_mod, B, T, S, Hq, Hkv, agent, window):
+    bits = inputs(B, T, S, Hq, Hkv, seed=7 * B + T + 3 * S, with_dout=True)
+    check_bwd(oracle_mod, "space", bits, agent, what=str((B, T, S, Hq, Hkv)))
+    check_bwd(oracle_mod, "time", bits, window, what=str((B, T, S, Hq, Hkv)))
+
+
+def test_backward_gradient_invariants_on_gpu():
+    """Keys no query reads get exactly zero gradient: the agent's K/V receive nothing from
+    world rows, and frames after t receive nothing from rows <= t."""
+    B, T, S, Hq, Hkv, a = 1, 6, 40, 4, 2, 39
+    q, k, v, do = (to_dev(x) for x in inputs(B, T, S, Hq, Hkv, seed=99, with_dout=True))
+    do2 = do.clone()
+    do2[:, :, a] = 0
+    o, l = api.space_attn_fwd(q, k, v, a)
+    dq, dk, dv = api.space_attn_bwd(q, k, v, o, l, do2, a)
+    assert torch.count_nonzero(dk[:, :, a]) == 0 and torch.count_nonzero(dv[:, :, a]) == 0
+    do3 = do.clone()
+    do3[:, 3:] = 0
+    o, l = api.time_attn_fwd(q, k, v, 4)
+    dq, dk, dv = api.time_attn_bwd(q, k, v, o, l, do3, 4)
+    assert torch.count_nonzero(dk[:, 3:]) == 0 and torch.count_nonzero(dv[:, 3:]) == 0
+    assert torch.count_nonzero(dq[:, 3:]) == 0
+
+
+@pytest.mark.parametrize("name", ["minecraft_fwd_bwd", "tokenizer_enc"])
+def test_backward_full_size_sampled_units(oracle_mod, name):
+    """Full-size backward (the bench's configuration): every gradient element is written and
+    finite; whole sampled units are checked against the oracle."""
+    w = synth.WORKLOADS[name]
+    q, k, v, do = synth.make_inputs(w, with_dout=True)
+    Q, K, V, DO = to_dev(q), to_dev(k), to_dev(v), to_dev(do)
+    G = w.G
+    X = oracle_mod.from_bf16
+    rng = np.random.default_rng(w.seed + 11)
+    for kind in ("space", "time"):
+        extra = w.agent if kind == "space" else w.window
+        fwd = api.space_attn_fwd if kind == "space" else api.time_attn_fwd
+        bwd = api.space_attn_bwd if kind == "space" else api.time_attn_bwd
+        o, l = fwd(Q, K, V, extra, w.scale)
+        grads = [torch.full_like(x, float("nan")) for x in (Q, K, V)]
+        dq, dk, dv, (fq, fk, fv) = bwd(Q, K, V, o, l, DO, extra, w.scale, fp32_grads=True, out=grads)
+        torch.cuda.synchronize()
+        st, site = api.get_device_status_detail()
+        assert st == 0, "device timeout at site word %#x" % site
+        for t_ in (dq, dk, dv, fq, fk, fv):
+            assert bool(torch.isfinite(t_).all())
+        F = w.T if kind == "space" else w.S
+        for _ in range(4):
+            b, f, h = int(rng.integers(w.B)), int(rng.integers(F)), int(rng.integers(w.Hkv))
+            hs = slice(h * G, (h + 1) * G)
+            if kind == "space":
+                sel_q = (slice(b, b + 1), slice(f, f + 1), slice(None), hs)
+                sel_k = (slice(b, b + 1), slice(f, f + 1), slice(None), slice(h, h + 1))
+                ref = oracle_mod.space_bwd(X(q[sel_q]), X(k[sel_k]), X(v[sel_k]), X(do[sel_q]), extra, w.scale)
+            else:
+                sel_q = (slice(b, b + 1), slice(None), slice(f, f + 1), hs)
+                sel_k = (slice(b, b + 1), slice(None), slice(f, f + 1), slice(h, h + 1))
+                ref = oracle_mod.time_bwd(X(q[sel_q]), X(k[sel_k]), X(v[sel_k]), X(do[sel_q]), extra, w.scale)
+            for nm, g, r in (("dQ", fq[sel_q], ref[2]), ("dK", fk[sel_k], ref[3]), ("dV", fv[sel_k], ref[4])):
+                assert_close(to_f64(g), r, "%s %s %s unit %s" % (name, kind, nm, (b, f, h)), bf16_out=False)
