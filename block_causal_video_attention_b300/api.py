@@ -65,6 +65,8 @@ def library():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = I
+            lib.od_space_attn_bwd_static_ws.argtypes = [P] * 12 + [I] * 7 + [F, P]
+            lib.od_space_attn_bwd_static_ws.restype = I
             lib.od_attn_bwd_workspace_bytes.argtypes = [I] * 7
             lib.od_attn_bwd_workspace_bytes.restype = Z
             lib.od_get_device_status.argtypes = [P]

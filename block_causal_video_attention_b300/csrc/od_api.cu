@@ -269,9 +269,50 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   return OD_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+// Fixed scratch for od_space_attn_bwd_static_ws: callers that cannot allocate device memory
+// (an allocator-free runtime, code running where cudaMalloc is forbidden or would
+// synchronise) still need the backward's per-row Delta scratch.  It lives in this
+// statically sized device array instead; each device that loads the library holds it until
+// the process exits.  Host code must never pass the symbol itself to a kernel: on the host
+// it is only a stand-in, so its device address is looked up once per device below.
+static __device__ __align__(256) unsigned char g_od_static_ws[OD_STATIC_WORKSPACE_BYTES];
+void* g_static_ws_ptr[kMaxDevices];
+
+od_status static_ws_pointer(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_static_ws_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_od_static_ws) != cudaSuccess || p == nullptr) return OD_ERR_CUDA;
+    g_static_ws_ptr[dev] = p;
+  }
+  *out = g_static_ws_ptr[dev];
+  return OD_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+od_status od_space_attn_bwd_static_ws(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dout, void* dq, void* dk,
+                                      void* dv, float* dq_f32, float* dk_f32, float* dv_f32, int B,
+                                      int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                                      float scale, void* stream) {
+  if (B <= 0 || T <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return OD_ERR_INVALID_ARG;
+  // the backward's scratch is one fp32 per query row; refuse what the fixed array cannot hold
+  const size_t need = od::bwd_workspace_bytes(B, T, S, Hq, D);
+  if (need > OD_STATIC_WORKSPACE_BYTES) return OD_ERR_WORKSPACE;
+  void* ws = nullptr;
+  od_status st = static_ws_pointer(&ws);
+  if (st != OD_OK) return st;
+  // the scratch is written completely before it is read, so nothing needs clearing
+  return launch_bwd(0, q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
+                    Hkv, D, agent_idx, 1, scale, ws, OD_STATIC_WORKSPACE_BYTES, stream);
+}
+
 
 od_status od_space_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,

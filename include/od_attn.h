@@ -93,6 +93,30 @@ od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const vo
                            int Hq, int Hkv, int D, int window, float scale, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* Size of the fixed device scratch used by od_space_attn_bwd_static_ws. */
+#define OD_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/* Space attention backward for callers that cannot allocate device memory -- for example
+ * code running under an allocator-free runtime, or at a point where cudaMalloc is not
+ * allowed or would synchronise the device.  (The Open Dreamer pages have no counterpart;
+ * this is a property of this library's interface.)  Same arguments and results as
+ * od_space_attn_bwd, minus the workspace: the per-query-row scratch the backward needs lives
+ * in a fixed device array of OD_STATIC_WORKSPACE_BYTES bytes inside the library, which every
+ * device that loads the library keeps until the process exits.  Calls with
+ * B*T*S*Hq*4 > OD_STATIC_WORKSPACE_BYTES are rejected with OD_ERR_WORKSPACE before anything
+ * is enqueued.  This call never allocates or frees device memory.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ * and caches it; make that first call before any stream capture on that device.
+ * Every call shares the one array and leaves its contents behind: calls whose kernels can
+ * overlap on the GPU (different streams, or different threads without ordering) race on it
+ * and must be serialised by the caller.  The scratch is fully rewritten by each call before
+ * it is read, so no clearing is needed. */
+od_status od_space_attn_bwd_static_ws(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dout, void* dq, void* dk,
+                                      void* dv, float* dq_f32, float* dk_f32, float* dv_f32, int B,
+                                      int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                                      float scale, void* stream);
+
 /* Bytes of device workspace the backward needs (which: 0 = space, 1 = time). Returns 0
  * for invalid sizes. */
 size_t od_attn_bwd_workspace_bytes(int which, int B, int T, int S, int Hq, int Hkv, int D);

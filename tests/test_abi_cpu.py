@@ -20,7 +20,7 @@ def test_every_declared_symbol_is_exported(lib):
     declared = set(re.findall(r"\b(od_\w+)\s*\(", src))
     assert {"od_space_attn_fwd", "od_time_attn_fwd", "od_space_attn_bwd", "od_time_attn_bwd",
             "od_attn_bwd_workspace_bytes", "od_get_device_status", "od_get_device_status_detail",
-            "od_status_string",
+            "od_status_string", "od_space_attn_bwd_static_ws",
             "od_version"} <= declared
     for name in declared:
         assert hasattr(lib, name), name
