@@ -131,6 +131,22 @@ def dist_info():
     return rank, world, local
 
 
+def max_over_ranks(x, device=None):
+    """Largest value of `x` over all ranks (the slowest replica sets the job's time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_step_per_rank, world, steps, ms):
+    """Whole-job throughput: every rank runs its own replica of the step (weak scaling)."""
+    return world * flop_per_step_per_rank * steps / (ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(w, nunits, with_bwd):
     """Time the fp64 oracle on `nunits` whole units of each op; returns (flop, seconds,
@@ -223,6 +239,12 @@ def run_ours(args, w, with_bwd):
     ops = ["space_fwd", "time_fwd"]
     if with_bwd:
         ops += ["space_bwd", "time_bwd"]
+    if args.op:
+        if args.op not in ops:
+            raise SystemExit("--op %s is not part of workload %s" % (args.op, w.name))
+        ops = [args.op]
+    run = set(ops)
+    if with_bwd:
         g = [torch.empty_like(x) for x in (dq, dk, dv, dq, dk, dv)]
         ws_s = torch.empty(max(api.bwd_workspace_bytes(0, w.B, w.T, w.S, w.Hq, w.Hkv), 16),
                            dtype=torch.uint8, device=dev)
@@ -241,14 +263,23 @@ def run_ours(args, w, with_bwd):
                 ev[op].append((a, b))
             else:
                 fn()
-        timed("space_fwd", lambda: api.space_attn_fwd(Q, K, V, w.agent, w.scale, o_s, l_s, stream))
-        timed("time_fwd", lambda: api.time_attn_fwd(Q, K, V, w.window, w.scale, o_t, l_t, stream))
-        if with_bwd:
+        if "space_fwd" in run:
+            timed("space_fwd", lambda: api.space_attn_fwd(Q, K, V, w.agent, w.scale, o_s, l_s, stream))
+        if "time_fwd" in run:
+            timed("time_fwd", lambda: api.time_attn_fwd(Q, K, V, w.window, w.scale, o_t, l_t, stream))
+        if "space_bwd" in run:
             timed("space_bwd", lambda: api.space_attn_bwd(Q, K, V, o_s, l_s, DO, w.agent, w.scale,
                                                           workspace=ws_s, out=g[:3], stream=stream))
+        if "time_bwd" in run:
             timed("time_bwd", lambda: api.time_attn_bwd(Q, K, V, o_t, l_t, DO, w.window, w.scale,
                                                         workspace=ws_t, out=g[3:], stream=stream))
 
+    if args.op and args.op.endswith("_bwd"):
+        # the backward reads the forward's O and LSE: produce them once, outside the timing
+        if args.op == "space_bwd":
+            api.space_attn_fwd(dq, dk, dv, w.agent, w.scale, o_s, l_s, stream)
+        else:
+            api.time_attn_fwd(dq, dk, dv, w.window, w.scale, o_t, l_t, stream)
     clk = Clocks(local).__enter__()
     for _ in range(args.warmup):
         step(False)
@@ -264,16 +295,12 @@ def run_ours(args, w, with_bwd):
         step(True)
     end.record(stream)
     torch.cuda.synchronize()
-    ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), dev)
     if api.get_device_status() != 0:
         raise RuntimeError("device timeout during the timed region")
     f = flops(w)
     step_flop = sum(f[o] for o in ops)
-    value = world * step_flop * args.steps / (ms * 1e-3) / 1e12
+    value = job_tflops(step_flop, world, args.steps, ms)
     per_op = {}
     for op in ops:
         t_ms = float(np.mean([a.elapsed_time(b) for a, b in ev[op]]))
@@ -304,13 +331,9 @@ def run_ours(args, w, with_bwd):
         e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b)
     clk.__exit__()
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = world * step_flop * args.steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(a.elapsed_time(b), dev)
+    e2e = job_tflops(step_flop, world, args.steps, e2e_ms)
 
     hbm, tc, tc_sus, src = load_peaks()
     # dominant kernel: the op with the largest share of device time
@@ -334,7 +357,7 @@ def run_ours(args, w, with_bwd):
                 "peak_source": "%s HBM copy" % src}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.op:
         fl, s, nth, desc = oracle_sample(w, args.ref_units, with_bwd)
         cpu = {"value": fl / s / 1e12, "unit": UNIT, "cores": nth, "kind": "oracle", "sample": desc}
 
@@ -371,6 +394,8 @@ def main():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--ref-units", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default=None, choices=["space_fwd", "time_fwd", "space_bwd", "time_bwd"],
+                    help="time one operator only (for profiling); the line then covers that op")
     args = ap.parse_args()
     name = args.workload or ("minecraft_fwd" if args.fwd_only else "minecraft_fwd_bwd")
     w = synth.WORKLOADS[name]

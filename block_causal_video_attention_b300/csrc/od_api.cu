@@ -211,8 +211,13 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   f.resident = 0;
   f.status = dev->status;
   if (f.nitems >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
+  if (1LL * B * f.F * Hkv * ((f.L + od::kKvBN - 1) / od::kKvBN) >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
 
   float* delta = static_cast<float*>(workspace);
+  float* amax = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                         od::bwd_delta_bytes(B, T, S, Hq));
+  const int num_ctas = dev->num_sms < od::kAmaxSlots ? dev->num_sms : od::kAmaxSlots;
+  int amax_slots = 0;
   const uint32_t qbox_space[5] = {64, (uint32_t)f.G, (uint32_t)f.nTok, 1, 1};
   const uint32_t qbox_time[5] = {64, (uint32_t)f.G, 1, (uint32_t)f.nTok, 1};
   const uint32_t* qbox = is_time ? qbox_time : qbox_space;
@@ -236,7 +241,9 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     dp.scale = scale;
     dp.dq = static_cast<__nv_bfloat16*>(dq);
     dp.dq_f32 = dq_f32;
-    const long long grid = f.nitems < dev->num_sms ? f.nitems : dev->num_sms;
+    dp.amax = amax;
+    const long long grid = f.nitems < num_ctas ? f.nitems : num_ctas;
+    amax_slots = static_cast<int>(grid);
     // 1. Delta pass, 2. dQ
     od::od_bwd_dq_kernel<true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
@@ -262,7 +269,9 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     kp.dv = static_cast<__nv_bfloat16*>(dv);
     kp.dk_f32 = dk_f32;
     kp.dv_f32 = dv_f32;
-    const long long grid = kp.nitems < dev->num_sms ? kp.nitems : dev->num_sms;
+    kp.amax = amax;
+    kp.amax_slots = amax_slots;
+    const long long grid = kp.nitems < num_ctas ? kp.nitems : num_ctas;
     od::od_bwd_dkdv_kernel<<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
   }

@@ -28,6 +28,50 @@
 
 namespace od {
 
+// ---------------------------------------------------------------- fp16 operand scaling
+// The dK/dV products run on fp16 operands scaled by powers of two: every bf16 input value
+// is exactly representable in fp16 once the tensor's largest magnitude is brought just
+// below 2^15 (only values 2^25 times smaller than that largest one lose bits as fp16
+// subnormals), and power-of-two scales cancel exactly after accumulation.  The Delta pass
+// records max|Q|, max|K|, max|V|, max|dO| per CTA (kAmaxSlots slots of 4 floats after the
+// Delta array in the workspace); the dK/dV kernel reduces the slots and derives the scales.
+constexpr int kAmaxSlots = 1024;
+
+// Running max of |x| over packed bf16 pairs, kept per 16-bit half as bf16 bit patterns
+// (non-negative bf16 patterns order like their values; NaN sorts above infinity).
+__device__ __forceinline__ uint32_t scan_amax(const uint8_t* buf, int bytes, int lane, uint32_t m) {
+  const uint4* src = reinterpret_cast<const uint4*>(buf);
+#pragma unroll 4
+  for (int x = lane; x < (bytes >> 4); x += 32) {
+    const uint4 d = src[x];
+    m = __vmaxu2(m, d.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, d.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, d.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, d.w & 0x7FFF7FFFu);
+  }
+  return m;
+}
+// Warp-wide max of scan_amax results, as a float.
+__device__ __forceinline__ float amax_reduce(uint32_t m) {
+  uint32_t h = max(m >> 16, m & 0xFFFFu);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) h = max(h, __shfl_xor_sync(0xffffffffu, h, o));
+  return __uint_as_float(h << 16);
+}
+// E with a < 2^E for a finite a > 0; 0 marks "no scaling" (a zero, infinite or NaN).
+__device__ __forceinline__ int amax_exp(float a, bool* usable) {
+  const uint32_t bits = __float_as_uint(a);
+  const int be = static_cast<int>((bits >> 23) & 0xFFu);
+  *usable = (a > 0.f) && (be != 0xFF);
+  return be == 0 ? -126 : be - 126;
+}
+// Power-of-two exponent e with a * 2^e < 2^15, clamped to [-60, 60].
+__device__ __forceinline__ int fp16_shift(float a) {
+  bool ok;
+  const int E = amax_exp(a, &ok);
+  return ok ? min(max(15 - E, -60), 60) : 0;
+}
+
 // ============================================================================ dQ kernel
 // Work items, Q tiles, key blocks and K/V staging as in the forward (FwdParams, fwd_decode).
 // TMEM per tile x (256 columns at 256 x): S [0,96), dP [96,192), dQ [192,256).
@@ -40,6 +84,7 @@ struct DqParams {
   FwdParams f;            // shapes and item schedule (f.o unused)
   const float* lse;       // forward logsumexp (natural log)
   float* delta;           // Delta per query row (written by the Delta pass, read otherwise)
+  float* amax;            // Delta pass: this CTA's max|Q|, max|K|, max|V|, max|dO| at 4*blockIdx.x
   float scale;
   __nv_bfloat16* dq;
   float* dq_f32;          // optional
@@ -96,7 +141,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (tid == 0) {
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.q_full[x], 1);
-      mbar_init(&sm.q_empty[x], 1);
+      mbar_init(&sm.q_empty[x], kDelta ? 2 : 1);  // + the range scanner in the Delta pass
       mbar_init(&sm.s_full[x], 1);
       mbar_init(&sm.ds_full[x], 4);
       mbar_init(&sm.dq_done[x], 1);
@@ -105,7 +150,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     for (int s = 0; s < kDqStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 2);
+      mbar_init(&sm.kv_empty[s], kDelta ? 3 : 2);
     }
     sm.ctl.abort = 0;
     fence_mbar_init();
@@ -123,7 +168,62 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
   if (warp >= 8) {
     regs_dec<kFwdCtrlRegs>();
-    if (warp == kFwdProducerWarp) {
+    if (kDelta && warp == 11) {
+      // ---------------------------------------------------------- operand range scan
+      // Walks the producer's fills in its order; every fill is scanned and then released
+      // (one more arrival on q_empty / kv_empty), so no buffer is refilled unscanned.
+      uint32_t mq = 0, mk = 0, mv = 0, mdo = 0;
+      long long prev_unit = -1;
+      uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
+      bool ok = true;
+      for (long long i = i0; i < i1 && ok; ++i) {
+        const FwdItem it = fwd_decode(p, i);
+        const int nb = it.kb_hi - it.kb_lo + 1;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (x == 1 && !it.validB) break;
+          ok = __all_sync(0xffffffffu, wait_bar(&sm.q_full[x], qn[x] & 1u, ctl, status, 17));
+          if (!ok) break;
+          ++qn[x];
+          mq = scan_amax(sQ[x], p.rows * 128, lane, mq);
+          mdo = scan_amax(sdO[x], p.rows * 128, lane, mdo);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.q_empty[x]);
+        }
+        if (!ok) break;
+        auto scan_kv = [&](int stage, uint32_t parity) -> bool {
+          bool w = wait_bar(&sm.k_full[stage], parity, ctl, status, 18) &&
+                   wait_bar(&sm.v_full[stage], parity, ctl, status, 18);
+          if (!__all_sync(0xffffffffu, w)) return false;
+          mk = scan_amax(sK + stage * kKVTile, kKVTile, lane, mk);
+          mv = scan_amax(sV + stage * kKVTile, kKVTile, lane, mv);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.kv_empty[stage]);
+          return true;
+        };
+        if (resident) {
+          if (it.unit != prev_unit) {
+            ++unit_loads;
+            prev_unit = it.unit;
+            for (int st = 0; st < p.nkb && ok; ++st) ok = scan_kv(st, (unit_loads - 1) & 1u);
+          }
+        } else {
+          for (int bi = 0; bi < nb && ok; ++bi) {
+            const uint32_t c = sbase + static_cast<uint32_t>(bi);
+            ok = scan_kv(static_cast<int>(c % kDqStages), (c / kDqStages) & 1u);
+          }
+        }
+        sbase += nb;
+      }
+      const float aq = amax_reduce(mq), ak = amax_reduce(mk), av = amax_reduce(mv),
+                  ad = amax_reduce(mdo);
+      if (lane == 0) {
+        float* slot = dp.amax + 4 * blockIdx.x;
+        slot[0] = aq;
+        slot[1] = ak;
+        slot[2] = av;
+        slot[3] = ad;
+      }
+    } else if (warp == kFwdProducerWarp) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
         tma_prefetch_desc(&tm_q);
@@ -455,18 +555,34 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 }
 
 // ============================================================================ dK/dV kernel
-// A CTA item is (unit, key block of 128 keys).  TMEM: S^T [0,128) (P^T high parts in place),
-// dP^T [128,256) (dS^T high parts in place), dK [256,320), dV [320,384), P^T residuals
-// [384,448), dS^T residuals [448,512); each accumulating product runs as high + residual.  Keys are TMEM lanes; Q tiles (nTok positions x G heads, as in
-// the forward) stream through two shared-memory slots together with dO and, per tile row,
-// log2-scaled LSE, Delta and the row's sequence position.
+// A CTA item is (unit, block of 128 keys); keys are TMEM lanes.  Every Q tile that can see
+// the block (nTok positions x G heads, as in the forward) is processed as two 64-row halves
+// h = 0, 1, each owned by its own warpgroup, so that the tensor core computes one half
+// while the other half's elementwise work runs:
+//   S^T_h = K Q_h^T and dP^T_h = V dO_h^T         (TMEM columns [128h, 128h+64), +64)
+//   P^T = exp2(S^T sl - LSE2),  dS^T = P^T (dP^T - Delta)   written as fp16 in place
+//   dV += P^T dO_h,  dK += dS^T Q_h                (TMEM [256,320) and [320,384))
+// All four operands are fp16 scaled by powers of two (see "fp16 operand scaling"): the
+// converter warps rewrite every K/V block and Q/dO tile in place after its TMA load.
+// Warps: 0-3 half 0, 4-7 half 1 (elementwise, then the epilogue: dK by warps 0-3, dV by
+// warps 4-7), 8 TMA producer + per-row LSE/Delta staging, 9 TMEM allocator + MMA issuer,
+// 10/11 converters (Q and K / dO and V).  K/V blocks are double-buffered across items and
+// Q/dO tiles stream through kKvQSlots slots.  CTA c takes items c, then 2*grid-1-c, then
+// 2*grid+c, ... so the items in flight at any time are consecutive (the key blocks of one
+// unit share its Q/dO tiles through L2) and alternate between cheaper and dearer blocks.
 constexpr int kKvBN = 128;
-constexpr int kKvThreads = 256;  // warps 0-3 elementwise, 4 producer, 5 MMA, 6-7 idle
+constexpr int kKvThreads = 384;
+constexpr int kKvQSlots = 4;
+constexpr int kKvProducerWarp = 8;
+constexpr int kKvMmaWarp = 9;
+constexpr int kKvConvWarp = 10;
 
 struct KvParams {
   FwdParams f;            // shapes (item fields unused)
   const float* lse;
   const float* delta;
+  const float* amax;      // Delta-pass slots: 4 floats per CTA of that launch
+  int amax_slots;
   float scale;
   long long nitems;       // units x key blocks
   int nkb;                // 128-key blocks per unit
@@ -477,22 +593,26 @@ struct KvParams {
 };
 
 struct KvSmem {
-  uint64_t kv_full, kv_free;
-  uint64_t q_full[2], q_empty[2];
-  uint64_t s_full, p_full, acc_done;
+  uint64_t kv_full[2], kv16[2], kv_free[2];
+  uint64_t q_full[kKvQSlots], q16[kKvQSlots], q_empty[kKvQSlots];
+  uint64_t sp_full[2], p_full[2], acc_done, acc_free;
   uint64_t drain;
   uint32_t tmem_base;
   Ctl ctl;
-  alignas(16) float lse2[2][128];   // read as float4: 16-byte aligned
-  alignas(16) float delta[2][128];
-  alignas(16) int qpos[2][128];
+  int eq, ek, ev, edo, eds;          // fp16 scale exponents
+  alignas(16) float nlse2[kKvQSlots][128];  // -log2(e) LSE per tile row (-inf: no row)
+  alignas(16) float ndel[kKvQSlots][128];   // -Delta * 2^eds per tile row
 };
-static_assert(offsetof(KvSmem, lse2) % 16 == 0 && offsetof(KvSmem, delta) % 16 == 0 &&
-                  offsetof(KvSmem, qpos) % 16 == 0,
+static_assert(offsetof(KvSmem, nlse2) % 16 == 0 && offsetof(KvSmem, ndel) % 16 == 0,
               "row arrays are read with 16-byte loads");
-// smem: [K V][Q0 Q1 dO0 dO1][KvSmem]
-constexpr size_t kKvTileBytes = size_t(2) * kTile + size_t(4) * kTile;
+// smem: [K0 V0 K1 V1][Q dO per slot][KvSmem]
+constexpr size_t kKvTileBytes = size_t(4) * kTile + size_t(2 * kKvQSlots) * kTile;
 constexpr size_t kKvSmemBytes = kKvTileBytes + 1024 + sizeof(KvSmem) + 64;
+static_assert(kKvSmemBytes <= 227 * 1024, "shared memory budget");
+constexpr int kKvElemRegs = 176;   // elementwise warpgroups
+constexpr int kKvCtrlRegs = 152;   // producer, issuer, converters
+static_assert(2 * 128 * kKvElemRegs + 128 * kKvCtrlRegs == kKvThreads * kFwdLaunchRegs,
+              "register split must add up to the launch allocation");
 
 struct KvItem {
   int b, fixed, kvh, kb;
@@ -521,6 +641,74 @@ __device__ __forceinline__ KvItem kv_decode(const KvParams& kp, long long i) {
   return it;
 }
 
+// The CTA's item sequence: round r takes item r*grid + c (r even) or r*grid + grid-1-c.
+struct KvSeq {
+  long long round = 0;
+  __device__ __forceinline__ bool next(const KvParams& kp, KvItem* it) {
+    for (;;) {
+      const long long base = round * static_cast<long long>(gridDim.x);
+      if (base >= kp.nitems) return false;
+      const long long c = (round & 1) ? static_cast<long long>(gridDim.x - 1 - blockIdx.x)
+                                      : static_cast<long long>(blockIdx.x);
+      ++round;
+      if (base + c < kp.nitems) {
+        *it = kv_decode(kp, base + c);
+        return true;
+      }
+    }
+  }
+};
+
+// One 32-column chunk of a key lane's elementwise step: P = exp2(S sl + nlse2) (zero
+// outside the lane's rows when kMasked), dS = P (dP c1 + ndel); both packed as fp16 pairs.
+template <bool kMasked>
+__device__ __forceinline__ void dkdv_chunk(const float* sv, const float* dv, const float* NL,
+                                           const float* ND, float2 sl2, float2 c12, uint32_t keep,
+                                           uint32_t* pk, uint32_t* dk) {
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) {
+    const float4 l4 = *reinterpret_cast<const float4*>(NL + 4 * j4);
+    const float4 d4 = *reinterpret_cast<const float4*>(ND + 4 * j4);
+    const float2 x0 = __ffma2_rn(make_float2(sv[4 * j4], sv[4 * j4 + 1]), sl2, make_float2(l4.x, l4.y));
+    const float2 x1 = __ffma2_rn(make_float2(sv[4 * j4 + 2], sv[4 * j4 + 3]), sl2, make_float2(l4.z, l4.w));
+    float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+    float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+    if (kMasked) {
+      const uint32_t kb = keep >> (4 * j4);
+      p0.x = (kb & 1u) ? p0.x : 0.f;
+      p0.y = (kb & 2u) ? p0.y : 0.f;
+      p1.x = (kb & 4u) ? p1.x : 0.f;
+      p1.y = (kb & 8u) ? p1.y : 0.f;
+    }
+    const float2 t0 = __ffma2_rn(make_float2(dv[4 * j4], dv[4 * j4 + 1]), c12, make_float2(d4.x, d4.y));
+    const float2 t1 = __ffma2_rn(make_float2(dv[4 * j4 + 2], dv[4 * j4 + 3]), c12, make_float2(d4.z, d4.w));
+    const float2 s0 = __fmul2_rn(p0, t0);
+    const float2 s1 = __fmul2_rn(p1, t1);
+    pk[2 * j4] = pack_f16x2(p0.x, p0.y);
+    pk[2 * j4 + 1] = pack_f16x2(p1.x, p1.y);
+    dk[2 * j4] = pack_f16x2(s0.x, s0.y);
+    dk[2 * j4 + 1] = pack_f16x2(s1.x, s1.y);
+  }
+}
+
+// Rewrite `bytes` of packed bf16 pairs as fp16 pairs times 2^e, in place (one warp).
+__device__ __forceinline__ void to_fp16_scaled(uint8_t* buf, int bytes, float s, int lane) {
+  uint4* p = reinterpret_cast<uint4*>(buf);
+  const float2 s2 = make_float2(s, s);
+#pragma unroll 4
+  for (int x = lane; x < (bytes >> 4); x += 32) {
+    uint4 d = p[x];
+    uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float2 f = __fmul2_rn(make_float2(__uint_as_float(w[h] << 16),
+                                              __uint_as_float(w[h] & 0xFFFF0000u)), s2);
+      w[h] = pack_f16x2(f.x, f.y);
+    }
+    p[x] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 __global__ void __launch_bounds__(kKvThreads, 1)
     od_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -529,42 +717,68 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sK = base;
-  uint8_t* sV = base + kTile;
-  uint8_t* sQ[2] = {base + 2 * kTile, base + 3 * kTile};
-  uint8_t* sdO[2] = {base + 4 * kTile, base + 5 * kTile};
+  uint8_t* sKV = base;                     // slot s: K at 2s*kTile, V at (2s+1)*kTile
+  uint8_t* sQD = base + 4 * kTile;         // slot q: Q at 2q*kTile, dO at (2q+1)*kTile
   KvSmem& sm = *reinterpret_cast<KvSmem*>(base + kKvTileBytes);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const long long i0 = (kp.nitems * blockIdx.x) / gridDim.x;
-  const long long i1 = (kp.nitems * (blockIdx.x + 1)) / gridDim.x;
 
-  {
+  {  // tile rows that TMA never writes stay zero (after conversion too)
     const int pad = (kBM - p.rows) * 128;
     for (int x = tid * 16; x < pad; x += kKvThreads * 16)
-      for (int t = 0; t < 2; ++t) {
-        *reinterpret_cast<uint4*>(sQ[t] + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sdO[t] + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
-      }
+      for (int t = 0; t < 2 * kKvQSlots; ++t)
+        *reinterpret_cast<uint4*>(sQD + t * kTile + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   if (tid == 0) {
-    mbar_init(&sm.kv_full, 1);
-    mbar_init(&sm.kv_free, 1);
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&sm.q_full[x], 1);
-      mbar_init(&sm.q_empty[x], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv16[s], 2);
+      mbar_init(&sm.kv_free[s], 1);
+      mbar_init(&sm.sp_full[s], 1);
+      mbar_init(&sm.p_full[s], 4);
     }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 4);
+    for (int q = 0; q < kKvQSlots; ++q) {
+      mbar_init(&sm.q_full[q], 1);
+      mbar_init(&sm.q16[q], 2);
+      mbar_init(&sm.q_empty[q], 1);
+    }
     mbar_init(&sm.acc_done, 1);
+    mbar_init(&sm.acc_free, 8);
     mbar_init(&sm.drain, 1);
     sm.ctl.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kKvProducerWarp) {
+    // operand ranges recorded by the Delta pass -> scale exponents
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int sl = lane; sl < kp.amax_slots; sl += 32)
+      for (int c = 0; c < 4; ++c) a[c] = fmaxf(a[c], kp.amax[4 * sl + c]);
+    // NaN compares false in fmaxf: propagate it explicitly so that no scaling is applied
+    for (int c = 0; c < 4; ++c) {
+      bool bad = false;
+      for (int sl = lane; sl < kp.amax_slots; sl += 32) bad |= !(kp.amax[4 * sl + c] == kp.amax[4 * sl + c]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        a[c] = fmaxf(a[c], __shfl_xor_sync(0xffffffffu, a[c], o));
+        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+      }
+      if (bad) a[c] = __int_as_float(0x7fc00000);
+    }
+    if (lane == 0) {
+      sm.eq = fp16_shift(a[0]);
+      sm.ek = fp16_shift(a[1]);
+      sm.ev = fp16_shift(a[2]);
+      sm.edo = fp16_shift(a[3]);
+      // |dS| <= |dP| + |Delta| <= 2 * 64 * max|dO| * max|V| < 2^(Edo + Ev + 7)
+      bool ok_do, ok_v;
+      const int Edo = amax_exp(a[3], &ok_do), Ev = amax_exp(a[2], &ok_v);
+      sm.eds = (ok_do && ok_v) ? min(max(15 - (Edo + Ev + 7), -60), 60) : 0;
+    }
+  }
+  if (warp == kKvMmaWarp) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
@@ -574,243 +788,308 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   Ctl* ctl = &sm.ctl;
   unsigned int* status = p.status;
-  const float lg2e = 1.4426950408889634f;
+  const int eq = sm.eq, ek = sm.ek, ev = sm.ev, edo = sm.edo, eds = sm.eds;
 
-  if (warp == 4) {
-    // ---------------------------------------------------------- producer (whole warp)
-    // lane 0 issues the TMA loads; all lanes stage the tile rows' LSE, Delta and position
-    uint32_t nt = 0, ni = 0;
-    bool ok = true;
-    for (long long i = i0; i < i1 && ok; ++i) {
-      const KvItem it = kv_decode(kp, i);
-      if (ni > 0) {
-        ok = wait_bar(&sm.kv_free, (ni - 1) & 1u, ctl, status, 20);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&sm.kv_full, 2 * kKvBN * 128);
-        const int k0 = it.kb * kKvBN;
-        if (p.is_time) {
-          tma_load_5d(sK, &tm_k, &sm.kv_full, 0, it.kvh, it.fixed, k0, it.b);
-          tma_load_5d(sV, &tm_v, &sm.kv_full, 0, it.kvh, it.fixed, k0, it.b);
-        } else {
-          tma_load_5d(sK, &tm_k, &sm.kv_full, 0, it.kvh, k0, it.fixed, it.b);
-          tma_load_5d(sV, &tm_v, &sm.kv_full, 0, it.kvh, k0, it.fixed, it.b);
-        }
-      }
-      ++ni;
-      for (int tq = it.t_lo; tq <= it.t_hi && ok; ++tq, ++nt) {
-        const int sl = nt & 1;
-        if (nt >= 2) {
-          ok = wait_bar(&sm.q_empty[sl], ((nt >> 1) - 1) & 1u, ctl, status, 21);
-          ok = __all_sync(0xffffffffu, ok);
+  if (warp >= 8) {
+    regs_dec<kKvCtrlRegs>();
+    if (warp == kKvProducerWarp) {
+      // ---------------------------------------------------------- producer (whole warp)
+      const float lg2e = 1.4426950408889634f;
+      const float c2 = ldexpf(1.f, eds);
+      KvSeq seq;
+      KvItem it;
+      uint32_t n = 0, tau = 0;
+      bool ok = true;
+      while (ok && seq.next(kp, &it)) {
+        const int slot = n & 1;
+        if (n >= 2) {
+          ok = __all_sync(0xffffffffu, wait_bar(&sm.kv_free[slot], ((n >> 1) - 1) & 1u, ctl, status, 20));
           if (!ok) break;
         }
-        const int t0 = tq * p.nTok;
-        // per tile row: log2-scaled LSE, Delta, sequence position (invalid rows: P = 0)
-        for (int rr = lane; rr < 128; rr += 32) {
-          const int tk = rr / p.G;
-          const int gg = rr - tk * p.G;
-          const int ps = t0 + tk;
-          float l2 = INFINITY, dl = 0.f;
-          int qp = 0x3FFFFFFF;
-          if (rr < p.rows && ps < p.L) {
-            const long long t_idx = p.is_time ? ps : it.fixed;
-            const long long s_idx = p.is_time ? it.fixed : ps;
-            const long long row =
-                ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * p.G + gg;
-            l2 = kp.lse[row] * lg2e;
-            dl = kp.delta[row];
-            qp = ps;
-          }
-          sm.lse2[sl][rr] = l2;
-          sm.delta[sl][rr] = dl;
-          sm.qpos[sl][rr] = qp;
-        }
-        __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.q_full[sl], 2 * p.rows * 128);
+          mbar_arrive_expect_tx(&sm.kv_full[slot], 2 * kKvBN * 128);
+          const int k0 = it.kb * kKvBN;
+          uint8_t* dK = sKV + (2 * slot) * kTile;
+          uint8_t* dV = sKV + (2 * slot + 1) * kTile;
           if (p.is_time) {
-            tma_load_5d(sQ[sl], &tm_q, &sm.q_full[sl], 0, it.kvh * p.G, it.fixed, t0, it.b);
-            tma_load_5d(sdO[sl], &tm_do, &sm.q_full[sl], 0, it.kvh * p.G, it.fixed, t0, it.b);
+            tma_load_5d(dK, &tm_k, &sm.kv_full[slot], 0, it.kvh, it.fixed, k0, it.b);
+            tma_load_5d(dV, &tm_v, &sm.kv_full[slot], 0, it.kvh, it.fixed, k0, it.b);
           } else {
-            tma_load_5d(sQ[sl], &tm_q, &sm.q_full[sl], 0, it.kvh * p.G, t0, it.fixed, it.b);
-            tma_load_5d(sdO[sl], &tm_do, &sm.q_full[sl], 0, it.kvh * p.G, t0, it.fixed, it.b);
+            tma_load_5d(dK, &tm_k, &sm.kv_full[slot], 0, it.kvh, k0, it.fixed, it.b);
+            tma_load_5d(dV, &tm_v, &sm.kv_full[slot], 0, it.kvh, k0, it.fixed, it.b);
+          }
+        }
+        ++n;
+        for (int tq = it.t_lo; tq <= it.t_hi && ok; ++tq, ++tau) {
+          const int q = static_cast<int>(tau % kKvQSlots);
+          if (tau >= kKvQSlots) {
+            ok = __all_sync(0xffffffffu,
+                            wait_bar(&sm.q_empty[q], ((tau / kKvQSlots) - 1) & 1u, ctl, status, 21));
+            if (!ok) break;
+          }
+          const int t0 = tq * p.nTok;
+          for (int rr = lane; rr < 128; rr += 32) {
+            const int tk = rr / p.G;
+            const int gg = rr - tk * p.G;
+            const int ps = t0 + tk;
+            float nl = -INFINITY, nd = 0.f;
+            if (rr < p.rows && ps < p.L) {
+              const long long t_idx = p.is_time ? ps : it.fixed;
+              const long long s_idx = p.is_time ? it.fixed : ps;
+              const long long row =
+                  ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * p.G + gg;
+              nl = -kp.lse[row] * lg2e;
+              nd = -kp.delta[row] * c2;
+            }
+            sm.nlse2[q][rr] = nl;
+            sm.ndel[q][rr] = nd;
+          }
+          __syncwarp();
+          if (lane == 0) {
+            uint8_t* dQ = sQD + (2 * q) * kTile;
+            uint8_t* dO = sQD + (2 * q + 1) * kTile;
+            mbar_arrive_expect_tx(&sm.q_full[q], 2 * p.rows * 128);
+            if (p.is_time) {
+              tma_load_5d(dQ, &tm_q, &sm.q_full[q], 0, it.kvh * p.G, it.fixed, t0, it.b);
+              tma_load_5d(dO, &tm_do, &sm.q_full[q], 0, it.kvh * p.G, it.fixed, t0, it.b);
+            } else {
+              tma_load_5d(dQ, &tm_q, &sm.q_full[q], 0, it.kvh * p.G, t0, it.fixed, it.b);
+              tma_load_5d(dO, &tm_do, &sm.q_full[q], 0, it.kvh * p.G, t0, it.fixed, it.b);
+            }
           }
         }
       }
-    }
-    if (lane == 0) {
-      if (ni > 0) drain_wait(&sm.kv_full, (ni - 1) & 1u);
-      for (int sl = 0; sl < 2; ++sl) {
-        const uint32_t uses = nt / 2 + (static_cast<uint32_t>(sl) < (nt & 1u) ? 1u : 0u);
-        if (uses > 0) drain_wait(&sm.q_full[sl], (uses - 1) & 1u);
+      if (lane == 0) {  // no TMA load may still be writing when the CTA exits
+        for (int s = 0; s < 2; ++s) {
+          const uint32_t uses = n / 2 + (static_cast<uint32_t>(s) < (n & 1u) ? 1u : 0u);
+          if (uses > 0) drain_wait(&sm.kv_full[s], (uses - 1) & 1u);
+        }
+        for (int q = 0; q < kKvQSlots; ++q) {
+          const uint32_t uses = tau / kKvQSlots + (static_cast<uint32_t>(q) < tau % kKvQSlots ? 1u : 0u);
+          if (uses > 0) drain_wait(&sm.q_full[q], (uses - 1) & 1u);
+        }
       }
-    }
-  } else if (warp == 5) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t tST = tmem, tDP = tmem + 128, tDK = tmem + 256, tDV = tmem + 320;
-      const uint32_t tPL = tmem + 384, tDL = tmem + 448;
-      const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);   // M keys, N tile rows
-      const uint32_t idesc_acc = idesc_bf16(128, 64, 0, 1);  // M keys, N head dim, B MN-major
-      uint32_t nt = 0, ni = 0, jp = 0;
+    } else if (warp == kKvMmaWarp) {
+      // ---------------------------------------------------------- MMA issuer
+      // Order: SP_0(0) SP_1(0); per tile t: [P_0(t)] DKV_0(t) SP_0(t+1) [P_1(t)] DKV_1(t)
+      // SP_1(t+1).  SP_h(t+1) overwrites half h's buffer after DKV_h(t) has been issued
+      // (tcgen05 MMAs of one thread run in issue order).
+      if (lane == 0) {
+        const uint32_t idesc_sp = idesc_fp16(128, 64, 0, 0);   // M keys, N 64 tile rows
+        const uint32_t idesc_acc = idesc_fp16(128, 64, 0, 1);  // M keys, N head dim, B MN-major
+        const uint32_t tDK = tmem + 256, tDV = tmem + 320;
+        KvSeq seq;
+        KvItem cur, nxt;
+        bool ok = seq.next(kp, &cur);
+        uint32_t n = 0, tau = 0;      // item and tile ordinals of the current tile
+        int k = 0;                    // tile within the current item
+        auto issue_sp = [&](int h, uint32_t t, uint32_t item_n) {
+          const int q = static_cast<int>(t % kKvQSlots);
+          const int slot = item_n & 1;
+          const uint64_t ak = sdesc_sw128(smem_u32(sKV + (2 * slot) * kTile), 16, 1024);
+          const uint64_t av = sdesc_sw128(smem_u32(sKV + (2 * slot + 1) * kTile), 16, 1024);
+          const uint64_t bq = sdesc_sw128(smem_u32(sQD + (2 * q) * kTile + h * 8192), 16, 1024);
+          const uint64_t bo = sdesc_sw128(smem_u32(sQD + (2 * q + 1) * kTile + h * 8192), 16, 1024);
+          const uint32_t dS = tmem + 128u * h, dP = dS + 64u;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_ss(dS, ak + 2 * kk, bq + 2 * kk, idesc_sp, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_ss(dP, av + 2 * kk, bo + 2 * kk, idesc_sp, kk > 0);
+          mma_commit(&sm.sp_full[h]);
+        };
+        auto issue_dkv = [&](int h, uint32_t t, bool first) {
+          const int q = static_cast<int>(t % kKvQSlots);
+          const uint64_t bq = sdesc_sw128(smem_u32(sQD + (2 * q) * kTile + h * 8192), 1024, 1024);
+          const uint64_t bo = sdesc_sw128(smem_u32(sQD + (2 * q + 1) * kTile + h * 8192), 1024, 1024);
+          const uint32_t aP = tmem + 128u * h, aD = aP + 64u;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_ts(tDV, aP + 8 * kk, bo + (2048 >> 4) * kk, idesc_acc, !(first && kk == 0));
+            mma_ts(tDK, aD + 8 * kk, bq + (2048 >> 4) * kk, idesc_acc, !(first && kk == 0));
+          }
+        };
+        // waits for the operands of tile t (item ordinal item_n, new item or not)
+        auto wait_operands = [&](uint32_t t, uint32_t item_n, bool new_item) -> bool {
+          if (new_item && !wait_bar(&sm.kv16[item_n & 1], (item_n >> 1) & 1u, ctl, status, 30)) return false;
+          if (!wait_bar(&sm.q16[t % kKvQSlots], (t / kKvQSlots) & 1u, ctl, status, 31)) return false;
+          tc_fence_after();
+          return true;
+        };
+        if (ok) {
+          ok = wait_operands(0, 0, true);
+          if (ok) {
+            issue_sp(0, 0, 0);
+            issue_sp(1, 0, 0);
+            if (cur.t_hi == cur.t_lo) mma_commit(&sm.kv_free[0]);
+          }
+        }
+        while (ok) {
+          const int ntl = cur.t_hi - cur.t_lo + 1;
+          // successor tile
+          bool has_next = true, next_new = false;
+          nxt = cur;
+          if (k + 1 >= ntl) {
+            has_next = seq.next(kp, &nxt);
+            next_new = true;
+          }
+          const uint32_t n1 = next_new ? n + 1 : n;
+          const int k1 = next_new ? 0 : k + 1;
+          const int ntl1 = nxt.t_hi - nxt.t_lo + 1;
+          // ---- half 0
+          if (!wait_bar(&sm.p_full[0], tau & 1u, ctl, status, 32)) break;
+          if (k == 0 && n > 0 && !wait_bar(&sm.acc_free, (n - 1) & 1u, ctl, status, 33)) break;
+          tc_fence_after();
+          issue_dkv(0, tau, k == 0);
+          if (has_next) {
+            if (!wait_operands(tau + 1, n1, next_new)) break;
+            issue_sp(0, tau + 1, n1);
+          }
+          // ---- half 1
+          if (!wait_bar(&sm.p_full[1], tau & 1u, ctl, status, 34)) break;
+          tc_fence_after();
+          issue_dkv(1, tau, false);
+          mma_commit(&sm.q_empty[tau % kKvQSlots]);
+          if (k == ntl - 1) mma_commit(&sm.acc_done);
+          if (!has_next) break;
+          issue_sp(1, tau + 1, n1);
+          if (k1 == ntl1 - 1) mma_commit(&sm.kv_free[n1 & 1]);
+          cur = nxt;
+          n = n1;
+          k = k1;
+          ++tau;
+        }
+        mma_commit(&sm.drain);
+        drain_wait(&sm.drain, 0);
+      }
+    } else {
+      // ---------------------------------------------------------- converters (10: Q, K; 11: dO, V)
+      const int which = warp - kKvConvWarp;  // 0: Q and K, 1: dO and V
+      const float sqd = ldexpf(1.f, which ? edo : eq);
+      const float skv = ldexpf(1.f, which ? ev : ek);
+      KvSeq seq;
+      KvItem it;
+      uint32_t n = 0, tau = 0;
       bool ok = true;
-      for (long long i = i0; i < i1 && ok; ++i) {
-        const KvItem it = kv_decode(kp, i);
-        if (!wait_bar(&sm.kv_full, ni & 1u, ctl, status, 22)) break;
-        ++ni;
-        const int ntl = it.t_hi - it.t_lo + 1;
-        for (int k = 0; k < ntl && ok; ++k, ++nt) {
-          const int sl = nt & 1;
-          if (!wait_bar(&sm.q_full[sl], (nt >> 1) & 1u, ctl, status, 23)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t ak = sdesc_sw128(smem_u32(sK), 16, 1024);
-          const uint64_t av = sdesc_sw128(smem_u32(sV), 16, 1024);
-          const uint64_t bq = sdesc_sw128(smem_u32(sQ[sl]), 16, 1024);
-          const uint64_t bdo = sdesc_sw128(smem_u32(sdO[sl]), 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_ss(tST, ak + 2 * kk, bq + 2 * kk, idesc_s, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_ss(tDP, av + 2 * kk, bdo + 2 * kk, idesc_s, kk > 0);
-          mma_commit(&sm.s_full);
-          if (!wait_bar(&sm.p_full, jp & 1u, ctl, status, 24)) { ok = false; break; }
-          ++jp;
-          tc_fence_after();
-          // dV += P^T dO and dK += dS^T Q (A from TMEM, B MN-major in shared memory)
-          const uint64_t bdo_mn = sdesc_sw128(smem_u32(sdO[sl]), 1024, 1024);
-          const uint64_t bq_mn = sdesc_sw128(smem_u32(sQ[sl]), 1024, 1024);
-          for (int kk = 0; kk < 8; ++kk) {
-            mma_ts(tDV, tST + 8 * kk, bdo_mn + (2048 >> 4) * kk, idesc_acc, (k > 0 || kk > 0));
-            mma_ts(tDV, tPL + 8 * kk, bdo_mn + (2048 >> 4) * kk, idesc_acc, 1);
-            mma_ts(tDK, tDP + 8 * kk, bq_mn + (2048 >> 4) * kk, idesc_acc, (k > 0 || kk > 0));
-            mma_ts(tDK, tDL + 8 * kk, bq_mn + (2048 >> 4) * kk, idesc_acc, 1);
-          }
-          mma_commit(&sm.q_empty[sl]);
-        }
+      while (ok && seq.next(kp, &it)) {
+        const int slot = n & 1;
+        ok = __all_sync(0xffffffffu, wait_bar(&sm.kv_full[slot], (n >> 1) & 1u, ctl, status, 35));
         if (!ok) break;
-        mma_commit(&sm.acc_done);
-        mma_commit(&sm.kv_free);
+        to_fp16_scaled(sKV + (2 * slot + which) * kTile, kKvBN * 128, skv, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.kv16[slot]);
+        ++n;
+        for (int tq = it.t_lo; tq <= it.t_hi && ok; ++tq, ++tau) {
+          const int q = static_cast<int>(tau % kKvQSlots);
+          ok = __all_sync(0xffffffffu, wait_bar(&sm.q_full[q], (tau / kKvQSlots) & 1u, ctl, status, 36));
+          if (!ok) break;
+          to_fp16_scaled(sQD + (2 * q + which) * kTile, p.rows * 128, sqd, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.q16[q]);
+        }
       }
-      mma_commit(&sm.drain);
-      drain_wait(&sm.drain, 0);
     }
-  } else if (warp < 4) {
-    // ---------------------------------------------------------- elementwise (key lanes)
-    const int j = tid;  // key lane within the block
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tST = tmem + lane_off, tDP = tmem + 128 + lane_off;
-    const uint32_t tDK = tmem + 256 + lane_off, tDV = tmem + 320 + lane_off;
-    const uint32_t tPL = tmem + 384 + lane_off, tDL = tmem + 448 + lane_off;
-    uint32_t nt = 0, js = 0, na = 0;
+  } else {
+    regs_inc<kKvElemRegs>();
+    // ------------------------------------------------------------ elementwise (key lanes)
+    const int h = warp >> 2;               // tile half: rows [64h, 64h+64)
+    const int j = tid & 127;               // key lane within the block
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + 128u * h + lane_off, tD = tS + 64u;
+    // logits: S^T carries 2^(eq+ek), dP^T carries 2^(edo+ev); dS^T is written times 2^eds
+    const float slx = p.sl * ldexpf(1.f, -(eq + ek));
+    const float c1 = ldexpf(1.f, eds - edo - ev);
+    const float2 sl2 = make_float2(slx, slx), c12 = make_float2(c1, c1);
+    const int Weff = min(p.window, p.L);
+    KvSeq seq;
+    KvItem it;
+    uint32_t n = 0, tau = 0;
     bool ok = true;
-    for (long long i = i0; i < i1 && ok; ++i) {
-      const KvItem it = kv_decode(kp, i);
+    while (ok && seq.next(kp, &it)) {
       const int kpos = it.kb * kKvBN + j;
-      const bool key_ok = kpos < p.L;
-      const bool is_agent = !p.is_time && kpos == p.agent;
-      const int ntl = it.t_hi - it.t_lo + 1;
-      for (int k = 0; k < ntl && ok; ++k, ++nt) {
-        const int sl = nt & 1;
-        // the tile rows' LSE/Delta/positions were staged by the producer before it armed
-        // q_full for this slot: acquire them from that barrier directly
-        ok = wait_bar(&sm.q_full[sl], (nt >> 1) & 1u, ctl, status, 27);
-        ok = ok && wait_bar(&sm.s_full, js & 1u, ctl, status, 25);
+      for (int tq = it.t_lo; tq <= it.t_hi && ok; ++tq, ++tau) {
+        const int q = static_cast<int>(tau % kKvQSlots);
+        ok = wait_bar(&sm.q_full[q], (tau / kKvQSlots) & 1u, ctl, status, 37) &&
+             wait_bar(&sm.sp_full[h], tau & 1u, ctl, status, 38);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        ++js;
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float sv[32], pv[32];
-          tmem_ld32(tST + 32 * c, sv);
-          tmem_ld32(tDP + 32 * c, pv);
-          tmem_wait_ld_dep32(sv);
-          tmem_wait_ld_dep32(pv);
-          uint32_t pk[16], dk[16], pl[16], dl[16];
+        float sv[64], dv[64];
+        tmem_ld32(tS, sv);
+        tmem_ld32(tS + 32, sv + 32);
+        tmem_ld32(tD, dv);
+        tmem_ld32(tD + 32, dv + 32);
+        // rows [r_lo, r_hi) of the tile may read this key (invalid rows have -inf LSE2)
+        const int t0 = tq * p.nTok;
+        int r_lo = 0, r_hi = 128;
+        if (p.is_time) {
+          const long long d = static_cast<long long>(kpos) - t0;
+          r_lo = static_cast<int>(min(max(d * p.G, 0LL), 128LL));
+          r_hi = static_cast<int>(min(max((d + Weff) * p.G, 0LL), 128LL));
+        } else if (kpos == p.agent) {
+          const long long d = static_cast<long long>(p.agent) - t0;
+          r_lo = static_cast<int>(min(max(d * p.G, 0LL), 128LL));
+          r_hi = static_cast<int>(min(max((d + 1) * p.G, 0LL), 128LL));
+        }
+        tmem_wait_ld_dep32(sv);
+        tmem_wait_ld_dep32(sv + 32);
+        tmem_wait_ld_dep32(dv);
+        tmem_wait_ld_dep32(dv + 32);
 #pragma unroll
-          for (int q = 0; q < 32; q += 2) {
-            const int col = 32 * c + q;
-            const float4 l4 = *reinterpret_cast<const float4*>(&sm.lse2[sl][col & ~3]);
-            const float4 d4 = *reinterpret_cast<const float4*>(&sm.delta[sl][col & ~3]);
-            const int4 q4 = *reinterpret_cast<const int4*>(&sm.qpos[sl][col & ~3]);
-            const int o = col & 3;  // 0 or 2
-            const float la = o ? l4.z : l4.x, lb = o ? l4.w : l4.y;
-            const float da = o ? d4.z : d4.x, db = o ? d4.w : d4.y;
-            const int qa = o ? q4.z : q4.x, qb = o ? q4.w : q4.y;
-            float p0 = ex2(fmaf(sv[q], p.sl, -la));
-            float p1 = ex2(fmaf(sv[q + 1], p.sl, -lb));
-            bool ka, kb2;
-            if (p.is_time) {
-              ka = qa >= kpos && qa - kpos < p.window;
-              kb2 = qb >= kpos && qb - kpos < p.window;
-            } else {
-              ka = !is_agent || qa == p.agent;
-              kb2 = !is_agent || qb == p.agent;
-            }
-            p0 = ka ? p0 : 0.f;
-            p1 = kb2 ? p1 : 0.f;
-            pk[q >> 1] = split_bf16x2(p0, p1, &pl[q >> 1]);
-            dk[q >> 1] = split_bf16x2(p0 * (pv[q] - da), p1 * (pv[q + 1] - db), &dl[q >> 1]);
-          }
-          tmem_st16(tST + 16 * c, pk);
-          tmem_st16(tDP + 16 * c, dk);
-          tmem_st16(tPL + 16 * c, pl);
-          tmem_st16(tDL + 16 * c, dl);
+        for (int c = 0; c < 2; ++c) {
+          const float* NL = &sm.nlse2[q][64 * h + 32 * c];
+          const float* ND = &sm.ndel[q][64 * h + 32 * c];
+          const uint32_t keep = keep_bits32(64 * h + 32 * c, r_lo, r_hi, -1);
+          uint32_t pk[16], dk[16];
+          if (__any_sync(0xffffffffu, keep != 0xFFFFFFFFu))
+            dkdv_chunk<true>(sv + 32 * c, dv + 32 * c, NL, ND, sl2, c12, keep, pk, dk);
+          else
+            dkdv_chunk<false>(sv + 32 * c, dv + 32 * c, NL, ND, sl2, c12, keep, pk, dk);
+          tmem_st16(tS + 16 * c, pk);   // P^T (fp16 pairs) over the scores already read
+          tmem_st16(tD + 16 * c, dk);   // dS^T (fp16 pairs, times 2^eds) over dP^T
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full);
+        if (lane == 0) mbar_arrive(&sm.p_full[h]);
       }
       if (!ok) break;
-      // ------------------------------------------------------------ epilogue: dK, dV rows
-      ok = wait_bar(&sm.acc_done, na & 1u, ctl, status, 26);
-      ok = __all_sync(0xffffffffu, ok);
+      // ------------------------------------------------------------ epilogue: dK (h 0), dV (h 1)
+      ok = __all_sync(0xffffffffu, wait_bar(&sm.acc_done, n & 1u, ctl, status, 39));
       if (!ok) break;
-      ++na;
+      ++n;
       tc_fence_after();
-      float gk[64], gv[64];
-      tmem_ld32(tDK, gk);
-      tmem_ld32(tDK + 32, gk + 32);
-      tmem_ld32(tDV, gv);
-      tmem_ld32(tDV + 32, gv + 32);
-      tmem_wait_ld_dep32(gk);
-      tmem_wait_ld_dep32(gk + 32);
-      tmem_wait_ld_dep32(gv);
-      tmem_wait_ld_dep32(gv + 32);
-      if (key_ok) {
+      float g[64];
+      const uint32_t tA = tmem + (h ? 320u : 256u) + lane_off;
+      tmem_ld32(tA, g);
+      tmem_ld32(tA + 32, g + 32);
+      tmem_wait_ld_dep32(g);
+      tmem_wait_ld_dep32(g + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_free);
+      if (kpos < p.L) {
+        const float f = h ? ldexpf(1.f, -edo) : kp.scale * ldexpf(1.f, -(eds + eq));
         const long long t_idx = p.is_time ? kpos : it.fixed;
         const long long s_idx = p.is_time ? it.fixed : kpos;
         const long long row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hkv + it.kvh;
-        uint4* dk_out = reinterpret_cast<uint4*>(kp.dk + row * 64);
-        uint4* dv_out = reinterpret_cast<uint4*>(kp.dv + row * 64);
+        uint4* out = reinterpret_cast<uint4*>((h ? kp.dv : kp.dk) + row * 64);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          uint4 a, b;
-          a.x = pack_bf16x2(gk[8 * c + 0] * kp.scale, gk[8 * c + 1] * kp.scale);
-          a.y = pack_bf16x2(gk[8 * c + 2] * kp.scale, gk[8 * c + 3] * kp.scale);
-          a.z = pack_bf16x2(gk[8 * c + 4] * kp.scale, gk[8 * c + 5] * kp.scale);
-          a.w = pack_bf16x2(gk[8 * c + 6] * kp.scale, gk[8 * c + 7] * kp.scale);
-          b.x = pack_bf16x2(gv[8 * c + 0], gv[8 * c + 1]);
-          b.y = pack_bf16x2(gv[8 * c + 2], gv[8 * c + 3]);
-          b.z = pack_bf16x2(gv[8 * c + 4], gv[8 * c + 5]);
-          b.w = pack_bf16x2(gv[8 * c + 6], gv[8 * c + 7]);
-          dk_out[c] = a;
-          dv_out[c] = b;
+          uint4 a;
+          a.x = pack_bf16x2(g[8 * c + 0] * f, g[8 * c + 1] * f);
+          a.y = pack_bf16x2(g[8 * c + 2] * f, g[8 * c + 3] * f);
+          a.z = pack_bf16x2(g[8 * c + 4] * f, g[8 * c + 5] * f);
+          a.w = pack_bf16x2(g[8 * c + 6] * f, g[8 * c + 7] * f);
+          out[c] = a;
         }
-        if (kp.dk_f32) {
-          float4* a = reinterpret_cast<float4*>(kp.dk_f32 + row * 64);
+        float* o32 = h ? kp.dv_f32 : kp.dk_f32;
+        if (o32) {
+          float4* a = reinterpret_cast<float4*>(o32 + row * 64);
 #pragma unroll
           for (int c = 0; c < 16; ++c)
-            a[c] = make_float4(gk[4 * c] * kp.scale, gk[4 * c + 1] * kp.scale, gk[4 * c + 2] * kp.scale,
-                               gk[4 * c + 3] * kp.scale);
-        }
-        if (kp.dv_f32) {
-          float4* b = reinterpret_cast<float4*>(kp.dv_f32 + row * 64);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) b[c] = make_float4(gv[4 * c], gv[4 * c + 1], gv[4 * c + 2], gv[4 * c + 3]);
+            a[c] = make_float4(g[4 * c] * f, g[4 * c + 1] * f, g[4 * c + 2] * f, g[4 * c + 3] * f);
         }
       }
     }
@@ -819,7 +1098,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kKvMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -844,12 +1123,18 @@ inline cudaError_t bwd_setup() {
   e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<true>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kFwdLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncGetAttributes(&fa, od_bwd_dkdv_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kFwdLaunchRegs) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 
-// workspace: Delta (fp32, one per query row)
-inline size_t bwd_workspace_bytes(int B, int T, int S, int Hq, int /*D*/) {
+// workspace: Delta (fp32, one per query row), then kAmaxSlots x 4 fp32 operand ranges
+inline size_t bwd_delta_bytes(int B, int T, int S, int Hq) {
   return (size_t(B) * T * S * Hq * sizeof(float) + 255) & ~size_t(255);
+}
+inline size_t bwd_workspace_bytes(int B, int T, int S, int Hq, int /*D*/) {
+  return bwd_delta_bytes(B, T, S, Hq) + size_t(kAmaxSlots) * 4 * sizeof(float);
 }
 
 struct BwdArgs {

@@ -77,7 +77,8 @@ od_status od_time_attn_fwd(const void* q, const void* k, const void* v, void* o,
 /* Space attention backward.  Inputs: Q, K, V, the forward's O and LSE, and dO.  Outputs
  * dQ [B,T,S,Hq,D], dK and dV [B,T,S,Hkv,D] in bf16 (overwritten).  `workspace` is
  * caller-owned device scratch of at least od_attn_bwd_workspace_bytes(0, ...) bytes
- * (fp32 row statistics and the fp32 dQ accumulator); its contents on entry do not matter.
+ * (Delta per query row in fp32, rounded up to 256 bytes, then 16 KiB of per-CTA operand
+ * ranges); its contents on entry do not matter.
  * If dq_f32/dk_f32/dv_f32 are non-NULL, the gradients are also written there in fp32
  * (same layouts), before rounding to bf16. */
 od_status od_space_attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -100,11 +101,13 @@ od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const vo
  * code running under an allocator-free runtime, or at a point where cudaMalloc is not
  * allowed or would synchronise the device.  (The Open Dreamer pages have no counterpart;
  * this is a property of this library's interface.)  Same arguments and results as
- * od_space_attn_bwd, minus the workspace: the per-query-row scratch the backward needs lives
- * in a fixed device array of OD_STATIC_WORKSPACE_BYTES bytes inside the library, which every
- * device that loads the library keeps until the process exits.  Calls with
- * B*T*S*Hq*4 > OD_STATIC_WORKSPACE_BYTES are rejected with OD_ERR_WORKSPACE before anything
- * is enqueued.  This call never allocates or frees device memory.
+ * od_space_attn_bwd, minus the workspace: the scratch the backward needs (fp32 per query row
+ * plus a fixed 16 KiB of operand ranges) lives in a fixed device array of
+ * OD_STATIC_WORKSPACE_BYTES bytes inside the library, which every device that loads the
+ * library keeps until the process exits.  Calls for which od_attn_bwd_workspace_bytes(0, ...)
+ * exceeds OD_STATIC_WORKSPACE_BYTES (B*T*S*Hq above 4,190,208) are rejected with
+ * OD_ERR_WORKSPACE before anything is enqueued.  This call never allocates or frees device
+ * memory.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress)
  * and caches it; make that first call before any stream capture on that device.
  * Every call shares the one array and leaves its contents behind: calls whose kernels can

@@ -76,6 +76,14 @@ def test_backward_rejects_invalid_arguments(lib, fn):
     assert f(*bad, 1, 4, 8, 4, 2, 64, extra, 0.125, GOOD, ws, P(0)) == 1
     assert f(*ptrs, 1, 4, 8, 4, 3, 64, extra, 0.125, GOOD, ws, P(0)) == 1           # Hq % Hkv
     assert lib.od_attn_bwd_workspace_bytes(2, 1, 4, 8, 4, 2, 64) == 0
+    # Delta (fp32 per query row, 256-byte rounded) + 1024 slots x 4 fp32 operand ranges
+    for dims in ((1, 4, 8, 4), (2, 7, 33, 12), (1, 256, 290, 30)):
+        rows = dims[0] * dims[1] * dims[2] * dims[3]
+        want = ((rows * 4 + 255) // 256) * 256 + 16384
+        assert lib.od_attn_bwd_workspace_bytes(0, *dims, 2 if dims[3] % 2 == 0 else 3, 64) == want
+    # the fixed array of the allocation-free entry point serves up to 4,190,208 rows
+    assert ((4190208 * 4 + 255) // 256) * 256 + 16384 <= 16 << 20
+    assert ((4190272 * 4 + 255) // 256) * 256 + 16384 > 16 << 20
     assert lib.od_attn_bwd_workspace_bytes(0, 1, 4, 8, 4, 3, 64) == 0
 
 

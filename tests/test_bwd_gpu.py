@@ -122,3 +122,28 @@ def test_backward_full_size_sampled_units(oracle_mod, name):
                 ref = oracle_mod.time_bwd(X(q[sel_q]), X(k[sel_k]), X(v[sel_k]), X(do[sel_q]), extra, w.scale)
             for nm, g, r in (("dQ", fq[sel_q], ref[2]), ("dK", fk[sel_k], ref[3]), ("dV", fv[sel_k], ref[4])):
                 assert_close(to_f64(g), r, "%s %s %s unit %s" % (name, kind, nm, (b, f, h)), bf16_out=False)
+
+
+def _scaled_bits(bits, e):
+    """bf16 bit patterns times 2^e (exact: only the exponent field moves)."""
+    x = synth.bf16_bits_to_f64(bits) * (2.0 ** e)
+    return synth.f64_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("kind", ["space", "time"])
+def test_backward_operands_far_from_unit_range(oracle_mod, kind):
+    """The dK/dV products run on fp16 operands scaled by powers of two taken from each
+    tensor's largest magnitude.  Inputs far outside fp16's own range (tiny dO, huge V, small
+    Q, large K) must give the same gradients, up to the exact power-of-two factors by which
+    each gradient scales: dQ ~ dO V K, dK ~ dO V Q, dV ~ dO."""
+    B, T, S, Hq, Hkv, agent, window = 1, 12, 150, 8, 2, 149, 7
+    q, k, v, do = inputs(B, T, S, Hq, Hkv, seed=4242, with_dout=True)
+    eq, ek, ev, edo = -9, 7, 20, -30
+    bits = (_scaled_bits(q, eq), _scaled_bits(k, ek), _scaled_bits(v, ev), _scaled_bits(do, edo))
+    extra = agent if kind == "space" else window
+    bf, f32, ref = run_bwd(oracle_mod, kind, bits, extra)
+    factors = (2.0 ** (edo + ev + ek), 2.0 ** (edo + ev + eq), 2.0 ** edo)
+    for name, g, gb, r, f in zip(("dQ", "dK", "dV"), f32, bf, ref, factors):
+        assert np.isfinite(g).all() and np.isfinite(gb).all()
+        assert_close(g / f, r / f, "scaled %s %s fp32" % (kind, name), bf16_out=False)
+        assert_close(gb / f, r / f, "scaled %s %s bf16" % (kind, name), mean_rel=3e-3)
