@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       // ---------------------------------------------------------- MMA issuers (per tile)
       // In order per tile: S(0), dP(0); then for each block j: wait dS(j), dQ += dS(j) K;
       // S(j+1), dP(j+1) (they overwrite buffers whose last reader was issued before them).
-      if (lane == 0) {
+      {  // whole warp in lockstep; one elected lane issues
         const int x = warp - kFwdMmaWarp;
         const uint32_t tS = tmem + 256u * x, tP = tS + 96u, tQ = tS + 192u;
         const uint32_t idesc_dq = idesc_bf16(128, 64, 0, 1);
@@ -319,13 +319,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const int nb = it.kb_hi - it.kb_lo + 1;
           if (resident && it.unit != prev_unit) {
             if (prev_unit >= 0)
-              for (int s = 0; s < p.nkb; ++s) mma_commit(&sm.kv_empty[s]);
+              for (int s = 0; s < p.nkb; ++s) mma_commit_w(&sm.kv_empty[s]);
             ++unit_loads;
             prev_unit = it.unit;
             for (int s = 0; s < p.nkb && ok; ++s)
-              ok = wait_bar(&sm.k_full[s], (unit_loads - 1) & 1u, ctl, status, 11);
+              ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[s], (unit_loads - 1) & 1u, ctl, status, 11));
             for (int s = 0; s < p.nkb && ok; ++s)
-              ok = wait_bar(&sm.v_full[s], (unit_loads - 1) & 1u, ctl, status, 11);
+              ok = __all_sync(0xffffffffu, wait_bar(&sm.v_full[s], (unit_loads - 1) & 1u, ctl, status, 11));
           }
           if (!ok) break;
           auto slot = [&](int bi) -> KvSlot {
@@ -344,19 +344,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (!resident)
               for (int bi = 0; bi < nb && ok; ++bi) {
                 const KvSlot ks = slot(bi);
-                ok = wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 12) &&
-                     wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 12);
-                if (ok) mma_commit(&sm.kv_empty[ks.stage]);
+                ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 12)) &&
+                     __all_sync(0xffffffffu, wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 12));
+                if (ok) mma_commit_w(&sm.kv_empty[ks.stage]);
               }
             sbase += nb;
             continue;
           }
-          if (!wait_bar(&sm.q_full[x], qn & 1u, ctl, status, 14)) break;
+          if (!__all_sync(0xffffffffu, wait_bar(&sm.q_full[x], qn & 1u, ctl, status, 14))) break;
           ++qn;
           auto issue_s = [&](int bi) -> bool {
             const KvSlot ks = slot(bi);
-            if (!wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 15)) return false;
-            if (!wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 15)) return false;
+            if (!__all_sync(0xffffffffu, wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 15))) return false;
+            if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 15))) return false;
             tc_fence_after();
             const int n = round16(block_ncols(it, it.kb_lo + bi));
             const uint32_t idesc = idesc_bf16(128, n, 0, 0);
@@ -365,17 +365,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             const uint64_t bk = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 16, 1024);
             const uint64_t bv = sdesc_sw128(smem_u32(sV + ks.stage * kKVTile), 16, 1024);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss(tS, aq + 2 * k, bk + 2 * k, idesc, k > 0);
+            for (int k = 0; k < 4; ++k) mma_ss_w(tS, aq + 2 * k, bk + 2 * k, idesc, k > 0);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss(tP, ado + 2 * k, bv + 2 * k, idesc, k > 0);
-            mma_commit(&sm.s_full[x]);
+            for (int k = 0; k < 4; ++k) mma_ss_w(tP, ado + 2 * k, bv + 2 * k, idesc, k > 0);
+            mma_commit_w(&sm.s_full[x]);
             ++js;
-            if (bi == nb - 1) mma_commit(&sm.q_empty[x]);
+            if (bi == nb - 1) mma_commit_w(&sm.q_empty[x]);
             return true;
           };
           ok = issue_s(0);
           for (int bi = 0; bi < nb && ok; ++bi) {
-            if (!wait_bar(&sm.ds_full[x], jd & 1u, ctl, status, 16)) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, wait_bar(&sm.ds_full[x], jd & 1u, ctl, status, 16))) { ok = false; break; }
             ++jd;
             tc_fence_after();
             const KvSlot ks = slot(bi);
@@ -383,20 +383,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
               const int ksteps = round16(block_ncols(it, it.kb_lo + bi)) >> 4;
               const uint64_t bk = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 1024, 1024);
               for (int k = 0; k < ksteps; ++k) {
-                mma_ts(tQ, tS + 8 * k, bk + (2048 >> 4) * k, idesc_dq, (bi > 0 || k > 0));
-                mma_ts(tQ, tP + 8 * k, bk + (2048 >> 4) * k, idesc_dq, 1);
+                mma_ts_w(tQ, tS + 8 * k, bk + (2048 >> 4) * k, idesc_dq, (bi > 0 || k > 0));
+                mma_ts_w(tQ, tP + 8 * k, bk + (2048 >> 4) * k, idesc_dq, 1);
               }
             }
-            if (!resident) mma_commit(&sm.kv_empty[ks.stage]);
+            if (!resident) mma_commit_w(&sm.kv_empty[ks.stage]);
             if (bi == nb - 1) {
-              if (!kDelta) mma_commit(&sm.dq_done[x]);
+              if (!kDelta) mma_commit_w(&sm.dq_done[x]);
             } else {
               ok = issue_s(bi + 1);
             }
           }
           sbase += nb;
         }
-        mma_commit(&sm.drain[x]);
+        mma_commit_w(&sm.drain[x]);
         drain_wait(&sm.drain[x], 0);
       }
     }
@@ -562,12 +562,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 //   S^T_h = K Q_h^T and dP^T_h = V dO_h^T         (TMEM columns [128h, 128h+64), +64)
 //   P^T = exp2(S^T sl - LSE2),  dS^T = P^T (dP^T - Delta)   written as fp16 in place
 //   dV += P^T dO_h,  dK += dS^T Q_h                (TMEM [256,320) and [320,384))
-// All four operands are fp16 scaled by powers of two (see "fp16 operand scaling"): the
-// converter warps rewrite every K/V block and Q/dO tile in place after its TMA load.
+// All four operands are fp16 scaled by powers of two (see "fp16 operand scaling").  K and V
+// of the item are the A operands of the first two products and live in TMEM ([384,416) and
+// [416,448)): the elementwise warpgroups write them there at the start of each item, so
+// every MMA reads only its B operand (a 64-row half tile) from shared memory.  The
+// converter warps rewrite each Q/dO tile in place as scaled fp16 after its TMA load.
 // Warps: 0-3 half 0, 4-7 half 1 (elementwise, then the epilogue: dK by warps 0-3, dV by
-// warps 4-7), 8 TMA producer + per-row LSE/Delta staging, 9 TMEM allocator + MMA issuer,
-// 10/11 converters (Q and K / dO and V).  K/V blocks are double-buffered across items and
-// Q/dO tiles stream through kKvQSlots slots.  CTA c takes items c, then 2*grid-1-c, then
+// warps 4-7), 8 TMA producer + per-row LSE/Delta copies, 9 TMEM allocator + MMA issuer
+// (whole warp, one elected lane issues), 10/11 converters (Q / dO).  K/V blocks are
+// double-buffered in shared memory across items; Q/dO tiles stream through kKvQSlots
+// slots.  CTA c takes items c, then 2*grid-1-c, then
 // 2*grid+c, ... so the items in flight at any time are consecutive (the key blocks of one
 // unit share its Q/dO tiles through L2) and alternate between cheaper and dearer blocks.
 constexpr int kKvBN = 128;
@@ -593,7 +597,7 @@ struct KvParams {
 };
 
 struct KvSmem {
-  uint64_t kv_full[2], kv16[2], kv_free[2];
+  uint64_t kv_full[2], kv_tmem[2];   // K/V block landed; copied into TMEM (slot reusable)
   uint64_t q_full[kKvQSlots], q16[kKvQSlots], q_empty[kKvQSlots];
   uint64_t sp_full[2], p_full[2], acc_done, acc_free;
   uint64_t drain;
@@ -724,6 +728,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  OD_TRACE_INIT();
 
   {  // tile rows that TMA never writes stay zero (after conversion too)
     const int pad = (kBM - p.rows) * 128;
@@ -731,17 +736,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       for (int t = 0; t < 2 * kKvQSlots; ++t)
         *reinterpret_cast<uint4*>(sQD + t * kTile + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
+    for (int x = tid; x < kKvQSlots * 128; x += kKvThreads) {
+      (&sm.nlse2[0][0])[x] = 0.f;
+      (&sm.ndel[0][0])[x] = 0.f;
+    }
   }
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv16[s], 2);
-      mbar_init(&sm.kv_free[s], 1);
+      mbar_init(&sm.kv_tmem[s], 8);
       mbar_init(&sm.sp_full[s], 1);
       mbar_init(&sm.p_full[s], 4);
     }
     for (int q = 0; q < kKvQSlots; ++q) {
-      mbar_init(&sm.q_full[q], 1);
+      mbar_init(&sm.q_full[q], 1 + 32);  // TMA issuer + the producer lanes' row copies
       mbar_init(&sm.q16[q], 2);
       mbar_init(&sm.q_empty[q], 1);
     }
@@ -754,9 +762,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   if (warp == kKvProducerWarp) {
     // operand ranges recorded by the Delta pass -> scale exponents
     float a[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int sl = lane; sl < kp.amax_slots; sl += 32)
+    for (int sl = lane; sl < kp.amax_slots; sl += 32) {
+#pragma unroll
       for (int c = 0; c < 4; ++c) a[c] = fmaxf(a[c], kp.amax[4 * sl + c]);
+    }
     // NaN compares false in fmaxf: propagate it explicitly so that no scaling is applied
+#pragma unroll
     for (int c = 0; c < 4; ++c) {
       bool bad = false;
       for (int sl = lane; sl < kp.amax_slots; sl += 32) bad |= !(kp.amax[4 * sl + c] == kp.amax[4 * sl + c]);
@@ -794,8 +805,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     regs_dec<kKvCtrlRegs>();
     if (warp == kKvProducerWarp) {
       // ---------------------------------------------------------- producer (whole warp)
-      const float lg2e = 1.4426950408889634f;
-      const float c2 = ldexpf(1.f, eds);
       KvSeq seq;
       KvItem it;
       uint32_t n = 0, tau = 0;
@@ -803,7 +812,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       while (ok && seq.next(kp, &it)) {
         const int slot = n & 1;
         if (n >= 2) {
-          ok = __all_sync(0xffffffffu, wait_bar(&sm.kv_free[slot], ((n >> 1) - 1) & 1u, ctl, status, 20));
+          ok = __all_sync(0xffffffffu, wait_bar(&sm.kv_tmem[slot], ((n >> 1) - 1) & 1u, ctl, status, 20));
           if (!ok) break;
         }
         if (lane == 0) {
@@ -822,29 +831,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         ++n;
         for (int tq = it.t_lo; tq <= it.t_hi && ok; ++tq, ++tau) {
           const int q = static_cast<int>(tau % kKvQSlots);
+          OD_TP(50, (int)tau, 0);
           if (tau >= kKvQSlots) {
             ok = __all_sync(0xffffffffu,
                             wait_bar(&sm.q_empty[q], ((tau / kKvQSlots) - 1) & 1u, ctl, status, 21));
             if (!ok) break;
           }
           const int t0 = tq * p.nTok;
-          for (int rr = lane; rr < 128; rr += 32) {
-            const int tk = rr / p.G;
-            const int gg = rr - tk * p.G;
-            const int ps = t0 + tk;
-            float nl = -INFINITY, nd = 0.f;
-            if (rr < p.rows && ps < p.L) {
-              const long long t_idx = p.is_time ? ps : it.fixed;
-              const long long s_idx = p.is_time ? it.fixed : ps;
-              const long long row =
-                  ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * p.G + gg;
-              nl = -kp.lse[row] * lg2e;
-              nd = -kp.delta[row] * c2;
-            }
-            sm.nlse2[q][rr] = nl;
-            sm.ndel[q][rr] = nd;
-          }
-          __syncwarp();
           if (lane == 0) {
             uint8_t* dQ = sQD + (2 * q) * kTile;
             uint8_t* dO = sQD + (2 * q + 1) * kTile;
@@ -857,6 +850,23 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               tma_load_5d(dO, &tm_do, &sm.q_full[q], 0, it.kvh * p.G, t0, it.fixed, it.b);
             }
           }
+          // raw LSE and Delta of the tile's rows, copied asynchronously (the converters
+          // rescale them); rows outside the sequence keep finite stale values, which only
+          // ever meet the zero Q/dO rows of the tile
+          for (int rr = lane; rr < p.rows; rr += 32) {
+            const int tk = rr / p.G;
+            const int ps = t0 + tk;
+            if (ps < p.L) {
+              const long long t_idx = p.is_time ? ps : it.fixed;
+              const long long s_idx = p.is_time ? it.fixed : ps;
+              const long long row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq +
+                                    it.kvh * p.G + (rr - tk * p.G);
+              cp_async4(&sm.nlse2[q][rr], kp.lse + row);
+              cp_async4(&sm.ndel[q][rr], kp.delta + row);
+            }
+          }
+          cp_async_arrive_noinc(&sm.q_full[q]);
+          OD_TP(51, (int)tau, 0);
         }
       }
       if (lane == 0) {  // no TMA load may still be writing when the CTA exits
@@ -873,8 +883,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       // ---------------------------------------------------------- MMA issuer
       // Order: SP_0(0) SP_1(0); per tile t: [P_0(t)] DKV_0(t) SP_0(t+1) [P_1(t)] DKV_1(t)
       // SP_1(t+1).  SP_h(t+1) overwrites half h's buffer after DKV_h(t) has been issued
-      // (tcgen05 MMAs of one thread run in issue order).
-      if (lane == 0) {
+      // (tcgen05 MMAs of one thread run in issue order).  The whole warp runs this loop in
+      // lockstep; one elected lane issues every MMA and commit.
+      {
         const uint32_t idesc_sp = idesc_fp16(128, 64, 0, 0);   // M keys, N 64 tile rows
         const uint32_t idesc_acc = idesc_fp16(128, 64, 0, 1);  // M keys, N head dim, B MN-major
         const uint32_t tDK = tmem + 256, tDV = tmem + 320;
@@ -883,19 +894,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         bool ok = seq.next(kp, &cur);
         uint32_t n = 0, tau = 0;      // item and tile ordinals of the current tile
         int k = 0;                    // tile within the current item
-        auto issue_sp = [&](int h, uint32_t t, uint32_t item_n) {
+        auto issue_sp = [&](int h, uint32_t t) {
           const int q = static_cast<int>(t % kKvQSlots);
-          const int slot = item_n & 1;
-          const uint64_t ak = sdesc_sw128(smem_u32(sKV + (2 * slot) * kTile), 16, 1024);
-          const uint64_t av = sdesc_sw128(smem_u32(sKV + (2 * slot + 1) * kTile), 16, 1024);
           const uint64_t bq = sdesc_sw128(smem_u32(sQD + (2 * q) * kTile + h * 8192), 16, 1024);
           const uint64_t bo = sdesc_sw128(smem_u32(sQD + (2 * q + 1) * kTile + h * 8192), 16, 1024);
           const uint32_t dS = tmem + 128u * h, dP = dS + 64u;
+          const uint32_t aK = tmem + 384u, aV = tmem + 416u;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_ss(dS, ak + 2 * kk, bq + 2 * kk, idesc_sp, kk > 0);
+          for (int kk = 0; kk < 4; ++kk) mma_ts_w(dS, aK + 8 * kk, bq + 2 * kk, idesc_sp, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_ss(dP, av + 2 * kk, bo + 2 * kk, idesc_sp, kk > 0);
-          mma_commit(&sm.sp_full[h]);
+          for (int kk = 0; kk < 4; ++kk) mma_ts_w(dP, aV + 8 * kk, bo + 2 * kk, idesc_sp, kk > 0);
+          mma_commit_w(&sm.sp_full[h]);
         };
         auto issue_dkv = [&](int h, uint32_t t, bool first) {
           const int q = static_cast<int>(t % kKvQSlots);
@@ -904,23 +913,22 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const uint32_t aP = tmem + 128u * h, aD = aP + 64u;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            mma_ts(tDV, aP + 8 * kk, bo + (2048 >> 4) * kk, idesc_acc, !(first && kk == 0));
-            mma_ts(tDK, aD + 8 * kk, bq + (2048 >> 4) * kk, idesc_acc, !(first && kk == 0));
+            mma_ts_w(tDV, aP + 8 * kk, bo + (2048 >> 4) * kk, idesc_acc, !(first && kk == 0));
+            mma_ts_w(tDK, aD + 8 * kk, bq + (2048 >> 4) * kk, idesc_acc, !(first && kk == 0));
           }
         };
         // waits for the operands of tile t (item ordinal item_n, new item or not)
         auto wait_operands = [&](uint32_t t, uint32_t item_n, bool new_item) -> bool {
-          if (new_item && !wait_bar(&sm.kv16[item_n & 1], (item_n >> 1) & 1u, ctl, status, 30)) return false;
-          if (!wait_bar(&sm.q16[t % kKvQSlots], (t / kKvQSlots) & 1u, ctl, status, 31)) return false;
+          if (new_item && !__all_sync(0xffffffffu, wait_bar(&sm.kv_tmem[item_n & 1], (item_n >> 1) & 1u, ctl, status, 30))) return false;
+          if (!__all_sync(0xffffffffu, wait_bar(&sm.q16[t % kKvQSlots], (t / kKvQSlots) & 1u, ctl, status, 31))) return false;
           tc_fence_after();
           return true;
         };
         if (ok) {
           ok = wait_operands(0, 0, true);
           if (ok) {
-            issue_sp(0, 0, 0);
-            issue_sp(1, 0, 0);
-            if (cur.t_hi == cur.t_lo) mma_commit(&sm.kv_free[0]);
+            issue_sp(0, 0);
+            issue_sp(1, 0);
           }
         }
         while (ok) {
@@ -934,56 +942,67 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           }
           const uint32_t n1 = next_new ? n + 1 : n;
           const int k1 = next_new ? 0 : k + 1;
-          const int ntl1 = nxt.t_hi - nxt.t_lo + 1;
           // ---- half 0
-          if (!wait_bar(&sm.p_full[0], tau & 1u, ctl, status, 32)) break;
-          if (k == 0 && n > 0 && !wait_bar(&sm.acc_free, (n - 1) & 1u, ctl, status, 33)) break;
+          if (!__all_sync(0xffffffffu, wait_bar(&sm.p_full[0], tau & 1u, ctl, status, 32))) break;
+          if (k == 0 && n > 0 && !__all_sync(0xffffffffu, wait_bar(&sm.acc_free, (n - 1) & 1u, ctl, status, 33))) break;
           tc_fence_after();
           issue_dkv(0, tau, k == 0);
-          if (has_next) {
-            if (!wait_operands(tau + 1, n1, next_new)) break;
-            issue_sp(0, tau + 1, n1);
+          OD_TP(61, (int)tau, 0);
+          if (has_next && !next_new) {
+            if (!wait_operands(tau + 1, n1, false)) break;
+            issue_sp(0, tau + 1);
+            OD_TP(62, (int)tau, 0);
           }
           // ---- half 1
-          if (!wait_bar(&sm.p_full[1], tau & 1u, ctl, status, 34)) break;
+          OD_TP(63, (int)tau, 0);
+          if (!__all_sync(0xffffffffu, wait_bar(&sm.p_full[1], tau & 1u, ctl, status, 34))) break;
           tc_fence_after();
           issue_dkv(1, tau, false);
-          mma_commit(&sm.q_empty[tau % kKvQSlots]);
-          if (k == ntl - 1) mma_commit(&sm.acc_done);
+          OD_TP(64, (int)tau, 0);
+          mma_commit_w(&sm.q_empty[tau % kKvQSlots]);
+          if (k == ntl - 1) mma_commit_w(&sm.acc_done);
           if (!has_next) break;
-          issue_sp(1, tau + 1, n1);
-          if (k1 == ntl1 - 1) mma_commit(&sm.kv_free[n1 & 1]);
+          // A new item's K/V reach TMEM only after its warpgroups have read this item's
+          // accumulators, which needs DKV_1 above: its first S/dP products go out here.
+          if (next_new) {
+            if (!wait_operands(tau + 1, n1, true)) break;
+            issue_sp(0, tau + 1);
+          }
+          issue_sp(1, tau + 1);
           cur = nxt;
           n = n1;
           k = k1;
           ++tau;
         }
-        mma_commit(&sm.drain);
+        mma_commit_w(&sm.drain);
         drain_wait(&sm.drain, 0);
       }
     } else {
-      // ---------------------------------------------------------- converters (10: Q, K; 11: dO, V)
-      const int which = warp - kKvConvWarp;  // 0: Q and K, 1: dO and V
+      // ---------------------------------------------------------- converters (10: Q, 11: dO)
+      const int which = warp - kKvConvWarp;  // 0: Q, 1: dO
       const float sqd = ldexpf(1.f, which ? edo : eq);
-      const float skv = ldexpf(1.f, which ? ev : ek);
+      const float rowf = which ? -ldexpf(1.f, eds) : -1.4426950408889634f;
       KvSeq seq;
       KvItem it;
       uint32_t n = 0, tau = 0;
       bool ok = true;
       while (ok && seq.next(kp, &it)) {
-        const int slot = n & 1;
-        ok = __all_sync(0xffffffffu, wait_bar(&sm.kv_full[slot], (n >> 1) & 1u, ctl, status, 35));
-        if (!ok) break;
-        to_fp16_scaled(sKV + (2 * slot + which) * kTile, kKvBN * 128, skv, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.kv16[slot]);
         ++n;
         for (int tq = it.t_lo; tq <= it.t_hi && ok; ++tq, ++tau) {
           const int q = static_cast<int>(tau % kKvQSlots);
+          OD_TP(70, (int)tau, 0);
           ok = __all_sync(0xffffffffu, wait_bar(&sm.q_full[q], (tau / kKvQSlots) & 1u, ctl, status, 36));
           if (!ok) break;
+          OD_TP(71, (int)tau, 0);
           to_fp16_scaled(sQD + (2 * q + which) * kTile, p.rows * 128, sqd, lane);
+          {  // rows of the tile: -log2(e) LSE (warp 10) or -Delta 2^eds (warp 11); 0 elsewhere
+            float* rowv = which ? sm.ndel[q] : sm.nlse2[q];
+            const int t0 = tq * p.nTok;
+            for (int rr = lane; rr < 128; rr += 32) {
+              const bool valid = rr < p.rows && t0 + rr / p.G < p.L;
+              rowv[rr] = valid ? rowv[rr] * rowf : 0.f;
+            }
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.q16[q]);
@@ -1002,18 +1021,46 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const float c1 = ldexpf(1.f, eds - edo - ev);
     const float2 sl2 = make_float2(slx, slx), c12 = make_float2(c1, c1);
     const int Weff = min(p.window, p.L);
+    const float skv = ldexpf(1.f, h ? ev : ek);
     KvSeq seq;
     KvItem it;
     uint32_t n = 0, tau = 0;
     bool ok = true;
     while (ok && seq.next(kp, &it)) {
       const int kpos = it.kb * kKvBN + j;
+      {  // this key's K (half 0) or V (half 1) row -> scaled fp16 -> TMEM A operand columns.
+         // The previous item's MMAs have all completed (its epilogue waited for them).
+        const int slot = n & 1;
+        ok = __all_sync(0xffffffffu, wait_bar(&sm.kv_full[slot], (n >> 1) & 1u, ctl, status, 35));
+        if (!ok) break;
+        const uint8_t* row = sKV + (2 * slot + h) * kTile + j * 128;
+        const float2 s2 = make_float2(skv, skv);
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row sits at chunk c ^ (j & 7)
+          const uint4 d = *reinterpret_cast<const uint4*>(row + ((c ^ (j & 7)) << 4));
+          const uint32_t x[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __fmul2_rn(make_float2(__uint_as_float(x[e] << 16),
+                                                    __uint_as_float(x[e] & 0xFFFF0000u)), s2);
+            w[4 * c + e] = pack_f16x2(f.x, f.y);
+          }
+        }
+        tmem_st32(tmem + lane_off + 384u + 32u * h, w);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.kv_tmem[slot]);
+      }
       for (int tq = it.t_lo; tq <= it.t_hi && ok; ++tq, ++tau) {
         const int q = static_cast<int>(tau % kKvQSlots);
-        ok = wait_bar(&sm.q_full[q], (tau / kKvQSlots) & 1u, ctl, status, 37) &&
+        OD_TP(40, (int)tau, 0);
+        ok = wait_bar(&sm.q16[q], (tau / kKvQSlots) & 1u, ctl, status, 37) &&
              wait_bar(&sm.sp_full[h], tau & 1u, ctl, status, 38);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        OD_TP(41, (int)tau, 0);
         tc_fence_after();
         float sv[64], dv[64];
         tmem_ld32(tS, sv);
@@ -1036,6 +1083,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tmem_wait_ld_dep32(sv + 32);
         tmem_wait_ld_dep32(dv);
         tmem_wait_ld_dep32(dv + 32);
+        OD_TP(45, (int)tau, 0);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const float* NL = &sm.nlse2[q][64 * h + 32 * c];
@@ -1049,15 +1097,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tmem_st16(tS + 16 * c, pk);   // P^T (fp16 pairs) over the scores already read
           tmem_st16(tD + 16 * c, dk);   // dS^T (fp16 pairs, times 2^eds) over dP^T
         }
+        OD_TP(46, (int)tau, 0);
         tmem_wait_st();
+        OD_TP(47, (int)tau, 0);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full[h]);
+        OD_TP(42, (int)tau, 0);
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue: dK (h 0), dV (h 1)
+      OD_TP(43, (int)n, 0);
       ok = __all_sync(0xffffffffu, wait_bar(&sm.acc_done, n & 1u, ctl, status, 39));
       if (!ok) break;
+      OD_TP(44, (int)n, 0);
       ++n;
       tc_fence_after();
       float g[64];

@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // tile's other score buffer; wait for P(j), issue P V(j).  At the end of an item the last
       // P V goes out at once.  Both issuers walk every item (tile B also the items it has no
       // rows in) and release every K/V fill they have seen arrive, so kv_empty counts two.
-      if (lane == 0) {
+      {  // whole warp in lockstep; one elected lane issues
         const int x = warp - kFwdMmaWarp;  // 0: tile A, 1: tile B
         const uint32_t idesc_pv_bf16 = idesc_bf16(128, 64, 0, 1);
         const uint32_t idesc_pv_fp16 = idesc_fp16(128, 64, 0, 1);
@@ -364,21 +364,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         bool ok = true;
         auto issue_pv = [&]() -> bool {
           const PvJob jb = (jp & 1u) ? f1 : f0;
-          if (!wait_bar(&sm.p_full[x], jp & 1u, ctl, status, 9)) return false;
-          if (!wait_bar(&sm.v16_ready[jb.stage], jb.vpar, ctl, status, 10)) return false;
+          if (!__all_sync(0xffffffffu, wait_bar(&sm.p_full[x], jp & 1u, ctl, status, 9))) return false;
+          if (!__all_sync(0xffffffffu, wait_bar(&sm.v16_ready[jb.stage], jb.vpar, ctl, status, 10))) return false;
           tc_fence_after();
           const uint64_t b = sdesc_sw128(smem_u32(sV + jb.stage * kKVTile), 1024, 1024);
           const uint32_t a = tmem + 192u * x + 96u * (jp & 1u);
           const uint32_t fmt = *reinterpret_cast<const uint32_t*>(sm.vfmt[jb.stage]);
           for (int k = 0; k < jb.ksteps; ++k) {
             const uint32_t idesc = ((fmt >> (8 * (k >> 1))) & 0xFFu) ? idesc_pv_bf16 : idesc_pv_fp16;
-            mma_ts(tOx, a + 8 * k, b + (2048 >> 4) * k, idesc, (jb.acc || k > 0));
+            mma_ts_w(tOx, a + 8 * k, b + (2048 >> 4) * k, idesc, (jb.acc || k > 0));
           }
-          mma_commit(&sm.o_done[x]);
+          mma_commit_w(&sm.o_done[x]);
           OD_TP(12 + x, 0, (int)jp);
           ++jp;
           --npend;
-          if (!p.resident) mma_commit(&sm.kv_empty[jb.stage]);
+          if (!p.resident) mma_commit_w(&sm.kv_empty[jb.stage]);
           return true;
         };
         for (long long i = i0; i < i1 && ok; ++i) {
@@ -387,13 +387,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (p.resident && it.unit != prev_unit) {
             if (prev_unit >= 0) {
               while (ok && npend > 0) ok = issue_pv();
-              for (int s2 = 0; s2 < p.nkb; ++s2) mma_commit(&sm.kv_empty[s2]);
+              for (int s2 = 0; s2 < p.nkb; ++s2) mma_commit_w(&sm.kv_empty[s2]);
             }
             ++unit_loads;
             prev_unit = it.unit;
             // observe the fill before this issuer can ever release it
             for (int s2 = 0; s2 < p.nkb && ok; ++s2)
-              ok = wait_bar(&sm.k_full[s2], (unit_loads - 1) & 1u, ctl, status, 11);
+              ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[s2], (unit_loads - 1) & 1u, ctl, status, 11));
           }
           if (!ok) break;
           if (x == 1 && !it.validB) {
@@ -401,8 +401,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               for (int bi = 0; bi < nb && ok; ++bi) {
                 const uint32_t c = sbase + static_cast<uint32_t>(bi);
                 const int stage = static_cast<int>(c % kStages);
-                ok = wait_bar(&sm.k_full[stage], (c / kStages) & 1u, ctl, status, 12);
-                if (ok) mma_commit(&sm.kv_empty[stage]);
+                ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[stage], (c / kStages) & 1u, ctl, status, 12));
+                if (ok) mma_commit_w(&sm.kv_empty[stage]);
               }
             }
             sbase += static_cast<uint32_t>(nb);
@@ -411,9 +411,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int bi = 0; bi < nb && ok; ++bi) {
             while (ok && npend >= 2) ok = issue_pv();
             if (!ok) break;
-            if (js > 0 && !wait_bar(&sm.s_taken[x], (js - 1) & 1u, ctl, status, 13)) { ok = false; break; }
+            if (js > 0 && !__all_sync(0xffffffffu, wait_bar(&sm.s_taken[x], (js - 1) & 1u, ctl, status, 13))) { ok = false; break; }
             if (bi == 0) {
-              if (!wait_bar(&sm.q_full[x], qn & 1u, ctl, status, 14)) { ok = false; break; }
+              if (!__all_sync(0xffffffffu, wait_bar(&sm.q_full[x], qn & 1u, ctl, status, 14))) { ok = false; break; }
               ++qn;
             }
             KvSlot ks;
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               ks.stage = static_cast<int>(c % kStages);
               ks.parity = (c / kStages) & 1u;
             }
-            if (!wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 15)) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 15))) { ok = false; break; }
             tc_fence_after();
             const int n = round16(block_ncols(it, it.kb_lo + bi));
             const uint32_t idesc = idesc_bf16(128, n, 0, 0);
@@ -433,8 +433,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const uint64_t b = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 16, 1024);
             const uint32_t d = tmem + 192u * x + 96u * (js & 1u);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss(d, a + 2 * k, b + 2 * k, idesc, k > 0);
-            mma_commit(&sm.s_full[x]);
+            for (int k = 0; k < 4; ++k) mma_ss_w(d, a + 2 * k, b + 2 * k, idesc, k > 0);
+            mma_commit_w(&sm.s_full[x]);
             OD_TP(10 + x, (int)i, bi);
             PvJob jb;
             jb.stage = static_cast<uint8_t>(ks.stage);
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (js & 1u) f1 = jb; else f0 = jb;
             ++js;
             ++npend;
-            if (bi == nb - 1) mma_commit(&sm.q_empty[x]);
+            if (bi == nb - 1) mma_commit_w(&sm.q_empty[x]);
             while (ok && npend >= 2) ok = issue_pv();
           }
           // the item's last P V goes out as soon as its P is ready
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           sbase += static_cast<uint32_t>(nb);
         }
         // wait until every MMA issued by this thread has completed before TMEM is freed
-        mma_commit(&sm.drain[x]);
+        mma_commit_w(&sm.drain[x]);
         drain_wait(&sm.drain[x], 0);
       }
     } else {
