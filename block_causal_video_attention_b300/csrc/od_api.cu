@@ -134,15 +134,19 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   p.npairs = (p.ntiles + 1) / 2;
   p.nitems = 1LL * B * p.F * Hkv * p.npairs;
   if (p.nitems >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
-  p.nkb = (p.L + od::kBN - 1) / od::kBN;
-  p.resident = p.nkb <= od::kStages;
+  p.rcp_npairs = od::host_div_rcp(p.npairs);
+  p.rcp_hkv = od::host_div_rcp(p.Hkv);
+  p.rcp_f = od::host_div_rcp(p.F);
+  p.bn = od::kFwdBN;
+  p.nkb = (p.L + od::kFwdBN - 1) / od::kFwdBN;
+  p.resident = p.nkb <= od::kFwdStages;
   p.lse = lse;
   p.status = dev->status;
 
   const uint32_t qbox_space[5] = {64, (uint32_t)p.G, (uint32_t)p.nTok, 1, 1};
   const uint32_t qbox_time[5] = {64, (uint32_t)p.G, 1, (uint32_t)p.nTok, 1};
-  const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kBN, 1, 1};
-  const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kBN, 1};
+  const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kFwdBN, 1, 1};
+  const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kFwdBN, 1};
   p.o = static_cast<__nv_bfloat16*>(o);
   CUtensorMap tq, tk, tv;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -207,6 +211,10 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   f.ntiles = (f.L + f.nTok - 1) / f.nTok;
   f.npairs = (f.ntiles + 1) / 2;
   f.nitems = 1LL * B * f.F * Hkv * f.npairs;
+  f.rcp_npairs = od::host_div_rcp(f.npairs);
+  f.rcp_hkv = od::host_div_rcp(f.Hkv);
+  f.rcp_f = od::host_div_rcp(f.F);
+  f.bn = od::kBN;
   f.nkb = (f.L + od::kBN - 1) / od::kBN;
   f.resident = 0;
   f.status = dev->status;

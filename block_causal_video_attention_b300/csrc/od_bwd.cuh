@@ -24,9 +24,13 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include "od_ptx.cuh"
-#include "od_fwd.cuh"
+#include "od_common.cuh"
 
 namespace od {
+
+// Key blocks of the query-stationary backward kernels (Delta pass and dQ): 96 keys.
+constexpr int kBN = 96;
+constexpr int kKVTile = kBN * 128;  // bytes of one K or V stage
 
 // ---------------------------------------------------------------- fp16 operand scaling
 // The dK/dV products run on fp16 operands scaled by powers of two: every bf16 input value
@@ -77,7 +81,7 @@ __device__ __forceinline__ int fp16_shift(float a) {
 // TMEM per tile x (256 columns at 256 x): S [0,96), dP [96,192), dQ [192,256).
 constexpr int kDqThreads = 384;
 constexpr int kDqStages = 5;
-static_assert(2 * 128 * kFwdSoftmaxRegs + 128 * kFwdCtrlRegs == kDqThreads * kFwdLaunchRegs,
+static_assert(2 * 128 * kQsSoftmaxRegs + 128 * kQsCtrlRegs == kDqThreads * kQsLaunchRegs,
               "register split must add up to the launch allocation");
 
 struct DqParams {
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     sm.ctl.abort = 0;
     fence_mbar_init();
   }
-  if (warp == kFwdMmaWarp) {
+  if (warp == kQsMmaWarp) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   unsigned int* status = p.status;
 
   if (warp >= 8) {
-    regs_dec<kFwdCtrlRegs>();
+    regs_dec<kQsCtrlRegs>();
     if (kDelta && warp == 11) {
       // ---------------------------------------------------------- operand range scan
       // Walks the producer's fills in its order; every fill is scanned and then released
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         slot[2] = av;
         slot[3] = ad;
       }
-    } else if (warp == kFwdProducerWarp) {
+    } else if (warp == kQsProducerWarp) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
         tma_prefetch_desc(&tm_q);
@@ -303,12 +307,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           }
         }
       }
-    } else if (warp == kFwdMmaWarp || warp == kFwdMmaWarp + 1) {
+    } else if (warp == kQsMmaWarp || warp == kQsMmaWarp + 1) {
       // ---------------------------------------------------------- MMA issuers (per tile)
       // In order per tile: S(0), dP(0); then for each block j: wait dS(j), dQ += dS(j) K;
       // S(j+1), dP(j+1) (they overwrite buffers whose last reader was issued before them).
       {  // whole warp in lockstep; one elected lane issues
-        const int x = warp - kFwdMmaWarp;
+        const int x = warp - kQsMmaWarp;
         const uint32_t tS = tmem + 256u * x, tP = tS + 96u, tQ = tS + 192u;
         const uint32_t idesc_dq = idesc_bf16(128, 64, 0, 1);
         uint32_t js = 0, jd = 0, qn = 0, unit_loads = 0, sbase = 0;
@@ -358,7 +362,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (!__all_sync(0xffffffffu, wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 15))) return false;
             if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 15))) return false;
             tc_fence_after();
-            const int n = round16(block_ncols(it, it.kb_lo + bi));
+            const int n = round16(block_ncols(it, it.kb_lo + bi, kBN));
             const uint32_t idesc = idesc_bf16(128, n, 0, 0);
             const uint64_t aq = sdesc_sw128(smem_u32(sQ[x]), 16, 1024);
             const uint64_t ado = sdesc_sw128(smem_u32(sdO[x]), 16, 1024);
@@ -380,7 +384,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tc_fence_after();
             const KvSlot ks = slot(bi);
             if (!kDelta) {
-              const int ksteps = round16(block_ncols(it, it.kb_lo + bi)) >> 4;
+              const int ksteps = round16(block_ncols(it, it.kb_lo + bi, kBN)) >> 4;
               const uint64_t bk = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 1024, 1024);
               for (int k = 0; k < ksteps; ++k) {
                 mma_ts_w(tQ, tS + 8 * k, bk + (2048 >> 4) * k, idesc_dq, (bi > 0 || k > 0));
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
     }
   } else {
-    regs_inc<kFwdSoftmaxRegs>();
+    regs_inc<kQsSoftmaxRegs>();
     // ------------------------------------------------------------ dS warpgroups
     const int x = warp >> 2;
     const int r = tid & 127;
@@ -434,7 +438,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const float2 nl2 = make_float2(-lse2, -lse2);
       for (int bi = 0; bi < nb; ++bi) {
         const int kbase = (it.kb_lo + bi) * kBN;
-        const int ncols = block_ncols(it, it.kb_lo + bi);
+        const int ncols = block_ncols(it, it.kb_lo + bi, kBN);
         const int n32 = (ncols + 31) >> 5;
         int lo, hi, ex;
         if (p.is_time) {
@@ -548,7 +552,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == kFwdMmaWarp) {
+  if (warp == kQsMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -615,7 +619,7 @@ constexpr size_t kKvSmemBytes = kKvTileBytes + 1024 + sizeof(KvSmem) + 64;
 static_assert(kKvSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kKvElemRegs = 176;   // elementwise warpgroups
 constexpr int kKvCtrlRegs = 152;   // producer, issuer, converters
-static_assert(2 * 128 * kKvElemRegs + 128 * kKvCtrlRegs == kKvThreads * kFwdLaunchRegs,
+static_assert(2 * 128 * kKvElemRegs + 128 * kKvCtrlRegs == kKvThreads * kQsLaunchRegs,
               "register split must add up to the launch allocation");
 
 struct KvItem {
@@ -1172,13 +1176,13 @@ inline cudaError_t bwd_setup() {
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<false>);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != kFwdLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<true>);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != kFwdLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncGetAttributes(&fa, od_bwd_dkdv_kernel);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != kFwdLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 

@@ -1,0 +1,161 @@
+// od_common.cuh -- definitions shared by the query-stationary kernels (sm_103a).
+//
+// A unit is one (b, t, kv head) for space attention or one (b, s, kv head) for time
+// attention; its sequence of L positions (S tokens of one timestep block, or T timesteps at
+// one token position) is cut into Q tiles of nTok = floor(128 / G) positions x G query heads
+// (rows r = tok * G + g, one 5-D TMA box), and its keys into blocks of `bn` keys.  A work item
+// is (unit, pair of consecutive Q tiles A and B).
+#pragma once
+#include <cuda.h>
+#include "od_ptx.cuh"
+
+// Timeline trace points: compiled out unless OD_TRACE is defined (a profiling build that
+// supplies od_trace(event, a, b)).
+#ifdef OD_TRACE
+#define OD_TP(ev, a, b) od_trace((ev), (a), (b))
+#define OD_TRACE_INIT() od_trace_init()
+#else
+#define OD_TP(ev, a, b) ((void)0)
+#define OD_TRACE_INIT() ((void)0)
+#endif
+
+namespace od {
+
+constexpr int kBM = 128;           // query rows per tile (MMA M)
+constexpr int kTile = 128 * 128;   // bytes of one Q tile: 128 rows x 64 16-bit elements
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// The 384-thread layout of the backward kernels: warps 0-7 elementwise (two warpgroups),
+// 8-11 control; launched with kQsLaunchRegs registers, then rebalanced per warpgroup.
+constexpr int kQsLaunchRegs = 168;
+constexpr int kQsSoftmaxRegs = 200;
+constexpr int kQsCtrlRegs = 104;
+constexpr int kQsProducerWarp = 8;
+constexpr int kQsMmaWarp = 9;
+
+struct FwdParams {
+  int B, T, S, Hq, Hkv, G;
+  int is_time;
+  int L;          // sequence length of a unit (S for space, T for time)
+  int F;          // second index of a unit (T for space, S for time)
+  int agent;      // space: agent token index or -1
+  int window;     // time: window length W >= 1
+  float sl;       // scale * log2(e)
+  int nTok;       // sequence positions per Q tile
+  int rows;       // nTok * G <= 128
+  int ntiles;     // Q tiles per unit
+  int npairs;     // work items per unit
+  long long nitems;
+  int bn;         // keys per key block
+  int nkb;        // key blocks per unit
+  int resident;   // nkb <= K/V stages: the unit's K/V stay in smem across its items
+  // reciprocals for the item decode: floor(2^64 / d) + 1 for d = npairs, Hkv, F (0 when
+  // d >= 2^16, where the plain division is used)
+  unsigned long long rcp_npairs, rcp_hkv, rcp_f;
+  __nv_bfloat16* o;
+  float* lse;
+  unsigned int* status;
+};
+
+struct FwdItem {
+  uint32_t unit;
+  int b, fixed, kvh;
+  int tok0[2];
+  int validB;
+  int key_lo, key_hi;  // allowed key positions of the item lie in [key_lo, key_hi)
+  int kb_lo, kb_hi;    // inclusive key-block range
+};
+
+// n / d for n < 2^32 and 1 < d < 2^16 with rcp = floor(2^64 / d) + 1: the product's error
+// term n (rcp d - 2^64) / (d 2^64) stays below n / 2^64 < 1 / d, so the high word is exact.
+__device__ __forceinline__ uint32_t div_rcp(uint32_t n, uint32_t d, unsigned long long rcp) {
+  if (rcp == 0ull) return n / d;
+  return static_cast<uint32_t>(__umul64hi(static_cast<unsigned long long>(n), rcp));
+}
+// Host side: the reciprocal div_rcp expects (0 selects the plain division).
+inline unsigned long long host_div_rcp(int d) {
+  if (d <= 1 || d >= 65536) return 0ull;
+  return (~0ull) / static_cast<unsigned long long>(d) + 1ull;
+}
+
+__device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
+  // the host guarantees nitems < 2^31, so 32-bit unsigned division suffices
+  FwdItem it;
+  const uint32_t ii = static_cast<uint32_t>(i);
+  const uint32_t unit = div_rcp(ii, static_cast<uint32_t>(p.npairs), p.rcp_npairs);
+  const int pair = static_cast<int>(ii - unit * static_cast<uint32_t>(p.npairs));
+  it.unit = unit;
+  const uint32_t r = div_rcp(unit, static_cast<uint32_t>(p.Hkv), p.rcp_hkv);
+  it.kvh = static_cast<int>(unit - r * static_cast<uint32_t>(p.Hkv));
+  const uint32_t bq = div_rcp(r, static_cast<uint32_t>(p.F), p.rcp_f);
+  it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
+  it.b = static_cast<int>(bq);
+  const int tA = 2 * pair;
+  it.tok0[0] = tA * p.nTok;
+  it.tok0[1] = (tA + 1) * p.nTok;
+  it.validB = (tA + 1) < p.ntiles;
+  const int last = min(p.L, (it.validB ? tA + 2 : tA + 1) * p.nTok) - 1;
+  if (p.is_time) {
+    it.key_lo = max(0, it.tok0[0] - p.window + 1);
+    it.key_hi = last + 1;
+  } else {
+    it.key_lo = 0;
+    it.key_hi = p.L;
+  }
+  it.kb_lo = it.key_lo / p.bn;
+  it.kb_hi = (it.key_hi - 1) / p.bn;
+  return it;
+}
+
+__device__ __forceinline__ int block_ncols(const FwdItem& it, int kb, int bn) {
+  return min(bn, it.key_hi - kb * bn);
+}
+__device__ __forceinline__ int round16(int x) { return (x + 15) & ~15; }
+
+// K/V stage and phase parity of block index bi (0-based within the item).
+struct KvSlot {
+  int stage;
+  uint32_t parity;
+};
+__device__ __forceinline__ KvSlot kv_slot(const FwdParams& p, const FwdItem& it, int bi,
+                                          uint32_t unit_loads, uint32_t stream_cnt, int stages) {
+  KvSlot s;
+  if (p.resident) {
+    s.stage = it.kb_lo + bi;
+    s.parity = (unit_loads - 1) & 1u;
+  } else {
+    const uint32_t c = stream_cnt + bi;
+    s.stage = static_cast<int>(c % static_cast<uint32_t>(stages));
+    s.parity = (c / static_cast<uint32_t>(stages)) & 1u;
+  }
+  return s;
+}
+
+// Bit j set <=> column c0 + j of a score row is allowed: lo <= col < hi and col != ex.
+__device__ __forceinline__ uint32_t keep_bits32(int c0, int lo, int hi, int ex) {
+  const int a = min(max(lo - c0, 0), 32);
+  const int b = min(max(hi - c0, 0), 32);
+  const uint32_t below_b = b >= 32 ? 0xFFFFFFFFu : ((1u << b) - 1u);
+  const uint32_t below_a = a >= 32 ? 0xFFFFFFFFu : ((1u << a) - 1u);
+  uint32_t m = below_b & ~below_a;
+  if (ex >= c0 && ex < c0 + 32) m &= ~(1u << (ex - c0));
+  return m;
+}
+__device__ __forceinline__ void apply_mask32(float* v, uint32_t keep) {
+  if (__any_sync(0xffffffffu, keep != 0xFFFFFFFFu)) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = ((keep >> j) & 1u) ? v[j] : -INFINITY;
+  }
+}
+
+// bounded wait that ignores the abort flag (used only to drain in-flight async work)
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer() - t0 > OD_WAIT_LIMIT_NS) break;
+  }
+}
+
+
+}  // namespace od

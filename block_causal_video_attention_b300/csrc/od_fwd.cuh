@@ -13,194 +13,84 @@
 // K/V of a unit are loaded once per CTA visit and reused by all G heads and all Q tiles.
 //
 // One persistent CTA per SM walks a contiguous range of work items; an item is
-// (unit, pair of Q tiles A and B).  Warp roles (384 threads, three warpgroups):
-//   warps 0-3   softmax warpgroup for Q tile A  (thread i owns TMEM lane / row i)
-//   warps 4-7   softmax warpgroup for Q tile B
-//   warp  8     TMA producer (one thread)
-//   warp  9     TMEM allocator + tcgen05.mma issuer for tile A (one thread)
-//   warp  10    tcgen05.mma issuer for tile B (one thread)
-//   warp  11    converts each V tile to fp16 in shared memory (P V runs in fp16)
-// The kernel launches with kFwdLaunchRegs registers per thread; the softmax warpgroups
-// then raise their limit to kFwdSoftmaxRegs and the control warpgroup lowers its own to
-// kFwdCtrlRegs.  2*128*kFwdSoftmaxRegs + 128*kFwdCtrlRegs equals the launch allocation, and
-// the host refuses to launch if the compiled register count differs from kFwdLaunchRegs.
+// (unit, pair of Q tiles A and B).  Keys come in blocks of 64.  Every score row is split
+// between two threads: one takes columns 0-31 of each block ("half a"), the other columns
+// 32-63 ("half b").  Each half keeps its own running maximum, its own row sum and its own
+// output accumulator (O_a, O_b in TMEM), so the halves never synchronise per block; at the
+// end of an item they exchange (max, sum) once through shared memory and combine
+//   O = (O_a 2^(m_a - M) + O_b 2^(m_b - M)) / (l_a 2^(m_a - M) + l_b 2^(m_b - M)),
+//   M = max(m_a, m_b).
+// Warp roles (640 threads, five warpgroups):
+//   warps 0-3 tile A half a, 4-7 tile A half b, 8-11 tile B half a, 12-15 tile B half b
+//        (thread i of a warpgroup owns TMEM lane / row i)
+//   warp 16  TMA producer (one thread)
+//   warps 17, 18  TMEM allocator (17) and tcgen05.mma issuers for tiles A and B (whole warp,
+//        one elected lane issues)
+//   warp 19  converts each V tile to fp16 in shared memory (P V runs in fp16)
+// The kernel launches with kFwdLaunchRegs registers per thread; the softmax warpgroups then
+// drop to kFwdSoftmaxRegs and the control warpgroup rises to kFwdCtrlRegs.  The shares add
+// up to the launch allocation, and the host refuses to launch if the compiled register count
+// differs from kFwdLaunchRegs.
 //
-// TMEM (512 columns): per tile two 96-column score buffers -- tile A [0,192), tile B
-// [192,384); a tile's j-th scores go to its buffer j mod 2 -- and O_A [384,448),
-// O_B [448,512).  The softmax writes P (fp16 pairs) in place over the first 48 columns of the
-// scores it came from; P V reads it from TMEM.  A tile's Q K^T number j is issued once its
-// softmax has taken scores j-1 and P V j-2 has been issued (tcgen05 MMAs of one thread run
-// in issue order), so each tile has its next scores computed while it works, independently
-// of the other tile.  Every mbarrier is waited on at most one phase ahead of or behind its
-// completions (a parity wait cannot tell more apart); the per-tile "taken" barrier bounds
-// the lookahead.
-// Key blocks are 96 keys; the key range of an item is the union of its rows' allowed
-// ranges, so key blocks that are fully masked for the whole item are never loaded;
-// partial blocks are masked per element.  Online softmax with a lazy rescale: the running
-// maximum used for the exponentials only moves when a block's maximum exceeds it by more
-// than 8 (log2 units); O is then rescaled in TMEM.  Statistics are fp32; LSE (natural log)
-// and O are written straight from registers.
+// TMEM (512 columns), per tile x at 256x: two 64-column score buffers [0,64) and [64,128)
+// (block j of the tile goes to buffer j mod 2), O_a [128,192), O_b [192,256).  Each half
+// writes its P (fp16 pairs, 16 columns) in place at the start of its own 32 columns; P V
+// reads it from TMEM.  A tile's Q K^T number j is issued once both halves have taken scores
+// j-1 and P V j-2 has been issued (tcgen05 MMAs of one thread run in issue order), so each
+// tile has its next scores computed while its softmax works; the softmax never waits for a
+// P V except to rescale O and at the end of an item.  Every mbarrier is waited on at
+// most one phase ahead of or behind its completions (a parity wait cannot tell more apart).
+// The key range of an item is the union of its rows' allowed ranges, so key blocks that are
+// fully masked for the whole item are never loaded; partial blocks are masked per element.
+// Online softmax with a lazy rescale: a half's running maximum only moves when a block's
+// maximum exceeds it by more than 8 (log2 units); that half's O is then rescaled in TMEM.
+// Statistics are fp32; LSE (natural log) and O are written from registers.
 #pragma once
-#include <cuda.h>
-#include "od_ptx.cuh"
-
-// Timeline trace points: compiled out unless OD_TRACE is defined (a profiling build that
-// supplies od_trace(event, a, b)).
-#ifdef OD_TRACE
-#define OD_TP(ev, a, b) od_trace((ev), (a), (b))
-#define OD_TRACE_INIT() od_trace_init()
-#else
-#define OD_TP(ev, a, b) ((void)0)
-#define OD_TRACE_INIT() ((void)0)
-#endif
+#include "od_common.cuh"
 
 namespace od {
 
-constexpr int kBM = 128;           // query rows per tile (MMA M)
-constexpr int kBN = 96;            // keys per key block (score buffer columns)
-constexpr int kStages = 6;         // K/V shared-memory stages
-constexpr int kTile = 128 * 128;   // bytes of one Q tile: 128 rows x 64 16-bit elements
-constexpr int kKVTile = kBN * 128; // bytes of one K or V stage: 96 rows x 64 elements
-constexpr int kFwdThreads = 384;
-constexpr int kFwdLaunchRegs = 168;
-constexpr int kFwdSoftmaxRegs = 200;
-constexpr int kFwdCtrlRegs = 104;
-static_assert(2 * 128 * kFwdSoftmaxRegs + 128 * kFwdCtrlRegs == kFwdThreads * kFwdLaunchRegs,
+constexpr int kFwdBN = 64;                    // keys per key block
+constexpr int kFwdStages = 6;                 // K/V shared-memory stages
+constexpr int kFwdKVTile = kFwdBN * 128;      // bytes of one K or V stage
+constexpr int kFwdThreads = 640;
+constexpr int kFwdLaunchRegs = 96;
+constexpr int kFwdSoftmaxRegs = 88;
+constexpr int kFwdCtrlRegs = 128;
+static_assert(512 * kFwdSoftmaxRegs + 128 * kFwdCtrlRegs == kFwdThreads * kFwdLaunchRegs,
               "register split must add up to the launch allocation");
-constexpr int kFwdProducerWarp = 8;
-constexpr int kFwdMmaWarp = 9;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
-
-struct FwdParams {
-  int B, T, S, Hq, Hkv, G;
-  int is_time;
-  int L;          // sequence length of a unit (S for space, T for time)
-  int F;          // second index of a unit (T for space, S for time)
-  int agent;      // space: agent token index or -1
-  int window;     // time: window length W >= 1
-  float sl;       // scale * log2(e)
-  int nTok;       // sequence positions per Q tile
-  int rows;       // nTok * G <= 128
-  int ntiles;     // Q tiles per unit
-  int npairs;     // work items per unit
-  long long nitems;
-  int nkb;        // key blocks per unit
-  int resident;   // nkb <= kStages: the unit's K/V stay in smem across its items
-  __nv_bfloat16* o;
-  float* lse;
-  unsigned int* status;
-};
+constexpr int kFwdProducerWarp = 16;
+constexpr int kFwdMmaWarp = 17;               // 17: tile A, 18: tile B
+constexpr int kFwdConvWarp = 19;
 
 struct FwdSmem {
-  uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStages], v_full[kStages], v16_ready[kStages], kv_empty[kStages];
-  // per tile: scores ready, scores taken by the softmax, P ready, P V complete
-  uint64_t s_full[2], s_taken[2], p_full[2], o_done[2];
+  uint64_t q_full[2][2], q_empty[2][2];  // per tile, two Q slots (next item's tile prefetched)
+  uint64_t k_full[kFwdStages], v_full[kFwdStages], v16_ready[kFwdStages], kv_empty[kFwdStages];
+  // per tile: scores ready, scores taken by both halves, P ready, (m, l) posted; P V of
+  // even / odd blocks complete (two barriers, so that a softmax that waits only when it
+  // needs to -- to rescale O, and at the end of an item -- never has two phases of one
+  // barrier outstanding: receiving scores j implies P V j-2 has completed)
+  uint64_t s_full[2], s_taken[2], p_full[2], ml_ready[2];
+  uint64_t o_done[2][2];
   uint64_t drain[2];
   uint32_t tmem_base;
   Ctl ctl;
-  uint8_t vfmt[kStages][4];  // per 32-key chunk of a V stage: 0 = fp16, 1 = bf16
+  uint8_t vfmt[kFwdStages][2];  // per 32-key half of a V stage: 0 = fp16, 1 = bf16
+  uint16_t rowtg[128];          // tile row r -> (r / G) << 8 | (r % G)
+  float2 ml[2][2][128];         // per tile, half, row: (running max, row sum)
 };
-// dynamic smem: [Q0 Q1][K0..][V0..][O staging, 4 KB per softmax warp][FwdSmem]
-constexpr size_t kFwdStageBytes = 8 * 32 * 128;
+// dynamic smem: [Q: tile A slots 0 1, tile B slots 0 1][K stages][V stages]
+//               [O staging, 2 KB per softmax warp][FwdSmem]
+constexpr size_t kFwdStageBytes = 16 * 2048;
 constexpr size_t kFwdTileBytes =
-    size_t(2) * kTile + size_t(2 * kStages) * kKVTile + kFwdStageBytes;
+    size_t(4) * kTile + size_t(2 * kFwdStages) * kFwdKVTile + kFwdStageBytes;
 constexpr size_t kFwdSmemBytes = kFwdTileBytes + 1024 + sizeof(FwdSmem) + 64;
 static_assert(kFwdSmemBytes <= 227 * 1024, "shared memory budget");
 
-struct FwdItem {
-  uint32_t unit;
-  int b, fixed, kvh;
-  int tok0[2];
-  int validB;
-  int key_lo, key_hi;  // allowed key positions of the item lie in [key_lo, key_hi)
-  int kb_lo, kb_hi;    // inclusive key-block range
-};
-
-__device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
-  // the host guarantees nitems < 2^31, so 32-bit unsigned division suffices
-  FwdItem it;
-  const uint32_t ii = static_cast<uint32_t>(i);
-  const uint32_t unit = ii / static_cast<uint32_t>(p.npairs);
-  const int pair = static_cast<int>(ii - unit * static_cast<uint32_t>(p.npairs));
-  it.unit = unit;
-  const uint32_t r = unit / static_cast<uint32_t>(p.Hkv);
-  it.kvh = static_cast<int>(unit - r * static_cast<uint32_t>(p.Hkv));
-  const uint32_t bq = r / static_cast<uint32_t>(p.F);
-  it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
-  it.b = static_cast<int>(bq);
-  const int tA = 2 * pair;
-  it.tok0[0] = tA * p.nTok;
-  it.tok0[1] = (tA + 1) * p.nTok;
-  it.validB = (tA + 1) < p.ntiles;
-  const int last = min(p.L, (it.validB ? tA + 2 : tA + 1) * p.nTok) - 1;
-  if (p.is_time) {
-    it.key_lo = max(0, it.tok0[0] - p.window + 1);
-    it.key_hi = last + 1;
-  } else {
-    it.key_lo = 0;
-    it.key_hi = p.L;
-  }
-  it.kb_lo = it.key_lo / kBN;
-  it.kb_hi = (it.key_hi - 1) / kBN;
-  return it;
-}
-
-__device__ __forceinline__ int block_ncols(const FwdItem& it, int kb) {
-  return min(kBN, it.key_hi - kb * kBN);
-}
-__device__ __forceinline__ int round16(int x) { return (x + 15) & ~15; }
-
-// K/V stage and phase parity of block index bi (0-based within the item).
-struct KvSlot {
-  int stage;
-  uint32_t parity;
-};
-__device__ __forceinline__ KvSlot kv_slot(const FwdParams& p, const FwdItem& it, int bi,
-                                          uint32_t unit_loads, uint32_t stream_cnt) {
-  KvSlot s;
-  if (p.resident) {
-    s.stage = it.kb_lo + bi;
-    s.parity = (unit_loads - 1) & 1u;
-  } else {
-    const uint32_t c = stream_cnt + bi;
-    s.stage = static_cast<int>(c % kStages);
-    s.parity = (c / kStages) & 1u;
-  }
-  return s;
-}
-
-// Bit j set <=> column c0 + j of a score row is allowed: lo <= col < hi and col != ex.
-__device__ __forceinline__ uint32_t keep_bits32(int c0, int lo, int hi, int ex) {
-  const int a = min(max(lo - c0, 0), 32);
-  const int b = min(max(hi - c0, 0), 32);
-  const uint32_t below_b = b >= 32 ? 0xFFFFFFFFu : ((1u << b) - 1u);
-  const uint32_t below_a = a >= 32 ? 0xFFFFFFFFu : ((1u << a) - 1u);
-  uint32_t m = below_b & ~below_a;
-  if (ex >= c0 && ex < c0 + 32) m &= ~(1u << (ex - c0));
-  return m;
-}
-__device__ __forceinline__ void apply_mask32(float* v, uint32_t keep) {
-  if (__any_sync(0xffffffffu, keep != 0xFFFFFFFFu)) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = ((keep >> j) & 1u) ? v[j] : -INFINITY;
-  }
-}
-
-// bounded wait that ignores the abort flag (used only to drain in-flight async work)
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(a, parity)) {
-    if (globaltimer() - t0 > OD_WAIT_LIMIT_NS) break;
-  }
-}
-
-// One pending P V product of the MMA issuer.
+// One pending P V product of an MMA issuer.
 struct PvJob {
-  uint8_t stage, acc, ksteps, vpar;
+  uint8_t stage, vpar, ksteps, acc_a, acc_b;
 };
-
 
 __global__ void __launch_bounds__(kFwdThreads, 1)
     od_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -209,10 +99,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sQ[2] = {base, base + kTile};
-  uint8_t* sK = base + 2 * kTile;
-  uint8_t* sV = sK + kStages * kKVTile;
-  uint8_t* sOst = sV + kStages * kKVTile;
+  uint8_t* sQ = base;  // tile x, slot s at (2x + s) * kTile
+  uint8_t* sK = base + 4 * kTile;
+  uint8_t* sV = sK + kFwdStages * kFwdKVTile;
+  uint8_t* sOst = sV + kFwdStages * kFwdKVTile;
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(base + kFwdTileBytes);
 
   const int tid = threadIdx.x;
@@ -226,32 +116,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // zero the Q-tile rows that TMA never writes (rows >= p.rows)
   {
     const int pad = (kBM - p.rows) * 128;
-    for (int x = tid * 16; x < pad; x += kFwdThreads * 16) {
-      *reinterpret_cast<uint4*>(sQ[0] + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sQ[1] + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
-    }
+    for (int x = tid * 16; x < pad; x += kFwdThreads * 16)
+      for (int t = 0; t < 4; ++t)
+        *reinterpret_cast<uint4*>(sQ + t * kTile + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   if (tid == 0) {
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&sm.q_full[x], 1);
-      mbar_init(&sm.q_empty[x], 1);
-      mbar_init(&sm.o_done[x], 1);
+      for (int q = 0; q < 2; ++q) {
+        mbar_init(&sm.q_full[x][q], 1);
+        mbar_init(&sm.q_empty[x][q], 1);
+      }
+      mbar_init(&sm.o_done[x][0], 1);
+      mbar_init(&sm.o_done[x][1], 1);
       mbar_init(&sm.s_full[x], 1);
-      mbar_init(&sm.s_taken[x], 4);
-      mbar_init(&sm.p_full[x], 4);
+      mbar_init(&sm.s_taken[x], 8);
+      mbar_init(&sm.p_full[x], 8);
+      mbar_init(&sm.ml_ready[x], 8);
+      mbar_init(&sm.drain[x], 1);
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kFwdStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v16_ready[s], 1);
       mbar_init(&sm.kv_empty[s], 2);
     }
-    mbar_init(&sm.drain[0], 1);
-    mbar_init(&sm.drain[1], 1);
     sm.ctl.abort = 0;
     fence_mbar_init();
   }
+  if (tid < 128) sm.rowtg[tid] = static_cast<uint16_t>(((tid / p.G) << 8) | (tid % p.G));
   if (warp == kFwdMmaWarp) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
@@ -263,8 +156,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   Ctl* ctl = &sm.ctl;
   unsigned int* status = p.status;
 
-  if (warp >= 8) {
-    regs_dec<kFwdCtrlRegs>();
+  if (warp >= 16) {
+    regs_inc<kFwdCtrlRegs>();
     if (warp == kFwdProducerWarp) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
@@ -277,24 +170,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (long long i = i0; i < i1 && ok; ++i) {
           const FwdItem it = fwd_decode(p, i);
           auto load_kv = [&](int stage, int kb) {
-            const int kp = kb * kBN;
-            mbar_arrive_expect_tx(&sm.k_full[stage], kKVTile);
-            mbar_arrive_expect_tx(&sm.v_full[stage], kKVTile);
+            const int kp = kb * kFwdBN;
+            mbar_arrive_expect_tx(&sm.k_full[stage], kFwdKVTile);
+            mbar_arrive_expect_tx(&sm.v_full[stage], kFwdKVTile);
+            uint8_t* dk = sK + stage * kFwdKVTile;
+            uint8_t* dv = sV + stage * kFwdKVTile;
             if (p.is_time) {
-              tma_load_5d(sK + stage * kKVTile, &tm_k, &sm.k_full[stage], 0, it.kvh, it.fixed, kp, it.b);
-              tma_load_5d(sV + stage * kKVTile, &tm_v, &sm.v_full[stage], 0, it.kvh, it.fixed, kp, it.b);
+              tma_load_5d(dk, &tm_k, &sm.k_full[stage], 0, it.kvh, it.fixed, kp, it.b);
+              tma_load_5d(dv, &tm_v, &sm.v_full[stage], 0, it.kvh, it.fixed, kp, it.b);
             } else {
-              tma_load_5d(sK + stage * kKVTile, &tm_k, &sm.k_full[stage], 0, it.kvh, kp, it.fixed, it.b);
-              tma_load_5d(sV + stage * kKVTile, &tm_v, &sm.v_full[stage], 0, it.kvh, kp, it.fixed, it.b);
+              tma_load_5d(dk, &tm_k, &sm.k_full[stage], 0, it.kvh, kp, it.fixed, it.b);
+              tma_load_5d(dv, &tm_v, &sm.v_full[stage], 0, it.kvh, kp, it.fixed, it.b);
             }
           };
           auto load_q = [&](int x, uint32_t& n) -> bool {
-            if (n > 0 && !wait_bar(&sm.q_empty[x], (n - 1) & 1u, ctl, status, 1)) return false;
-            mbar_arrive_expect_tx(&sm.q_full[x], p.rows * 128);
+            const int q = n & 1;
+            if (n >= 2 && !wait_bar(&sm.q_empty[x][q], ((n >> 1) - 1) & 1u, ctl, status, 1)) return false;
+            uint8_t* dst = sQ + (2 * x + q) * kTile;
+            mbar_arrive_expect_tx(&sm.q_full[x][q], p.rows * 128);
             if (p.is_time)
-              tma_load_5d(sQ[x], &tm_q, &sm.q_full[x], 0, it.kvh * p.G, it.fixed, it.tok0[x], it.b);
+              tma_load_5d(dst, &tm_q, &sm.q_full[x][q], 0, it.kvh * p.G, it.fixed, it.tok0[x], it.b);
             else
-              tma_load_5d(sQ[x], &tm_q, &sm.q_full[x], 0, it.kvh * p.G, it.tok0[x], it.fixed, it.b);
+              tma_load_5d(dst, &tm_q, &sm.q_full[x][q], 0, it.kvh * p.G, it.tok0[x], it.fixed, it.b);
             ++n;
             return true;
           };
@@ -317,8 +214,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int nb = it.kb_hi - it.kb_lo + 1;
             for (int bi = 0; bi < nb && ok; ++bi) {
               const uint32_t c = stream_cnt + bi;
-              const int stage = static_cast<int>(c % kStages);
-              const uint32_t n = c / kStages;
+              const int stage = static_cast<int>(c % kFwdStages);
+              const uint32_t n = c / kFwdStages;
               if (n > 0) ok = wait_bar(&sm.kv_empty[stage], (n - 1) & 1u, ctl, status, 3);
               if (ok) load_kv(stage, it.kb_lo + bi);
             }
@@ -326,8 +223,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         // make sure no TMA load is still writing into this CTA's smem when it exits
-        if (qn0 > 0) drain_wait(&sm.q_full[0], (qn0 - 1) & 1u);
-        if (qn1 > 0) drain_wait(&sm.q_full[1], (qn1 - 1) & 1u);
+        for (int x = 0; x < 2; ++x)
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t n = x ? qn1 : qn0;
+            const uint32_t uses = n / 2 + (static_cast<uint32_t>(q) < (n & 1u) ? 1u : 0u);
+            if (uses > 0) drain_wait(&sm.q_full[x][q], (uses - 1) & 1u);
+          }
         if (p.resident) {
           if (unit_loads > 0)
             for (int s = 0; s < p.nkb; ++s) {
@@ -335,9 +236,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               drain_wait(&sm.v_full[s], (unit_loads - 1) & 1u);
             }
         } else {
-          for (int s = 0; s < kStages; ++s) {
+          for (int s = 0; s < kFwdStages; ++s) {
             const uint32_t uses =
-                stream_cnt / kStages + (static_cast<uint32_t>(s) < stream_cnt % kStages ? 1u : 0u);
+                stream_cnt / kFwdStages + (static_cast<uint32_t>(s) < stream_cnt % kFwdStages ? 1u : 0u);
             if (uses > 0) {
               drain_wait(&sm.k_full[s], (uses - 1) & 1u);
               drain_wait(&sm.v_full[s], (uses - 1) & 1u);
@@ -347,17 +248,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     } else if (warp == kFwdMmaWarp || warp == kFwdMmaWarp + 1) {
       // ---------------------------------------------------------- MMA issuers
-      // Warp 9 issues tile A's MMAs, warp 10 tile B's, each in order: Q K^T(0); then for
-      // every block j: wait until the softmax has taken scores j, issue Q K^T(j+1) into the
-      // tile's other score buffer; wait for P(j), issue P V(j).  At the end of an item the last
-      // P V goes out at once.  Both issuers walk every item (tile B also the items it has no
-      // rows in) and release every K/V fill they have seen arrive, so kv_empty counts two.
-      {  // whole warp in lockstep; one elected lane issues
+      // Warp 17 issues tile A's MMAs, warp 18 tile B's, each in order: Q K^T(0); then for
+      // every block j: wait until both halves have taken scores j, issue Q K^T(j+1) into the
+      // tile's other score buffer; wait for P(j), issue P V(j) as O_a += P_a V_a (keys 0-31)
+      // and O_b += P_b V_b (keys 32-63).  At the end of an item the last P V goes out at
+      // once.  Both issuers walk every item (tile B also the items it has no rows in) and
+      // release every K/V fill they have seen arrive, so kv_empty counts two.
+      {
         const int x = warp - kFwdMmaWarp;  // 0: tile A, 1: tile B
         const uint32_t idesc_pv_bf16 = idesc_bf16(128, 64, 0, 1);
         const uint32_t idesc_pv_fp16 = idesc_fp16(128, 64, 0, 1);
-        const uint32_t tOx = tmem + 384u + 64u * x;
+        const uint32_t tOa = tmem + 256u * x + 128u, tOb = tOa + 64u;
         uint32_t js = 0, jp = 0, qn = 0, unit_loads = 0, sbase = 0;
+        int qs = 0;  // Q slot of the current item
         long long prev_unit = -1;
         PvJob f0{}, f1{};
         int npend = 0;  // pending P V products; the oldest is slot jp & 1
@@ -367,14 +270,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!__all_sync(0xffffffffu, wait_bar(&sm.p_full[x], jp & 1u, ctl, status, 9))) return false;
           if (!__all_sync(0xffffffffu, wait_bar(&sm.v16_ready[jb.stage], jb.vpar, ctl, status, 10))) return false;
           tc_fence_after();
-          const uint64_t b = sdesc_sw128(smem_u32(sV + jb.stage * kKVTile), 1024, 1024);
-          const uint32_t a = tmem + 192u * x + 96u * (jp & 1u);
-          const uint32_t fmt = *reinterpret_cast<const uint32_t*>(sm.vfmt[jb.stage]);
-          for (int k = 0; k < jb.ksteps; ++k) {
-            const uint32_t idesc = ((fmt >> (8 * (k >> 1))) & 0xFFu) ? idesc_pv_bf16 : idesc_pv_fp16;
-            mma_ts_w(tOx, a + 8 * k, b + (2048 >> 4) * k, idesc, (jb.acc || k > 0));
-          }
-          mma_commit_w(&sm.o_done[x]);
+          const uint64_t b = sdesc_sw128(smem_u32(sV + jb.stage * kFwdKVTile), 1024, 1024);
+          const uint32_t a = tmem + 256u * x + 64u * (jp & 1u);
+          const uint32_t ida = sm.vfmt[jb.stage][0] ? idesc_pv_bf16 : idesc_pv_fp16;
+          const uint32_t idb = sm.vfmt[jb.stage][1] ? idesc_pv_bf16 : idesc_pv_fp16;
+          // O_a takes keys 0-31 of the block; O_b keys 32-63 -- and on an item's first block
+          // at least one k-step even when the block is shorter (its P_b is then all zero),
+          // so that O_b always holds this item's (finite) sum
+          const int ka = jb.ksteps < 2 ? jb.ksteps : 2;
+          const int kb = jb.ksteps > 2 ? jb.ksteps - 2 : (jb.acc_b ? 0 : 1);
+          for (int k = 0; k < ka; ++k)
+            mma_ts_w(tOa, a + 8 * k, b + (2048 >> 4) * k, ida, (jb.acc_a || k > 0));
+          for (int k = 0; k < kb; ++k)
+            mma_ts_w(tOb, a + 32 + 8 * k, b + (2048 >> 4) * (2 + k), idb, (jb.acc_b || k > 0));
+          mma_commit_w(&sm.o_done[x][jp & 1u]);
           OD_TP(12 + x, 0, (int)jp);
           ++jp;
           --npend;
@@ -400,8 +309,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!p.resident) {
               for (int bi = 0; bi < nb && ok; ++bi) {
                 const uint32_t c = sbase + static_cast<uint32_t>(bi);
-                const int stage = static_cast<int>(c % kStages);
-                ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[stage], (c / kStages) & 1u, ctl, status, 12));
+                const int stage = static_cast<int>(c % kFwdStages);
+                ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[stage], (c / kFwdStages) & 1u, ctl, status, 12));
                 if (ok) mma_commit_w(&sm.kv_empty[stage]);
               }
             }
@@ -413,25 +322,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!ok) break;
             if (js > 0 && !__all_sync(0xffffffffu, wait_bar(&sm.s_taken[x], (js - 1) & 1u, ctl, status, 13))) { ok = false; break; }
             if (bi == 0) {
-              if (!__all_sync(0xffffffffu, wait_bar(&sm.q_full[x], qn & 1u, ctl, status, 14))) { ok = false; break; }
+              qs = qn & 1;
+              if (!__all_sync(0xffffffffu, wait_bar(&sm.q_full[x][qs], (qn >> 1) & 1u, ctl, status, 14))) { ok = false; break; }
               ++qn;
             }
-            KvSlot ks;
-            if (p.resident) {
-              ks.stage = it.kb_lo + bi;
-              ks.parity = (unit_loads - 1) & 1u;
-            } else {
-              const uint32_t c = sbase + static_cast<uint32_t>(bi);
-              ks.stage = static_cast<int>(c % kStages);
-              ks.parity = (c / kStages) & 1u;
-            }
+            const KvSlot ks = kv_slot(p, it, bi, unit_loads, sbase, kFwdStages);
             if (!__all_sync(0xffffffffu, wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 15))) { ok = false; break; }
             tc_fence_after();
-            const int n = round16(block_ncols(it, it.kb_lo + bi));
+            const int n = round16(block_ncols(it, it.kb_lo + bi, kFwdBN));
             const uint32_t idesc = idesc_bf16(128, n, 0, 0);
-            const uint64_t a = sdesc_sw128(smem_u32(sQ[x]), 16, 1024);
-            const uint64_t b = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 16, 1024);
-            const uint32_t d = tmem + 192u * x + 96u * (js & 1u);
+            const uint64_t a = sdesc_sw128(smem_u32(sQ + (2 * x + qs) * kTile), 16, 1024);
+            const uint64_t b = sdesc_sw128(smem_u32(sK + ks.stage * kFwdKVTile), 16, 1024);
+            const uint32_t d = tmem + 256u * x + 64u * (js & 1u);
 #pragma unroll
             for (int k = 0; k < 4; ++k) mma_ss_w(d, a + 2 * k, b + 2 * k, idesc, k > 0);
             mma_commit_w(&sm.s_full[x]);
@@ -439,28 +341,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             PvJob jb;
             jb.stage = static_cast<uint8_t>(ks.stage);
             jb.vpar = static_cast<uint8_t>(ks.parity);
-            jb.acc = bi > 0;
             jb.ksteps = static_cast<uint8_t>(n >> 4);
+            jb.acc_a = bi > 0;
+            jb.acc_b = bi > 0;
             if (js & 1u) f1 = jb; else f0 = jb;
             ++js;
             ++npend;
-            if (bi == nb - 1) mma_commit_w(&sm.q_empty[x]);
+            if (bi == nb - 1) mma_commit_w(&sm.q_empty[x][qs]);
             while (ok && npend >= 2) ok = issue_pv();
           }
           // the item's last P V goes out as soon as its P is ready
           while (ok && npend > 0) ok = issue_pv();
           sbase += static_cast<uint32_t>(nb);
         }
-        // wait until every MMA issued by this thread has completed before TMEM is freed
+        // wait until every MMA issued by this warp has completed before TMEM is freed
         mma_commit_w(&sm.drain[x]);
         drain_wait(&sm.drain[x], 0);
       }
     } else {
-      // ---------------------------------------------------------- V converter (warp 11)
+      // ---------------------------------------------------------- V converter (warp 19)
       // P V runs in fp16: P in [0, 256] loses 8x less to rounding than in bf16.  Each fill
-      // of a V stage is converted in place, per 32-key chunk, when the chunk's magnitude
-      // is inside a safe fp16 range (2^-10 <= max|v| <= 2^15, or all zero); otherwise the
-      // chunk stays bf16 and the softmax and MMA use bf16 for those keys.
+      // of a V stage is converted in place, per 32-key half, when the half's magnitude is
+      // inside a safe fp16 range (2^-10 <= max|v| <= 2^15, or all zero); otherwise the half
+      // stays bf16 and the softmax and MMA use bf16 for those keys.
       long long prev_unit = -1;
       uint32_t unit_loads = 0, stream_cnt = 0;
       bool ok = true;
@@ -468,8 +371,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         bool w = wait_bar(&sm.v_full[stage], parity, ctl, status, 4);
         if (!__all_sync(0xffffffffu, w)) return false;
 #pragma unroll 1
-        for (int cc = 0; cc < kBN / 32; ++cc) {
-          uint4* chunk = reinterpret_cast<uint4*>(sV + stage * kKVTile + cc * 32 * 128);
+        for (int cc = 0; cc < kFwdBN / 32; ++cc) {
+          uint4* chunk = reinterpret_cast<uint4*>(sV + stage * kFwdKVTile + cc * 32 * 128);
           float mx = 0.f;
 #pragma unroll 2
           for (int jj = 0; jj < 8; ++jj) {
@@ -514,23 +417,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int nb = it.kb_hi - it.kb_lo + 1;
           for (int bi = 0; bi < nb && ok; ++bi) {
             const uint32_t c = stream_cnt + bi;
-            ok = convert(static_cast<int>(c % kStages), (c / kStages) & 1u);
+            ok = convert(static_cast<int>(c % kFwdStages), (c / kFwdStages) & 1u);
           }
           stream_cnt += nb;
         }
       }
     }
   } else {
-    regs_inc<kFwdSoftmaxRegs>();
+    regs_dec<kFwdSoftmaxRegs>();
     // ------------------------------------------------------------ softmax warpgroups
-    const int x = warp >> 2;         // 0: tile A, 1: tile B
-    const int r = tid & 127;         // row of the tile == TMEM lane
+    const int x = warp >> 3;         // 0: tile A, 1: tile B
+    const int hf = (warp >> 2) & 1;  // 0: columns 0-31 of each block, 1: columns 32-63
+    const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + 384 + x * 64 + lane_off;
+    const uint32_t tX = tmem + 256u * x + lane_off;
+    const uint32_t tO = tX + 128u + 64u * hf;  // this half's accumulator
     const int G = p.G;
     const int tok = r / G;
     const int g = r - tok * G;
-    uint32_t jS = 0, jP = 0;
+    uint32_t jS = 0, jP = 0, jM = 0;
     long long prev_unit = -1;
     uint32_t unit_loads = 0, stream_next = 0;
     bool ok = true;
@@ -550,10 +455,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int bi = 0; bi < nb; ++bi) {
         const int kb = it.kb_lo + bi;
-        const int kbase = kb * kBN;
-        const int ncols = block_ncols(it, kb);
-        const int n32 = (ncols + 31) >> 5;
-        const uint32_t tS = tmem + 192u * x + 96u * (jS & 1u) + lane_off;
+        const int kbase = kb * kFwdBN;
+        const int ncols = block_ncols(it, kb, kFwdBN);
         int lo, hi, ex;
         if (p.is_time) {
           lo = pos - p.window + 1 - kbase;
@@ -562,116 +465,90 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         } else {
           lo = 0;
           hi = ncols;
-          ex = (p.agent >= kbase && p.agent < kbase + kBN && pos != p.agent) ? p.agent - kbase : -1;
+          ex = (p.agent >= kbase && p.agent < kbase + kFwdBN && pos != p.agent) ? p.agent - kbase : -1;
         }
+        // masking is needed only when this half's 32 columns are not all allowed
+        const int c0 = 32 * hf;
+        const bool partial = (lo > c0) || (hi < c0 + 32) || (ex >= c0 && ex < c0 + 32);
         OD_TP(20, (int)i, bi);
-        ok = wait_bar(&sm.s_full[x], jS & 1u, ctl, status, 5);
-        ok = __all_sync(0xffffffffu, ok);
+        ok = __all_sync(0xffffffffu, wait_bar(&sm.s_full[x], jS & 1u, ctl, status, 5));
         if (!ok) break;
+        const uint32_t tS = tX + 64u * (jS & 1u) + 32u * hf;
         ++jS;
         if (lane == 0) mbar_arrive(&sm.s_taken[x]);
-        OD_TP(21, (int)i, bi);
         tc_fence_after();
-        // Pass 1 over the scores (32 columns per step, next step's TMEM load in flight):
-        // masks and the row maximum.  The loops stay rolled to keep the code small.
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-        {
-          // every chunk's TMEM load in flight at once: one round trip
-          float v[96];
+        float v[32];
+        tmem_ld32(tS, v);
+        tmem_wait_ld_dep32(v);
+        OD_TP(21, (int)i, bi);
+        if (__any_sync(0xffffffffu, partial)) {
+          const uint32_t keep = keep_bits32(c0, lo, hi, ex);
 #pragma unroll
-          for (int c = 0; c < 3; ++c)
-            if (c < n32) tmem_ld32(tS + 32 * c, v + 32 * c);
-          tmem_wait_ld_dep32(v);
-          tmem_wait_ld_dep32(v + 32);
-          tmem_wait_ld_dep32(v + 64);
-#pragma unroll
-          for (int c = 0; c < 3; ++c)
-            if (c < n32) {
-              apply_mask32(v + 32 * c, keep_bits32(32 * c, lo, hi, ex));
-#pragma unroll
-              for (int jj = 0; jj < 32; jj += 8) {
-                mx0 = max3(mx0, v[32 * c + jj], v[32 * c + jj + 1]);
-                mx1 = max3(mx1, v[32 * c + jj + 2], v[32 * c + jj + 3]);
-                mx2 = max3(mx2, v[32 * c + jj + 4], v[32 * c + jj + 5]);
-                mx3 = max3(mx3, v[32 * c + jj + 6], v[32 * c + jj + 7]);
-              }
-            }
+          for (int j = 0; j < 32; ++j) v[j] = ((keep >> j) & 1u) ? v[j] : -INFINITY;
         }
+        // row maximum of the 32 columns: four chains of 3-input max over v[0..31]
+        float mx0 = max3(v[0], v[1], v[2]), mx1 = max3(v[3], v[4], v[5]);
+        float mx2 = max3(v[6], v[7], v[8]), mx3 = max3(v[9], v[10], v[11]);
+#pragma unroll
+        for (int jj = 12; jj < 28; jj += 8) {
+          mx0 = max3(mx0, v[jj], v[jj + 1]);
+          mx1 = max3(mx1, v[jj + 2], v[jj + 3]);
+          mx2 = max3(mx2, v[jj + 4], v[jj + 5]);
+          mx3 = max3(mx3, v[jj + 6], v[jj + 7]);
+        }
+        mx0 = max3(mx0, v[28], v[29]);
+        mx1 = max3(mx1, v[30], v[31]);
         const float mb = fmaxf(max3(mx0, mx1, mx2), mx3);
-        OD_TP(23, (int)i, bi);
         const float mnew = mb * p.sl;
         float alpha = 1.f;
         bool rescale = false;
         if (mb != -INFINITY && (m_used == -INFINITY || mnew > m_used + kRescaleThreshold)) {
           if (m_used != -INFINITY) {
             alpha = ex2(m_used - mnew);
-            rescale = bi > 0;
+            rescale = true;
           }
           m_used = mnew;
           l *= alpha;
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
         // V of this block must be converted before P's format can be chosen
-        const KvSlot ks = kv_slot(p, it, bi, unit_loads, stream_cnt);
-        ok = wait_bar(&sm.v16_ready[ks.stage], ks.parity, ctl, status, 6);
-        ok = __all_sync(0xffffffffu, ok);
+        const KvSlot ks = kv_slot(p, it, bi, unit_loads, stream_cnt, kFwdStages);
+        ok = __all_sync(0xffffffffu, wait_bar(&sm.v16_ready[ks.stage], ks.parity, ctl, status, 6));
         if (!ok) break;
-        OD_TP(25, (int)i, bi);
-        const uint32_t fmt_bits = *reinterpret_cast<const uint32_t*>(sm.vfmt[ks.stage]);
         const float2 sl2 = make_float2(p.sl, p.sl);
         const float2 nm2 = make_float2(-msub, -msub);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
-        // Pass 2: exponentials, row sum, and P written in place over the first half of the
-        // score buffer (the P pairs of step c land in columns already read by steps <= c).
-        {
-          float va[32];
-          tmem_ld32(tS, va);
-#pragma unroll 1
-          for (int c = 0; c < n32; ++c) {
-            tmem_wait_ld_dep32(va);
-            float2 pp[16];
-            apply_mask32(va, keep_bits32(32 * c, lo, hi, ex));
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+        uint32_t pk[16];
+        if (sm.vfmt[ks.stage][hf] == 0) {  // warp-uniform: the format of this half's V keys
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 xx = __ffma2_rn(make_float2(va[2 * j], va[2 * j + 1]), sl2, nm2);
-              pp[j] = make_float2(ex2(xx.x), ex2(xx.y));
-            }
-            if (c + 1 < n32) tmem_ld32(tS + 32 * (c + 1), va);
+          for (int j = 0; j < 16; ++j) {
+            const float2 xx = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]), sl2, nm2);
+            const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+            if (j & 1) acc1 = __fadd2_rn(acc1, pp); else acc0 = __fadd2_rn(acc0, pp);
+            pk[j] = pack_f16x2(pp.x, pp.y);
+          }
+        } else {
 #pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-              acc0 = __fadd2_rn(acc0, pp[j]);
-              acc1 = __fadd2_rn(acc1, pp[j + 1]);
-              acc2 = __fadd2_rn(acc2, pp[j + 2]);
-              acc3 = __fadd2_rn(acc3, pp[j + 3]);
-            }
-            uint32_t pk[16];
-            if ((fmt_bits >> (8 * c)) & 0xFFu) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(pp[j].x, pp[j].y);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) pk[j] = pack_f16x2(pp[j].x, pp[j].y);
-            }
-            tmem_st16(tS + 16 * c, pk);
+          for (int j = 0; j < 16; ++j) {
+            const float2 xx = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]), sl2, nm2);
+            const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+            if (j & 1) acc1 = __fadd2_rn(acc1, pp); else acc0 = __fadd2_rn(acc0, pp);
+            pk[j] = pack_bf16x2(pp.x, pp.y);
           }
         }
+        tmem_st16(tS, pk);  // P pairs over the first 16 of this half's 32 score columns
         {
-          const float2 a01 = __fadd2_rn(acc0, acc1);
-          const float2 a23 = __fadd2_rn(acc2, acc3);
-          const float2 a = __fadd2_rn(a01, a23);
+          const float2 a = __fadd2_rn(acc0, acc1);
           l += a.x + a.y;
         }
         OD_TP(26, (int)i, bi);
-        // The previous block's P V must be complete before this block's P is released
-        // (keeps o_done exactly one phase behind, and O stable for a rescale).
-        if (jP > 0) {
-          ok = wait_bar(&sm.o_done[x], (jP - 1) & 1u, ctl, status, 7);
-          ok = __all_sync(0xffffffffu, ok);
+        // A rescale of O needs the previous block's P V complete (this block's P V is issued
+        // only after p_full below).  P(j) itself overwrites scores j, written after P V j-2.
+        if (__any_sync(0xffffffffu, rescale && bi > 0)) {
+          ok = __all_sync(0xffffffffu, wait_bar(&sm.o_done[x][(jP - 1) & 1u], ((jP - 1) >> 1) & 1u, ctl, status, 7));
           if (!ok) break;
           tc_fence_after();
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float f = rescale ? alpha : 1.f;
+          const float f = (rescale && bi > 0) ? alpha : 1.f;
 #pragma unroll 1
           for (int h = 0; h < 8; ++h) {
             uint32_t u[8];
@@ -691,59 +568,79 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
-      ok = wait_bar(&sm.o_done[x], (jP - 1) & 1u, ctl, status, 8);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
       OD_TP(30, (int)i, 0);
+      ok = __all_sync(0xffffffffu, wait_bar(&sm.o_done[x][(jP - 1) & 1u], ((jP - 1) >> 1) & 1u, ctl, status, 8));
+      if (!ok) break;
       tc_fence_after();
-      float o[64];
-      tmem_ld32(tO, o);
-      tmem_ld32(tO + 32, o + 32);
-      tmem_wait_ld_dep32(o);
-      tmem_wait_ld_dep32(o + 32);
-      // Each warp stages its 32 rows (bf16, 128 B each, XOR-swizzled by row to keep the
-      // shared-memory accesses conflict free) and then stores them coalesced: one
-      // instruction writes 4 whole rows, 8 lanes per row.
+      OD_TP(33, (int)i, 0);
+      sm.ml[x][hf][r] = make_float2(m_used, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.ml_ready[x]);
+      ok = __all_sync(0xffffffffu, wait_bar(&sm.ml_ready[x], jM & 1u, ctl, status, 16));
+      if (!ok) break;
+      ++jM;
+      OD_TP(32, (int)i, 0);
+      const float2 other = sm.ml[x][hf ^ 1][r];
+      const float M = fmaxf(m_used, other.x);
+      const float w_me = (m_used == -INFINITY) ? 0.f : ex2(m_used - M);
+      const float w_ot = (other.x == -INFINITY) ? 0.f : ex2(other.x - M);
+      const float lsum = l * w_me + other.y * w_ot;
+      const float inv = 1.f / lsum;
+      // (both accumulators hold this item's finite sums; a half that saw no allowed key
+      // has weight 0)
+      const float wa = (hf ? w_ot : w_me) * inv, wb = (hf ? w_me : w_ot) * inv;
+      if (hf == 0 && row_ok) {
+        const int hq = it.kvh * G + g;
+        const long long t_idx = p.is_time ? pos : it.fixed;
+        const long long s_idx = p.is_time ? it.fixed : pos;
+        p.lse[((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + hq] =
+            (M + log2f(lsum)) * 0.69314718055994531f;
+      }
+      // This half writes output columns [32 hf, 32 hf + 32): each warp stages its 32 rows
+      // (64 bytes each, 16-byte chunks XOR-swizzled by row) and stores them coalesced.
+      uint8_t* stg = sOst + warp * 2048;
+      const uint32_t tOa = tX + 128u + 32u * hf, tOb = tOa + 64u;
+#pragma unroll 1
+      for (int c2 = 0; c2 < 2; ++c2) {
+        float oa[16], ob[16];
+        tmem_ld16(tOa + 16 * c2, oa);
+        tmem_ld16(tOb + 16 * c2, ob);
+        tmem_wait_ld_dep16(oa);
+        tmem_wait_ld_dep16(ob);
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 y = __ffma2_rn(make_float2(oa[2 * j], oa[2 * j + 1]), make_float2(wa, wa),
+                                      __fmul2_rn(make_float2(ob[2 * j], ob[2 * j + 1]), make_float2(wb, wb)));
+          w[j] = pack_bf16x2(y.x, y.y);
+        }
+        *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * c2) ^ (lane & 3)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * c2 + 1) ^ (lane & 3)) << 4)) =
+            make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      __syncwarp();
+      OD_TP(34, (int)i, 0);
       {
-        const float inv = 1.f / l;
-        uint8_t* stg = sOst + (warp & 7) * 4096;
-        const int wr = lane;  // row within the warp
+        const int sub = lane >> 2, ch = lane & 3;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 wv;
-          wv.x = pack_bf16x2(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
-          wv.y = pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-          wv.z = pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-          wv.w = pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
-          *reinterpret_cast<uint4*>(stg + wr * 128 + ((c ^ (wr & 7)) << 4)) = wv;
-        }
-        if (row_ok) {
-          const int hq = it.kvh * G + g;
-          const long long t_idx = p.is_time ? pos : it.fixed;
-          const long long s_idx = p.is_time ? it.fixed : pos;
-          p.lse[((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + hq] =
-              (m_used + log2f(l)) * 0.69314718055994531f;
-        }
-        __syncwarp();
-        const int sub = lane >> 3, ch = lane & 7;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int rr = 4 * k + sub;                // row within the warp
+        for (int k = 0; k < 4; ++k) {
+          const int rr = 8 * k + sub;                // row within the warp
           const int rt = (warp & 3) * 32 + rr;       // row within the tile
-          const int tk = rt / G;
-          const int gg = rt - tk * G;
-          const int ps = mytok0 + tk;
+          const int tg = sm.rowtg[rt];
+          const int gg = tg & 0xFF;
+          const int ps = mytok0 + (tg >> 8);
           if (rt < p.rows && ps < p.L) {
             const long long t_idx = p.is_time ? ps : it.fixed;
             const long long s_idx = p.is_time ? it.fixed : ps;
             const long long row =
                 ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + gg;
-            const uint4 wv = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
-            reinterpret_cast<uint4*>(p.o + row * 64)[ch] = wv;
+            const uint4 wv = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((ch ^ (rr & 3)) << 4));
+            reinterpret_cast<uint4*>(p.o + row * 64 + 32 * hf)[ch] = wv;
           }
         }
-        __syncwarp();
       }
+      __syncwarp();
       OD_TP(31, (int)i, 0);
     }
   }
