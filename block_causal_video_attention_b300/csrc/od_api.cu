@@ -252,6 +252,7 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     dp.amax = amax;
     const long long grid = f.nitems < num_ctas ? f.nitems : num_ctas;
     amax_slots = static_cast<int>(grid);
+    dp.amax_slots = amax_slots;
     // 1. Delta pass, 2. dQ
     od::od_bwd_dq_kernel<true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;

@@ -11,12 +11,13 @@
 //        workspace.  It equals <dO, O> for the exact O; the bf16 O passed in would give
 //        Delta only to ~1e-2 absolute, which the gradients inherit.
 //   2. od_bwd_dq_kernel<false>: Q-tile stationary (the forward's work items and warp roles):
-//        S = Q K^T and dP = dO V^T per 96-key block in TMEM; dS split into bf16 high parts
-//        (in place over S) and bf16 residuals (in place over dP); dQ += dS K as two MMAs per
-//        step into one fp32 accumulator, written once per tile.
+//        S = Q K^T and dP = dO V^T per 96-key block in TMEM; dS written in place over S as
+//        fp16 times 2^eds; dQ += dS K into one fp32 accumulator, written once per tile.  Q
+//        tiles and K blocks are rewritten as scaled fp16 in shared memory first (see "fp16
+//        operand scaling"), so S runs on exact fp16 operands and dQ on fp16.
 //   3. od_bwd_dkdv_kernel:  key-block stationary: a CTA item is (unit, 128-key block);
 //        for every Q tile that can see the block, S^T = K Q^T and dP^T = V dO^T in TMEM
-//        (keys on TMEM lanes), P^T and dS^T written in place (bf16), then
+//        (keys on TMEM lanes), P^T and dS^T written in place (scaled fp16), then
 //        dV += P^T dO and dK += dS^T Q accumulate in TMEM.  All G heads of the group are
 //        rows of the same Q tile, so the GQA reduction of dK/dV happens on chip.
 #pragma once
@@ -76,6 +77,24 @@ __device__ __forceinline__ int fp16_shift(float a) {
   return ok ? min(max(15 - E, -60), 60) : 0;
 }
 
+// Rewrite `bytes` of packed bf16 pairs as fp16 pairs times 2^e, in place (one warp).
+__device__ __forceinline__ void to_fp16_scaled(uint8_t* buf, int bytes, float s, int lane) {
+  uint4* p = reinterpret_cast<uint4*>(buf);
+  const float2 s2 = make_float2(s, s);
+#pragma unroll 4
+  for (int x = lane; x < (bytes >> 4); x += 32) {
+    uint4 d = p[x];
+    uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float2 f = __fmul2_rn(make_float2(__uint_as_float(w[h] << 16),
+                                              __uint_as_float(w[h] & 0xFFFF0000u)), s2);
+      w[h] = pack_f16x2(f.x, f.y);
+    }
+    p[x] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // ============================================================================ dQ kernel
 // Work items, Q tiles, key blocks and K/V staging as in the forward (FwdParams, fwd_decode).
 // TMEM per tile x (256 columns at 256 x): S [0,96), dP [96,192), dQ [192,256).
@@ -89,6 +108,7 @@ struct DqParams {
   const float* lse;       // forward logsumexp (natural log)
   float* delta;           // Delta per query row (written by the Delta pass, read otherwise)
   float* amax;            // Delta pass: this CTA's max|Q|, max|K|, max|V|, max|dO| at 4*blockIdx.x
+  int amax_slots;         // dQ pass: slots the Delta pass wrote (scales for the fp16 products)
   float scale;
   __nv_bfloat16* dq;
   float* dq_f32;          // optional
@@ -97,10 +117,12 @@ struct DqParams {
 struct DqSmem {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kDqStages], v_full[kDqStages], kv_empty[kDqStages];
+  uint64_t q16[2], k16[kDqStages];  // dQ pass: Q tile / K stage rewritten as scaled fp16
   uint64_t s_full[2], ds_full[2], dq_done[2];
   uint64_t drain[2];
   uint32_t tmem_base;
   Ctl ctl;
+  int eq, ek, eds;  // dQ pass: fp16 scale exponents
 };
 // smem: [Q0 Q1 dO0 dO1][K stages][V stages][dQ staging 8 x 4 KB][DqSmem]
 constexpr size_t kDqTileBytes = size_t(4) * kTile + size_t(2 * kDqStages) * kKVTile + 8 * 4096;
@@ -146,6 +168,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.q_full[x], 1);
       mbar_init(&sm.q_empty[x], kDelta ? 2 : 1);  // + the range scanner in the Delta pass
+      mbar_init(&sm.q16[x], 1);
       mbar_init(&sm.s_full[x], 1);
       mbar_init(&sm.ds_full[x], 4);
       mbar_init(&sm.dq_done[x], 1);
@@ -155,9 +178,39 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.kv_empty[s], kDelta ? 3 : 2);
+      mbar_init(&sm.k16[s], 1);
     }
     sm.ctl.abort = 0;
     fence_mbar_init();
+  }
+  if (!kDelta && warp == kQsProducerWarp) {
+    // operand ranges recorded by the Delta pass -> scale exponents
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    bool bad[4] = {false, false, false, false};
+    for (int sl = lane; sl < dp.amax_slots; sl += 32) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float v = dp.amax[4 * sl + c];
+        a[c] = fmaxf(a[c], v);
+        bad[c] |= !(v == v);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        a[c] = fmaxf(a[c], __shfl_xor_sync(0xffffffffu, a[c], o));
+        bad[c] |= __shfl_xor_sync(0xffffffffu, bad[c], o);
+      }
+      if (bad[c]) a[c] = __int_as_float(0x7fc00000);
+    }
+    if (lane == 0) {
+      sm.eq = fp16_shift(a[0]);
+      sm.ek = fp16_shift(a[1]);
+      bool ok_do, ok_v;
+      const int Edo = amax_exp(a[3], &ok_do), Ev = amax_exp(a[2], &ok_v);
+      sm.eds = (ok_do && ok_v) ? min(max(15 - (Edo + Ev + 7), -60), 60) : 0;
+    }
   }
   if (warp == kQsMmaWarp) {
     tmem_alloc(&sm.tmem_base, 512);
@@ -169,10 +222,57 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   Ctl* ctl = &sm.ctl;
   unsigned int* status = p.status;
+  const int eq = kDelta ? 0 : sm.eq, ek = kDelta ? 0 : sm.ek, eds = kDelta ? 0 : sm.eds;
 
   if (warp >= 8) {
     regs_dec<kQsCtrlRegs>();
-    if (kDelta && warp == 11) {
+    if (!kDelta && warp == 11) {
+      // ---------------------------------------------------------- operand conversion
+      // dQ pass: every Q tile and K block is rewritten in place as fp16 times 2^eq / 2^ek (S
+      // then runs on fp16 operands -- exact, the scales fold into the exponent -- and
+      // dQ += dS K on fp16 dS) and released to the MMA issuers through q16 / k16.  Walks the
+      // producer's fills in its order.
+      const float sq = ldexpf(1.f, eq), sk = ldexpf(1.f, ek);
+      long long prev_unit = -1;
+      uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
+      bool ok = true;
+      auto conv_k = [&](int stage, uint32_t parity) -> bool {
+        if (!__all_sync(0xffffffffu, wait_bar(&sm.k_full[stage], parity, ctl, status, 19))) return false;
+        to_fp16_scaled(sK + stage * kKVTile, kKVTile, sk, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.k16[stage]);
+        return true;
+      };
+      for (long long i = i0; i < i1 && ok; ++i) {
+        const FwdItem it = fwd_decode(p, i);
+        const int nb = it.kb_hi - it.kb_lo + 1;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (x == 1 && !it.validB) break;
+          ok = __all_sync(0xffffffffu, wait_bar(&sm.q_full[x], qn[x] & 1u, ctl, status, 17));
+          if (!ok) break;
+          ++qn[x];
+          to_fp16_scaled(sQ[x], p.rows * 128, sq, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.q16[x]);
+        }
+        if (!ok) break;
+        if (resident) {
+          if (it.unit != prev_unit) {
+            ++unit_loads;
+            prev_unit = it.unit;
+            for (int st = 0; st < p.nkb && ok; ++st) ok = conv_k(st, (unit_loads - 1) & 1u);
+          }
+        } else {
+          for (int bi = 0; bi < nb && ok; ++bi) {
+            const uint32_t c = sbase + static_cast<uint32_t>(bi);
+            ok = conv_k(static_cast<int>(c % kDqStages), (c / kDqStages) & 1u);
+          }
+        }
+        sbase += nb;
+      }
+    } else if (kDelta && warp == 11) {
       // ---------------------------------------------------------- operand range scan
       // Walks the producer's fills in its order; every fill is scanned and then released
       // (one more arrival on q_empty / kv_empty), so no buffer is refilled unscanned.
@@ -314,7 +414,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       {  // whole warp in lockstep; one elected lane issues
         const int x = warp - kQsMmaWarp;
         const uint32_t tS = tmem + 256u * x, tP = tS + 96u, tQ = tS + 192u;
-        const uint32_t idesc_dq = idesc_bf16(128, 64, 0, 1);
+        const uint32_t idesc_dq = idesc_fp16(128, 64, 0, 1);
+        // the dQ pass reads Q and K after their fp16 rewrite, the Delta pass as loaded
+        uint64_t* const qb = kDelta ? sm.q_full : sm.q16;
+        uint64_t* const kb16 = kDelta ? sm.k_full : sm.k16;
         uint32_t js = 0, jd = 0, qn = 0, unit_loads = 0, sbase = 0;
         long long prev_unit = -1;
         bool ok = true;
@@ -327,7 +430,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             ++unit_loads;
             prev_unit = it.unit;
             for (int s = 0; s < p.nkb && ok; ++s)
-              ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[s], (unit_loads - 1) & 1u, ctl, status, 11));
+              ok = __all_sync(0xffffffffu, wait_bar(&kb16[s], (unit_loads - 1) & 1u, ctl, status, 11));
             for (int s = 0; s < p.nkb && ok; ++s)
               ok = __all_sync(0xffffffffu, wait_bar(&sm.v_full[s], (unit_loads - 1) & 1u, ctl, status, 11));
           }
@@ -348,28 +451,29 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (!resident)
               for (int bi = 0; bi < nb && ok; ++bi) {
                 const KvSlot ks = slot(bi);
-                ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 12)) &&
+                ok = __all_sync(0xffffffffu, wait_bar(&kb16[ks.stage], ks.parity, ctl, status, 12)) &&
                      __all_sync(0xffffffffu, wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 12));
                 if (ok) mma_commit_w(&sm.kv_empty[ks.stage]);
               }
             sbase += nb;
             continue;
           }
-          if (!__all_sync(0xffffffffu, wait_bar(&sm.q_full[x], qn & 1u, ctl, status, 14))) break;
+          if (!__all_sync(0xffffffffu, wait_bar(&qb[x], qn & 1u, ctl, status, 14))) break;
           ++qn;
           auto issue_s = [&](int bi) -> bool {
             const KvSlot ks = slot(bi);
-            if (!__all_sync(0xffffffffu, wait_bar(&sm.k_full[ks.stage], ks.parity, ctl, status, 15))) return false;
+            if (!__all_sync(0xffffffffu, wait_bar(&kb16[ks.stage], ks.parity, ctl, status, 15))) return false;
             if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 15))) return false;
             tc_fence_after();
             const int n = round16(block_ncols(it, it.kb_lo + bi, kBN));
             const uint32_t idesc = idesc_bf16(128, n, 0, 0);
+            const uint32_t idesc_s = kDelta ? idesc : idesc_fp16(128, n, 0, 0);
             const uint64_t aq = sdesc_sw128(smem_u32(sQ[x]), 16, 1024);
             const uint64_t ado = sdesc_sw128(smem_u32(sdO[x]), 16, 1024);
             const uint64_t bk = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 16, 1024);
             const uint64_t bv = sdesc_sw128(smem_u32(sV + ks.stage * kKVTile), 16, 1024);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss_w(tS, aq + 2 * k, bk + 2 * k, idesc, k > 0);
+            for (int k = 0; k < 4; ++k) mma_ss_w(tS, aq + 2 * k, bk + 2 * k, idesc_s, k > 0);
 #pragma unroll
             for (int k = 0; k < 4; ++k) mma_ss_w(tP, ado + 2 * k, bv + 2 * k, idesc, k > 0);
             mma_commit_w(&sm.s_full[x]);
@@ -386,10 +490,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (!kDelta) {
               const int ksteps = round16(block_ncols(it, it.kb_lo + bi, kBN)) >> 4;
               const uint64_t bk = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 1024, 1024);
-              for (int k = 0; k < ksteps; ++k) {
+              for (int k = 0; k < ksteps; ++k)
                 mma_ts_w(tQ, tS + 8 * k, bk + (2048 >> 4) * k, idesc_dq, (bi > 0 || k > 0));
-                mma_ts_w(tQ, tP + 8 * k, bk + (2048 >> 4) * k, idesc_dq, 1);
-              }
             }
             if (!resident) mma_commit_w(&sm.kv_empty[ks.stage]);
             if (bi == nb - 1) {
@@ -425,16 +527,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int pos = mytok0 + tok;
       const bool row_ok = (r < p.rows) && (pos < p.L);
       long long row = 0;
-      float lse2 = INFINITY, dlt = 0.f;
+      float lse2 = INFINITY, ndl = 0.f;
       float dacc[4] = {0.f, 0.f, 0.f, 0.f};
       if (row_ok) {
         const long long t_idx = p.is_time ? pos : it.fixed;
         const long long s_idx = p.is_time ? it.fixed : pos;
         row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + g;
         lse2 = dp.lse[row] * lg2e;
-        if (!kDelta) dlt = dp.delta[row];
+        if (!kDelta) ndl = -dp.delta[row] * ldexpf(1.f, eds);
       }
-      const float2 sl2 = make_float2(p.sl, p.sl);
+      // the dQ pass's S carries 2^(eq + ek); its dS is written times 2^eds
+      const float slx = kDelta ? p.sl : p.sl * ldexpf(1.f, -(eq + ek));
+      const float c1 = ldexpf(1.f, eds);
+      const float2 sl2 = make_float2(slx, slx), c12 = make_float2(c1, c1), nd2 = make_float2(ndl, ndl);
       const float2 nl2 = make_float2(-lse2, -lse2);
       for (int bi = 0; bi < nb; ++bi) {
         const int kbase = (it.kb_lo + bi) * kBN;
@@ -473,18 +578,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             }
             continue;
           }
-          uint32_t pk[16], lk[16];
+          uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float2 xx = __ffma2_rn(make_float2(sv[2 * j], sv[2 * j + 1]), sl2, nl2);
+            const float2 t = __ffma2_rn(make_float2(pv[2 * j], pv[2 * j + 1]), c12, nd2);
+            const float2 d = __fmul2_rn(make_float2(ex2(xx.x), ex2(xx.y)), t);
             // masked (and stale, beyond the block's N) columns give exactly zero: select,
             // never multiply, since stale TMEM may hold NaN
-            const float d0 = ((keep >> (2 * j)) & 1u) ? ex2(xx.x) * (pv[2 * j] - dlt) : 0.f;
-            const float d1 = ((keep >> (2 * j + 1)) & 1u) ? ex2(xx.y) * (pv[2 * j + 1] - dlt) : 0.f;
-            pk[j] = split_bf16x2(d0, d1, &lk[j]);
+            pk[j] = pack_f16x2(((keep >> (2 * j)) & 1u) ? d.x : 0.f, ((keep >> (2 * j + 1)) & 1u) ? d.y : 0.f);
           }
-          tmem_st16(tS + 16 * c, pk);   // dS high parts over the scores already read
-          tmem_st16(tP + 16 * c, lk);   // dS residuals over dP already read
+          tmem_st16(tS + 16 * c, pk);   // dS (fp16 pairs, times 2^eds) over the scores already read
         }
         if (!kDelta) tmem_wait_st();
         tc_fence_before();
@@ -507,12 +611,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tmem_ld32(tQ + 32, o + 32);
       tmem_wait_ld_dep32(o);
       tmem_wait_ld_dep32(o + 32);
+      const float fq = dp.scale * ldexpf(1.f, -(eds + ek));  // undo the fp16 scales
       if (row_ok && dp.dq_f32) {
         float4* dst = reinterpret_cast<float4*>(dp.dq_f32 + row * 64);
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          dst[c] = make_float4(o[4 * c] * dp.scale, o[4 * c + 1] * dp.scale, o[4 * c + 2] * dp.scale,
-                               o[4 * c + 3] * dp.scale);
+          dst[c] = make_float4(o[4 * c] * fq, o[4 * c + 1] * fq, o[4 * c + 2] * fq, o[4 * c + 3] * fq);
       }
       {
         uint8_t* stg = sOst + (warp & 7) * 4096;
@@ -520,10 +624,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint4 wv;
-          wv.x = pack_bf16x2(o[8 * c + 0] * dp.scale, o[8 * c + 1] * dp.scale);
-          wv.y = pack_bf16x2(o[8 * c + 2] * dp.scale, o[8 * c + 3] * dp.scale);
-          wv.z = pack_bf16x2(o[8 * c + 4] * dp.scale, o[8 * c + 5] * dp.scale);
-          wv.w = pack_bf16x2(o[8 * c + 6] * dp.scale, o[8 * c + 7] * dp.scale);
+          wv.x = pack_bf16x2(o[8 * c + 0] * fq, o[8 * c + 1] * fq);
+          wv.y = pack_bf16x2(o[8 * c + 2] * fq, o[8 * c + 3] * fq);
+          wv.z = pack_bf16x2(o[8 * c + 4] * fq, o[8 * c + 5] * fq);
+          wv.w = pack_bf16x2(o[8 * c + 6] * fq, o[8 * c + 7] * fq);
           *reinterpret_cast<uint4*>(stg + wr * 128 + ((c ^ (wr & 7)) << 4)) = wv;
         }
         __syncwarp();
@@ -699,23 +803,6 @@ __device__ __forceinline__ void dkdv_chunk(const float* sv, const float* dv, con
   }
 }
 
-// Rewrite `bytes` of packed bf16 pairs as fp16 pairs times 2^e, in place (one warp).
-__device__ __forceinline__ void to_fp16_scaled(uint8_t* buf, int bytes, float s, int lane) {
-  uint4* p = reinterpret_cast<uint4*>(buf);
-  const float2 s2 = make_float2(s, s);
-#pragma unroll 4
-  for (int x = lane; x < (bytes >> 4); x += 32) {
-    uint4 d = p[x];
-    uint32_t w[4] = {d.x, d.y, d.z, d.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const float2 f = __fmul2_rn(make_float2(__uint_as_float(w[h] << 16),
-                                              __uint_as_float(w[h] & 0xFFFF0000u)), s2);
-      w[h] = pack_f16x2(f.x, f.y);
-    }
-    p[x] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
 
 __global__ void __launch_bounds__(kKvThreads, 1)
     od_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
