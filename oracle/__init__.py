@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for masked space attention and windowed causal time attention.
+"""fp64 CPU oracle for masked space attention and windowed causal time attention
+(training forward/backward and the rollout decode step).
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's CPU
 baseline may import this package; the CUDA library never calls it, and it shares
@@ -6,7 +7,8 @@ no code with the CUDA path.  The arithmetic lives in od_oracle.c (plain loops,
 double precision); this module compiles it with gcc and marshals numpy arrays.
 
 Every function takes float64 arrays in the library's layouts
-(Q/O/dO/dQ [B,T,S,Hq,D], K/V/dK/dV [B,T,S,Hkv,D], LSE [B,T,S,Hq]) and returns
+(Q/O/dO/dQ [B,T,S,Hq,D], K/V/dK/dV [B,T,S,Hkv,D], LSE [B,T,S,Hq]; the decode step
+takes one frame [B,S,H,D] and a ring-buffer cache [B,W,S,Hkv,D]) and returns
 float64 results.  Use `from_bf16` to widen the bf16 inputs exactly.
 """
 from __future__ import annotations
@@ -50,6 +52,9 @@ def _load():
                 f = getattr(lib, name)
                 f.argtypes = args
                 f.restype = ctypes.c_int
+            lib.oracle_time_decode.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i,
+                                               ctypes.c_longlong, ctypes.c_double]
+            lib.oracle_time_decode.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = [i]
             lib.oracle_num_threads.restype = i
             _lib = lib
@@ -134,3 +139,31 @@ def space_bwd(q, k, v, dout, agent=-1, scale=None, nthreads=0):
 def time_bwd(q, k, v, dout, window, scale=None, nthreads=0):
     """Time attention backward. Returns (O, LSE, dQ, dK, dV)."""
     return _bwd("oracle_time_bwd", q, k, v, dout, window, scale, nthreads)
+
+
+def time_decode(q, k_new, v_new, k_cache, v_cache, t, scale=None):
+    """Decode step of time attention with a ring-buffer KV cache of W = k_cache.shape[1]
+    frames: stores the new frame (absolute index t) in slot t mod W, then attends over frames
+    max(0, t-W+1) .. t.  q [B,S,Hq,D]; k_new, v_new [B,S,Hkv,D]; caches [B,W,S,Hkv,D].
+    Returns (O [B,S,Hq,D], LSE [B,S,Hq], K cache after, V cache after); the inputs are not
+    modified."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k_new = np.ascontiguousarray(k_new, dtype=np.float64)
+    v_new = np.ascontiguousarray(v_new, dtype=np.float64)
+    kc = np.array(k_cache, dtype=np.float64, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.float64, copy=True, order="C")
+    B, S, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    W = kc.shape[1]
+    if k_new.shape != (B, S, Hkv, D) or v_new.shape != k_new.shape or kc.shape != (B, W, S, Hkv, D) \
+            or vc.shape != kc.shape:
+        raise ValueError("expected q [B,S,Hq,D], k_new/v_new [B,S,Hkv,D], caches [B,W,S,Hkv,D]")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, S, Hq), dtype=np.float64)
+    rc = _load().oracle_time_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc), _ptr(o),
+                                    _ptr(lse), B, S, Hq, Hkv, D, W, int(t), float(scale))
+    if rc:
+        raise ValueError("oracle rejected the arguments")
+    return o, lse, kc, vc

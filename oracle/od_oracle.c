@@ -38,6 +38,11 @@
  *     dQ = scale sum_j dS_j k_j,  dK_j += scale dS_j q,  dV_j += p_j dO,
  *   where dK and dV sum over every query row and every query head of the group.
  *
+ *   Decode step (oracle_time_decode, at the end of this file): one new frame of a
+ *   rollout attends, per token position, to the last W frames held in a ring-buffer
+ *   KV cache -- the time-attention rows above for the single step t, with the new
+ *   frame stored into its cache slot first.
+ *
  * Layouts (row-major, contiguous): Q, O, dQ, dO [B,T,S,Hq,D];
  * K, V, dK, dV [B,T,S,Hkv,D]; LSE [B,T,S,Hq] (natural log).
  *
@@ -262,4 +267,67 @@ int oracle_time_bwd(const double *q, const double *k, const double *v, const dou
 int oracle_num_threads(int requested) {
     if (requested > 0) return requested;
     return (int)sysconf(_SC_NPROCESSORS_ONLN);
+}
+
+/*
+ * Decode step of time attention with a ring-buffer KV cache.  Rollout generates frames one
+ * at a time (7minutos.es page, section "Lo que realmente se envió": the local rollout
+ * harness; the time window of W frames as above).  The new frame has absolute index t; the
+ * cache holds the last W frames, frame f in slot f mod W.  The step first stores the new
+ * frame's K and V in slot t mod W; then every query head h of every token position s of the
+ * new frame attends, at the same (b, s) and KV head floor(h / G), to the frames
+ *     f = max(0, t - W + 1) .. t
+ * with logits l_f = scale <q, k_f>:  LSE = ln sum_f exp(l_f),  O = sum_f exp(l_f - LSE) v_f.
+ * Layouts: q, o [B,S,Hq,D]; k_new, v_new [B,S,Hkv,D]; k_cache, v_cache [B,W,S,Hkv,D] (updated
+ * in place); lse [B,S,Hq].  Single-threaded: decode shapes are small.
+ */
+int oracle_time_decode(const double *q, const double *k_new, const double *v_new,
+                       double *k_cache, double *v_cache, double *o, double *lse,
+                       int B, int S, int Hq, int Hkv, int D, int W, long long t, double scale) {
+    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || t < 0 || Hq % Hkv) return 1;
+    const int G = Hq / Hkv;
+    const long slot_t = (long)(t % W);
+    /* 1. the new frame's K/V into its slot */
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < S; ++s)
+            for (int h = 0; h < Hkv; ++h) {
+                const long src = (((long)b * S + s) * Hkv + h) * D;
+                const long dst = ((((long)b * W + slot_t) * S + s) * Hkv + h) * D;
+                for (int d = 0; d < D; ++d) {
+                    k_cache[dst + d] = k_new[src + d];
+                    v_cache[dst + d] = v_new[src + d];
+                }
+            }
+    /* 2. attention of the new frame's queries over the frames in the window */
+    const long long f0 = t - W + 1 > 0 ? t - W + 1 : 0;
+    const int nk = (int)(t - f0 + 1);
+    double *logit = (double *)malloc(sizeof(double) * (size_t)nk);
+    if (!logit) return 2;
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < S; ++s)
+            for (int h = 0; h < Hq; ++h) {
+                const int kvh = h / G;
+                const double *qr = q + (((long)b * S + s) * Hq + h) * D;
+                double m = -INFINITY;
+                for (int j = 0; j < nk; ++j) {
+                    const long slot = (long)((f0 + j) % W);
+                    const double *kr = k_cache + ((((long)b * W + slot) * S + s) * Hkv + kvh) * D;
+                    logit[j] = scale * dot(qr, kr, D);
+                    if (logit[j] > m) m = logit[j];
+                }
+                double sum = 0.0;
+                for (int j = 0; j < nk; ++j) sum += exp(logit[j] - m);
+                const double l = m + log(sum);
+                lse[((long)b * S + s) * Hq + h] = l;
+                double *orow = o + (((long)b * S + s) * Hq + h) * D;
+                for (int d = 0; d < D; ++d) orow[d] = 0.0;
+                for (int j = 0; j < nk; ++j) {
+                    const long slot = (long)((f0 + j) % W);
+                    const double *vr = v_cache + ((((long)b * W + slot) * S + s) * Hkv + kvh) * D;
+                    const double pj = exp(logit[j] - l);
+                    for (int d = 0; d < D; ++d) orow[d] += pj * vr[d];
+                }
+            }
+    free(logit);
+    return 0;
 }

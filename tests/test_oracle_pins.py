@@ -343,6 +343,93 @@ def test_backward_causal_and_agent_zero_gradients(oracle_mod):
 
 
 # ----------------------------------------------------------------------------
+# decode step over a ring-buffer KV cache
+# ----------------------------------------------------------------------------
+def _rollout(oracle_mod, q, k, v, W, scale, fill=0.0):
+    """Feeds frames 0..T-1 one at a time through the decode step, starting from a
+    cache filled with `fill`; returns the per-frame outputs and the final caches."""
+    B, T, S, Hq, D = q.shape
+    Hkv = k.shape[3]
+    kc = np.full((B, W, S, Hkv, D), fill)
+    vc = np.full((B, W, S, Hkv, D), fill)
+    os_, ls_ = [], []
+    for t in range(T):
+        o, lse, kc, vc = oracle_mod.time_decode(q[:, t], k[:, t], v[:, t], kc, vc, t, scale)
+        os_.append(o)
+        ls_.append(lse)
+    return np.stack(os_, 1), np.stack(ls_, 1), kc, vc
+
+
+@pytest.mark.parametrize("B,T,S,Hq,Hkv,W", [(1, 9, 3, 4, 2, 4), (2, 6, 5, 6, 3, 6),
+                                             (1, 7, 2, 3, 1, 1), (2, 5, 3, 2, 2, 9)])
+def test_decode_rollout_matches_sdpa_over_the_window(oracle_mod, B, T, S, Hq, Hkv, W):
+    """A rollout of T decode steps reproduces, frame by frame, torch's float64 SDPA over
+    the frames max(0, t-W+1)..t (ring wrap-around included when T > W); the cache's
+    unwritten slots hold values (1e300) that would poison any read of them."""
+    D, sc = 8, 0.3
+    G = Hq // Hkv
+    q, k, v = rnd((B, T, S, Hq, D), 60), rnd((B, T, S, Hkv, D), 61), rnd((B, T, S, Hkv, D), 62)
+    o, lse, kc, vc = _rollout(oracle_mod, q, k, v, W, sc, fill=1e300)
+    for t in range(T):
+        lo = max(0, t - W + 1)
+        qt = torch.from_numpy(q[:, t]).permute(0, 1, 2, 3).reshape(B * S, Hq, 1, D)
+        kt = torch.from_numpy(np.repeat(k[:, lo:t + 1], G, axis=3)).permute(0, 2, 3, 1, 4)
+        vt = torch.from_numpy(np.repeat(v[:, lo:t + 1], G, axis=3)).permute(0, 2, 3, 1, 4)
+        kt = kt.reshape(B * S, Hq, t + 1 - lo, D)
+        vt = vt.reshape(B * S, Hq, t + 1 - lo, D)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=sc)
+        np.testing.assert_allclose(o[:, t], ref.reshape(B, S, Hq, D).numpy(), rtol=0, atol=1e-12)
+        logits = torch.einsum("nhd,nhkd->nhk", qt[:, :, 0], kt) * sc
+        np.testing.assert_allclose(lse[:, t], torch.logsumexp(logits, -1).reshape(B, S, Hq).numpy(),
+                                   rtol=0, atol=1e-12)
+    # the final cache holds frame f in slot f mod W for the last min(T, W) frames
+    for f in range(max(0, T - W), T):
+        np.testing.assert_array_equal(kc[:, f % W], k[:, f])
+        np.testing.assert_array_equal(vc[:, f % W], v[:, f])
+
+
+def test_decode_rollout_equals_the_windowed_time_forward(oracle_mod):
+    """The decode step and the full-sequence time forward are two routes to the same rows."""
+    B, T, S, Hq, Hkv, D, W = 1, 11, 4, 6, 2, 8, 4
+    q, k, v = rnd((B, T, S, Hq, D), 63), rnd((B, T, S, Hkv, D), 64), rnd((B, T, S, Hkv, D), 65)
+    o, lse, _, _ = _rollout(oracle_mod, q, k, v, W, 0.125)
+    O, L = oracle_mod.time_fwd(q, k, v, W, 0.125)
+    np.testing.assert_allclose(o, O, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, L, rtol=0, atol=1e-13)
+
+
+def test_decode_first_frame_and_zero_query_closed_forms(oracle_mod):
+    """t = 0 reads only the new frame: O = v_new, LSE = scale <q, k_new>.  q = 0 gives
+    LSE = ln min(t+1, W) and O = the mean of V over the window's frames."""
+    B, S, Hq, Hkv, D, W = 2, 3, 4, 2, 8, 5
+    G = Hq // Hkv
+    q, kn, vn = rnd((B, S, Hq, D), 66), rnd((B, S, Hkv, D), 67), rnd((B, S, Hkv, D), 68)
+    kc, vc = rnd((B, W, S, Hkv, D), 69), rnd((B, W, S, Hkv, D), 70)
+    o, lse, _, _ = oracle_mod.time_decode(q, kn, vn, kc, vc, 0, 0.25)
+    np.testing.assert_array_equal(o, np.repeat(vn, G, axis=2))
+    np.testing.assert_allclose(lse, 0.25 * (q * np.repeat(kn, G, axis=2)).sum(-1), rtol=0, atol=1e-15)
+    for t in (2, 4, 5, 13):
+        o, lse, kc2, vc2 = oracle_mod.time_decode(np.zeros_like(q), kn, vn, kc, vc, t, 0.25)
+        n = min(t + 1, W)
+        np.testing.assert_allclose(lse, np.log(n), rtol=0, atol=1e-15)
+        frames = [(f % W) for f in range(max(0, t - W + 1), t + 1)]
+        mean_v = vc2[:, frames].mean(axis=1)
+        np.testing.assert_allclose(o, np.repeat(mean_v, G, axis=2), rtol=0, atol=1e-14)
+
+
+def test_decode_writes_only_the_new_frames_slot(oracle_mod):
+    B, S, Hq, Hkv, D, W, t = 2, 3, 4, 2, 8, 6, 15
+    q, kn, vn = rnd((B, S, Hq, D), 71), rnd((B, S, Hkv, D), 72), rnd((B, S, Hkv, D), 73)
+    kc, vc = rnd((B, W, S, Hkv, D), 74), rnd((B, W, S, Hkv, D), 75)
+    _, _, kc2, vc2 = oracle_mod.time_decode(q, kn, vn, kc, vc, t)
+    others = [i for i in range(W) if i != t % W]
+    np.testing.assert_array_equal(kc2[:, others], kc[:, others])
+    np.testing.assert_array_equal(vc2[:, others], vc[:, others])
+    np.testing.assert_array_equal(kc2[:, t % W], kn)
+    np.testing.assert_array_equal(vc2[:, t % W], vn)
+
+
+# ----------------------------------------------------------------------------
 # workload shapes and the input generator
 # ----------------------------------------------------------------------------
 def test_workload_shapes_follow_the_pages():
