@@ -12,7 +12,7 @@ the op raises instead of falling back to any other implementation.
 from __future__ import annotations
 
 _API = (
-    "space_attn_fwd", "space_attn_bwd", "time_attn_fwd", "time_attn_bwd",
+    "space_attn_fwd", "space_attn_bwd", "time_attn_fwd", "time_attn_bwd", "time_attn_decode",
     "bwd_workspace_bytes", "get_device_status", "get_device_status_detail", "library", "library_path",
     "ODError", "EXPORTED_SYMBOLS",
 )

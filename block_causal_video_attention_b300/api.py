@@ -65,6 +65,8 @@ def library():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = I
+            lib.od_time_attn_decode.argtypes = [P] * 7 + [I] * 6 + [ctypes.c_longlong, F, P]
+            lib.od_time_attn_decode.restype = I
             lib.od_space_attn_bwd_static_ws.argtypes = [P] * 12 + [I] * 7 + [F, P]
             lib.od_space_attn_bwd_static_ws.restype = I
             lib.od_attn_bwd_workspace_bytes.argtypes = [I] * 7
@@ -184,6 +186,42 @@ def time_attn_bwd(q, k, v, o, lse, dout, window, scale=None, fp32_grads=False,
     """Time attention backward -> (dQ, dK, dV) bf16 [, (dQ, dK, dV) fp32]."""
     return _bwd("od_time_attn_bwd", 1, q, k, v, o, lse, dout, window, scale, fp32_grads,
                 workspace, out, stream)
+
+
+def time_attn_decode(q, k_new, v_new, k_cache, v_cache, t, scale=None, out=None, lse=None,
+                     stream=None):
+    """One rollout step of time attention over a ring-buffer KV cache -> (O bf16, LSE fp32).
+
+    q [B,S,Hq,D]; k_new, v_new [B,S,Hkv,D]; k_cache, v_cache [B,W,S,Hkv,D] (bf16, updated in
+    place: the new frame goes to slot t mod W); t is the new frame's absolute index.  O is
+    [B,S,Hq,D] bf16, LSE [B,S,Hq] fp32 -- the rows of time_attn_fwd at step t."""
+    ts = (("q", q, 4), ("k_new", k_new, 4), ("v_new", v_new, 4), ("k_cache", k_cache, 5),
+          ("v_cache", v_cache, 5))
+    for name, x, nd in ts:
+        if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.bfloat16:
+            raise TypeError("%s must be a bf16 CUDA tensor" % name)
+        if not x.is_contiguous() or x.dim() != nd:
+            raise ValueError("%s must be a contiguous %d-D tensor" % (name, nd))
+    B, S, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    W = k_cache.shape[1]
+    if k_new.shape != (B, S, Hkv, D) or v_new.shape != k_new.shape or \
+            k_cache.shape != (B, W, S, Hkv, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("expected q [B,S,Hq,D], k_new/v_new [B,S,Hkv,D], caches [B,W,S,Hkv,D]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, S, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if l.shape != (B, S, Hq) or l.dtype != torch.float32 or not l.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,S,Hq]")
+    st = library().od_time_attn_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                       _ptr(v_cache), _ptr(o), _ptr(l), B, S, Hq, Hkv, D, W,
+                                       int(t), float(scale), _stream(stream))
+    if st:
+        raise ODError(st, "od_time_attn_decode")
+    return o, l
 
 
 def get_device_status(stream=None) -> int:

@@ -15,6 +15,7 @@
 #include "od_attn.h"
 #include "od_fwd.cuh"
 #include "od_bwd.cuh"
+#include "od_decode.cuh"
 
 // Device status words: [0] has bit OD_DEV_TIMEOUT set by any kernel whose bounded wait
 // expired; [1] holds the first such wait's site word (site << 24 | parity << 23 | block).
@@ -54,6 +55,9 @@ od_status device_state(DeviceState** out) {
         fa.numRegs != od::kFwdLaunchRegs)
       return OD_ERR_CUDA;
     if (od::bwd_setup() != cudaSuccess) return OD_ERR_CUDA;
+    if (cudaFuncSetAttribute(od::od_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(od::kDecSmemBytes)) != cudaSuccess)
+      return OD_ERR_CUDA;
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -287,6 +291,67 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   return OD_OK;
 }
 
+// One rollout step of time attention over the ring-buffer KV cache [B,W,S,Hkv,64].
+od_status launch_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, void* o, float* lse, int B, int S, int Hq, int Hkv, int D,
+                        int window, long long t, float scale, void* stream) {
+  const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o, lse};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return OD_ERR_INVALID_ARG;
+  if (t < 0 || window < 1) return OD_ERR_INVALID_ARG;
+  od_status st = check_shape(B, 1, S, Hq, Hkv, D, scale);
+  if (st != OD_OK) return st;
+  if (Hq / Hkv > 16) return OD_ERR_UNSUPPORTED;
+  // cache coordinates (frames x positions x heads) and the unit count stay 32-bit
+  if (1LL * B * window * S * Hkv * D * 2 >= (1LL << 40) || window > (1 << 24) ||
+      1LL * B * S * Hkv >= (1LL << 31))
+    return OD_ERR_UNSUPPORTED;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != OD_OK) return st;
+
+  od::DecParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.B = B; p.S = S; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.W = window;
+  p.n_valid = static_cast<int>(t + 1 < window ? t + 1 : window);
+  p.slot = static_cast<int>(t % window);
+  p.nb = (p.n_valid + od::kDecBN - 1) / od::kDecBN;
+  p.units = B * S * Hkv;
+  p.sl = scale * 1.4426950408889634f;
+  p.status = dev->status;
+
+  // The window's frames are the slots 0 .. n_valid - 1; the map's frame extent is n_valid, so
+  // the rows of a last partial block come back zero-filled instead of reading unused slots.
+  CUtensorMap tk, tv;
+  const cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)S,
+                              (cuuint64_t)p.n_valid, (cuuint64_t)B};
+  cuuint64_t strides[4];
+  strides[0] = (cuuint64_t)D * 2;
+  strides[1] = strides[0] * Hkv;
+  strides[2] = strides[1] * S;
+  strides[3] = strides[2] * window;
+  const cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)od::kDecBN, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  for (int which = 0; which < 2; ++which) {
+    CUresult r = g_encode(which ? &tv : &tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                          which ? v_cache : k_cache, dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return OD_ERR_CUDA;
+  }
+  const long long warps_needed = p.units;
+  long long grid = (warps_needed + od::kDecWarps - 1) / od::kDecWarps;
+  if (grid > dev->num_sms) grid = dev->num_sms;
+  od::od_decode_kernel<<<(unsigned)grid, od::kDecThreads, od::kDecSmemBytes,
+                         static_cast<cudaStream_t>(stream)>>>(tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? OD_OK : OD_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------------------------------
 // Fixed scratch for od_space_attn_bwd_static_ws: callers that cannot allocate device memory
 // (an allocator-free runtime, code running where cudaMalloc is forbidden or would
@@ -365,6 +430,13 @@ od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const vo
                            size_t workspace_bytes, void* stream) {
   return launch_bwd(1, q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
                     Hkv, D, -1, window, scale, workspace, workspace_bytes, stream);
+}
+
+od_status od_time_attn_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                              void* v_cache, void* o, float* lse, int B, int S, int Hq, int Hkv,
+                              int D, int window, long long t, float scale, void* stream) {
+  return launch_decode(q, k_new, v_new, k_cache, v_cache, o, lse, B, S, Hq, Hkv, D, window, t,
+                       scale, stream);
 }
 
 od_status od_get_device_status_detail(void* stream, unsigned int* site_word) {

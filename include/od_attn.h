@@ -94,6 +94,26 @@ od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const vo
                            int Hq, int Hkv, int D, int window, float scale, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* One rollout (decode) step of time attention over a ring-buffer KV cache.  A rollout
+ * generates one frame at a time (the local rollout harness and the frame-by-frame demo,
+ * 7minutos.es page, section "Lo que realmente se envió"); the time layer then needs, for
+ * the new frame t only, the rows of od_time_attn_fwd at step t.  The cache holds the last
+ * `window` (= W) frames of K and V, frame f in slot f mod W:
+ *   q, o           : [B, S, Hq, D]     bf16, the new frame's queries / outputs
+ *   k_new, v_new   : [B, S, Hkv, D]    bf16, the new frame's keys and values
+ *   k_cache, v_cache: [B, W, S, Hkv, D] bf16, read and updated in place
+ *   lse            : [B, S, Hq]        fp32, natural log
+ * The call stores k_new / v_new in slot t mod W, then for every (b, s, h) attends from
+ * q[b,s,h] to the frames max(0, t - W + 1) .. t of position s (KV head floor(h / G)), i.e.
+ * the slots 0 .. min(t+1, W) - 1.  The slots a caller has not written yet (t < W - 1) are
+ * never read.  t is the frame's absolute index (t >= 0); the caller feeds t = 0, 1, 2, ...
+ * in order, or fills the slots of frames t-W+1 .. t-1 itself beforehand.
+ * Errors as for od_time_attn_fwd (t < 0 or window < 1 is OD_ERR_INVALID_ARG), and
+ * OD_ERR_UNSUPPORTED for G = Hq / Hkv > 16. */
+od_status od_time_attn_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                              void* v_cache, void* o, float* lse, int B, int S, int Hq, int Hkv,
+                              int D, int window, long long t, float scale, void* stream);
+
 /* Size of the fixed device scratch used by od_space_attn_bwd_static_ws. */
 #define OD_STATIC_WORKSPACE_BYTES (16u << 20)
 

@@ -20,7 +20,7 @@ def test_every_declared_symbol_is_exported(lib):
     declared = set(re.findall(r"\b(od_\w+)\s*\(", src))
     assert {"od_space_attn_fwd", "od_time_attn_fwd", "od_space_attn_bwd", "od_time_attn_bwd",
             "od_attn_bwd_workspace_bytes", "od_get_device_status", "od_get_device_status_detail",
-            "od_status_string", "od_space_attn_bwd_static_ws",
+            "od_status_string", "od_space_attn_bwd_static_ws", "od_time_attn_decode",
             "od_version"} <= declared
     for name in declared:
         assert hasattr(lib, name), name
@@ -85,6 +85,26 @@ def test_backward_rejects_invalid_arguments(lib, fn):
     assert ((4190208 * 4 + 255) // 256) * 256 + 16384 <= 16 << 20
     assert ((4190272 * 4 + 255) // 256) * 256 + 16384 > 16 << 20
     assert lib.od_attn_bwd_workspace_bytes(0, 1, 4, 8, 4, 3, 64) == 0
+
+
+def test_decode_rejects_invalid_arguments(lib):
+    f = lib.od_time_attn_decode
+    base = dict(B=2, S=5, Hq=4, Hkv=2, D=64, W=6, t=3, scale=0.125)
+
+    def call(ptrs=None, **kw):
+        a = dict(base, **kw)
+        p = ptrs or (GOOD,) * 7
+        return f(*p, a["B"], a["S"], a["Hq"], a["Hkv"], a["D"], a["W"], a["t"], a["scale"], P(0))
+    assert call(ptrs=(GOOD,) * 3 + (P(0),) + (GOOD,) * 3) == 1     # null cache
+    assert call(ptrs=(GOOD,) * 6 + (P(4100),)) == 1                 # misaligned LSE
+    assert call(t=-1) == 1
+    assert call(W=0) == 1
+    assert call(B=0) == 1
+    assert call(Hq=5) == 1                                          # Hq % Hkv
+    assert call(scale=float("inf")) == 1
+    assert call(D=32) == 2
+    assert call(Hq=34, Hkv=2) == 2                                  # G = 17 > 16
+    assert call(W=(1 << 24) + 1) == 2
 
 
 def test_binding_refuses_cpu_tensors():
