@@ -6,6 +6,7 @@ space attention forward, time attention forward, and (when enabled) both backwar
 Metric: algorithmic TFLOP/s (allowed query-key pairs only; a backward counts 2.5 forward).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --workload minecraft_decode     # the rollout decode step (GB/s)
 
 --impl reference times the fp64 CPU oracle (the only reference this project has) on a
 bounded sample of the same workload.  Under torchrun each rank runs an independent replica
@@ -14,6 +15,7 @@ bounded sample of the same workload.  Under torchrun each rank runs an independe
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -413,6 +415,173 @@ def run_ours(args, w, with_bwd):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- decode step
+DECODE_METRIC = "rollout decode step (time attention over a ring-buffer KV cache) GB/s and % of B300 HBM roofline"
+
+
+def decode_bytes(w):
+    """Algorithmic HBM bytes of one decode step with a full window: the window's K and V rows
+    once, the new frame's q / k_new / v_new, the two cache rows written, O and LSE."""
+    n_valid = min(w.T, w.window)
+    kv_row = w.D * 2
+    return (w.B * w.S * w.Hkv * (2 * n_valid * kv_row + 4 * kv_row)
+            + w.B * w.S * w.Hq * (2 * w.D * 2 + 4))
+
+
+def decode_flops(w):
+    return 4.0 * w.D * w.B * w.S * w.Hq * min(w.T, w.window)
+
+
+def decode_oracle_sample(w, rollouts, inputs=None):
+    """Time the oracle's decode step on `rollouts` whole rollouts (all S x Hkv units each);
+    returns (algorithmic bytes of that sample, seconds, threads, description)."""
+    import oracle
+    oracle.build()
+    q, kn, vn, kc, vc = inputs if inputs is not None else synth.make_decode_inputs(w)
+    X = oracle.from_bf16
+    sl = slice(0, rollouts)
+    args = [X(a[sl]) for a in (q, kn, vn, kc, vc)]
+    t0 = time.perf_counter()
+    oracle.time_decode(*args, w.T - 1, w.scale)
+    s = time.perf_counter() - t0
+    return decode_bytes(w) * rollouts / w.B, s, 1, (
+        "%d of %d rollouts of %s (all %d positions x %d KV heads each), one decode step" % (
+            rollouts, w.B, w.name, w.S, w.Hkv))
+
+
+def run_decode(args, w):
+    import torch
+    import torch.distributed as dist
+    from block_causal_video_attention_b300 import api
+
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inputs = synth.make_decode_inputs(w)
+        vals = [decode_oracle_sample(w, 1, inputs) for _ in range(args.steps)]
+        b = sum(v[0] for v in vals)
+        s = sum(v[1] for v in vals)
+        value = b / s / 1e9
+        line = {"impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * s / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name},
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": vals[0][2],
+                                 "kind": "oracle", "sample": vals[0][3] + " per step"},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    torch.cuda.set_device(local)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    inputs = synth.make_decode_inputs(w)
+    q, kn, vn, kc, vc = inputs
+    hq, hkn, hvn = (to(a).pin_memory() for a in (q, kn, vn))
+    dq, dkn, dvn = (t.to(dev) for t in (hq, hkn, hvn))
+    # the cache is device-resident state of the rollout (frames t-191 .. t-1 and a stale slot)
+    dkc, dvc = to(kc).to(dev), to(vc).to(dev)
+    stream = torch.cuda.current_stream()
+    o = torch.empty_like(dq)
+    lse = torch.empty(dq.shape[:3], dtype=torch.float32, device=dev)
+    t0 = w.T - 1  # steady state: every step reads a full window
+
+    def step(i, Q=dq, KN=dkn, VN=dvn):
+        api.time_attn_decode(Q, KN, VN, dkc, dvc, t0 + i, w.scale, o, lse, stream)
+
+    clk = Clocks(local).__enter__()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if api.get_device_status() != 0:
+        raise RuntimeError("device timeout during warm-up")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step(args.warmup + i)
+        evs[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end), dev)
+    if api.get_device_status() != 0:
+        raise RuntimeError("device timeout during the timed region")
+    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    nbytes = decode_bytes(w)
+    value = world * nbytes * args.steps / (ms * 1e-3) / 1e9
+
+    # end to end: the new frame's q, k_new, v_new from pinned host memory, O and LSE back
+    hin = [hq, hkn, hvn]
+    din = [torch.empty_like(dq), torch.empty_like(dkn), torch.empty_like(dvn)]
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step(i):
+        for h, d in zip(hin, din):
+            d.copy_(h, non_blocking=True)
+        step(i, din[0], din[1], din[2])
+        for d, h in zip((o, lse), hout):
+            h.copy_(d, non_blocking=True)
+    base = args.warmup + args.steps
+    for i in range(2):
+        e2e_step(base + i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(args.steps):
+        e2e_step(base + 2 + i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    clk.__exit__()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), dev)
+    e2e = world * nbytes * args.steps / (e2e_ms * 1e-3) / 1e9
+
+    hbm, _, _, src = load_peaks()
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    traffic = None
+    if csrc_digest() == MEASURED_TRAFFIC["csrc_sha256"]:
+        traffic = MEASURED_TRAFFIC.get(w.name, {}).get("decode")
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": traffic, "kernel": "od_decode_kernel",
+            "peak_source": "%s HBM copy" % src}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        b_, s_, nth, desc = decode_oracle_sample(w, w.B, inputs)
+        cpu = {"value": b_ / s_ / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
+               "sample": desc}
+    if rank == 0:
+        line = {"metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "rollouts": w.B, "S": w.S, "Hq": w.Hq,
+                           "Hkv": w.Hkv, "head_dim": w.D, "window": w.window,
+                           "frame_index": t0, "l2": "inputs larger than L2 (KV cache %.0f MB)" %
+                           (2 * w.B * w.window * w.S * w.Hkv * w.D * 2 / 1e6),
+                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "tflops": decode_flops(w) / (kern_ms * 1e-3) / 1e12,
+                "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h},
+                "gpu_launches": args.steps, "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,11 +592,19 @@ def main():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--ref-units", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (rollouts for the decode workload), e.g. "
+                         "for a smaller profiling case")
     ap.add_argument("--op", default=None, choices=["space_fwd", "time_fwd", "space_bwd", "time_bwd"],
                     help="time one operator only (for profiling); the line then covers that op")
     args = ap.parse_args()
     name = args.workload or ("minecraft_fwd" if args.fwd_only else "minecraft_fwd_bwd")
     w = synth.WORKLOADS[name]
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch, name="%s_b%d" % (w.name, args.batch))
+    if name.endswith("_decode"):
+        run_decode(args, w)
+        return
     with_bwd = w.backward and not args.fwd_only
     if args.impl == "reference":
         run_reference(args, w, with_bwd)

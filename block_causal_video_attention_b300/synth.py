@@ -25,7 +25,9 @@ the CoinRun stage, and the tokenizer geometry (368x640 frames, 16x16 patches,
 """
 from __future__ import annotations
 
+import os
 from dataclasses import dataclass, field
+
 import numpy as np
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -68,25 +70,38 @@ def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return _f32_to_bf16_bits(np.asarray(x, dtype=np.float64).astype(np.float32))
 
 
+def _normal_chunk(seed: int, start: int, m: int) -> np.ndarray:
+    m2 = m + (m & 1)
+    u = _uniform(seed, start, m2)
+    u1, u2 = u[0::2], u[1::2]
+    r = np.sqrt(-2.0 * np.log(u1))
+    z = np.empty(m2, dtype=np.float64)
+    z[0::2] = r * np.cos(2.0 * np.pi * u2)
+    z[1::2] = r * np.sin(2.0 * np.pi * u2)
+    return f64_to_bf16_bits(z[:m])
+
+
 def normal_bf16(seed: int, start: int, n: int) -> np.ndarray:
     """Values [start, start+n) of the seeded N(0,1) stream, as bf16 bits.
 
-    `start` must be even (Box-Muller works on pairs)."""
+    `start` must be even (Box-Muller works on pairs).  Chunks of the stream are independent
+    (the generator is counter-based), so large requests are filled by several threads; the
+    values do not depend on how the work is split."""
     if start % 2:
         raise ValueError("start must be even")
     out = np.empty(n, dtype=np.uint16)
-    pos = 0
-    while pos < n:
-        m = min(_CHUNK, n - pos)
-        m2 = m + (m & 1)
-        u = _uniform(seed, start + pos, m2)
-        u1, u2 = u[0::2], u[1::2]
-        r = np.sqrt(-2.0 * np.log(u1))
-        z = np.empty(m2, dtype=np.float64)
-        z[0::2] = r * np.cos(2.0 * np.pi * u2)
-        z[1::2] = r * np.sin(2.0 * np.pi * u2)
-        out[pos:pos + m] = f64_to_bf16_bits(z[:m])
-        pos += m
+    chunks = [(pos, min(_CHUNK, n - pos)) for pos in range(0, n, _CHUNK)]
+
+    def fill(c):
+        pos, m = c
+        out[pos:pos + m] = _normal_chunk(seed, start + pos, m)
+    if len(chunks) > 2:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, chunks))
+    else:
+        for c in chunks:
+            fill(c)
     return out
 
 
@@ -141,7 +156,24 @@ WORKLOADS = {
     # frame; d_model 1536 as 24 heads x 64; no agent; window = T = 32.
     "tokenizer_enc": Workload("tokenizer_enc", 2, 32, 1432, 24, 24, 64, 32, -1, 4, True,
                               "tokenizer encoder layer, forward + backward"),
+    # Rollout decode of the Minecraft dynamics layer: 16 concurrent rollouts, one new frame
+    # per step attending to a full 192-frame window (T = absolute index of the new frame + 1).
+    "minecraft_decode": Workload("minecraft_decode", 16, 501, 290, 30, 3, 64, 192, 289, 5, False,
+                                 "Minecraft 1.6B dynamics layer, rollout decode step"),
 }
+
+
+def make_decode_inputs(w: Workload):
+    """Seeded bf16 inputs of one decode step (uint16 numpy): q [B,S,Hq,D], k_new and v_new
+    [B,S,Hkv,D], and full K/V caches [B,W,S,Hkv,D]."""
+    shapes = [(w.B, w.S, w.Hq, w.D), (w.B, w.S, w.Hkv, w.D), (w.B, w.S, w.Hkv, w.D),
+              (w.B, w.window, w.S, w.Hkv, w.D), (w.B, w.window, w.S, w.Hkv, w.D)]
+    out, start = [], 0
+    for shp in shapes:
+        n = int(np.prod(shp))
+        out.append(normal_bf16(w.seed, start, n).reshape(shp))
+        start += n + (n & 1)
+    return tuple(out)
 
 
 def make_inputs(w: Workload, with_dout: bool | None = None):
