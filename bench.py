@@ -275,8 +275,14 @@ def run_ours(args, w, with_bwd):
             raise SystemExit("--op %s is not part of workload %s" % (args.op, w.name))
         ops = [args.op]
     run = set(ops)
+    packed = bool(args.packed)
+    if packed:
+        # one fused-projection tensor [B,T,S,Hq+2Hkv,D] instead of three
+        dqkv_in = torch.cat([dq, dk, dv], dim=3).contiguous()
     if with_bwd:
         g = [torch.empty_like(x) for x in (dq, dk, dv, dq, dk, dv)]
+        if packed:
+            g_packed = [torch.empty_like(dqkv_in), torch.empty_like(dqkv_in)]
         ws_s = torch.empty(max(api.bwd_workspace_bytes(0, w.B, w.T, w.S, w.Hq, w.Hkv), 16),
                            dtype=torch.uint8, device=dev)
         ws_t = torch.empty(max(api.bwd_workspace_bytes(1, w.B, w.T, w.S, w.Hq, w.Hkv), 16),
@@ -284,7 +290,10 @@ def run_ours(args, w, with_bwd):
 
     ev = {op: [] for op in ops}
 
-    def step(record, Q=dq, K=dk, V=dv, DO=dd):
+    def step(record, Q=dq, K=dk, V=dv, DO=dd, QKV=None):
+        if packed:
+            return step_packed(record, dqkv_in if QKV is None else QKV, DO)
+
         def timed(op, fn):
             if record:
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -304,6 +313,27 @@ def run_ours(args, w, with_bwd):
         if "time_bwd" in run:
             timed("time_bwd", lambda: api.time_attn_bwd(Q, K, V, o_t, l_t, DO, w.window, w.scale,
                                                         workspace=ws_t, out=g[3:], stream=stream))
+
+    def step_packed(record, QKV, DO):
+        def timed(op, fn):
+            if record:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ev[op].append((a, b))
+            else:
+                fn()
+        if "space_fwd" in run:
+            timed("space_fwd", lambda: api.space_attn_fwd_packed(QKV, w.Hq, w.agent, w.scale, o_s, l_s, stream))
+        if "time_fwd" in run:
+            timed("time_fwd", lambda: api.time_attn_fwd_packed(QKV, w.Hq, w.window, w.scale, o_t, l_t, stream))
+        if "space_bwd" in run:
+            timed("space_bwd", lambda: api.space_attn_bwd_packed(
+                QKV, w.Hq, o_s, l_s, DO, w.agent, w.scale, workspace=ws_s, out=g_packed[0], stream=stream))
+        if "time_bwd" in run:
+            timed("time_bwd", lambda: api.time_attn_bwd_packed(
+                QKV, w.Hq, o_t, l_t, DO, w.window, w.scale, workspace=ws_t, out=g_packed[1], stream=stream))
 
     if args.op and args.op.endswith("_bwd"):
         # the backward reads the forward's O and LSE: produce them once, outside the timing
@@ -338,17 +368,25 @@ def run_ours(args, w, with_bwd):
         per_op[op] = {"ms": t_ms, "tflops": f[op] / (t_ms * 1e-3) / 1e12}
 
     # end to end: pinned host inputs -> device, the step, results back to pinned host memory
-    outs = [o_s, l_s, o_t, l_t] + (g if with_bwd else [])
+    outs = [o_s, l_s, o_t, l_t] + ((g_packed if packed else g) if with_bwd else [])
     hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    hin = [hq, hk, hv] + ([hd] if with_bwd else [])
-    din = [torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv), torch.empty_like(dd)]
+    if packed:
+        hqkv = dqkv_in.cpu().pin_memory()
+        hin = [hqkv] + ([hd] if with_bwd else [])
+        din = [torch.empty_like(dqkv_in), torch.empty_like(dd)]
+    else:
+        hin = [hq, hk, hv] + ([hd] if with_bwd else [])
+        din = [torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv), torch.empty_like(dd)]
     h2d = sum(t.numel() * t.element_size() for t in hin)
     d2h = sum(t.numel() * t.element_size() for t in hout)
 
     def e2e_step():
         for h, d in zip(hin, din):
             d.copy_(h, non_blocking=True)
-        step(False, din[0], din[1], din[2], din[3])
+        if packed:
+            step(False, DO=din[1], QKV=din[0])
+        else:
+            step(False, din[0], din[1], din[2], din[3])
         for d, h in zip(outs, hout):
             h.copy_(d, non_blocking=True)
     for _ in range(2):
@@ -401,7 +439,8 @@ def run_ours(args, w, with_bwd):
                 "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "B": w.B, "T": w.T, "S": w.S, "Hq": w.Hq,
                            "Hkv": w.Hkv, "head_dim": w.D, "window": w.window, "agent": w.agent,
-                           "ops": ops, "l2": "inputs larger than L2 (Q alone %.0f MB)" %
+                           "ops": ops, "qkv": "packed [B,T,S,Hq+2Hkv,D]" if packed else "separate",
+                           "l2": "inputs larger than L2 (Q alone %.0f MB)" %
                            (w.B * w.T * w.S * w.Hq * w.D * 2 / 1e6),
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "per_op": per_op, "roofline": roof, "cpu_baseline": cpu,
@@ -592,6 +631,9 @@ def main():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--ref-units", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--packed", action="store_true",
+                    help="read Q, K, V from one packed [B,T,S,Hq+2Hkv,D] tensor (fused QKV "
+                         "projection layout) and write packed dQKV")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (rollouts for the decode workload), e.g. "
                          "for a smaller profiling case")

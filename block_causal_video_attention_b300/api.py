@@ -65,6 +65,13 @@ def library():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = I
+            fwdp = [P, P, P, I, I, I, I, I, I, I, F, P]
+            bwdp = [P] * 8 + [I] * 7 + [F, P, Z, P]
+            for name, args in (("od_space_attn_fwd_packed", fwdp), ("od_time_attn_fwd_packed", fwdp),
+                               ("od_space_attn_bwd_packed", bwdp), ("od_time_attn_bwd_packed", bwdp)):
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = I
             lib.od_time_attn_decode.argtypes = [P] * 7 + [I] * 6 + [ctypes.c_longlong, F, P]
             lib.od_time_attn_decode.restype = I
             lib.od_space_attn_bwd_static_ws.argtypes = [P] * 12 + [I] * 7 + [F, P]
@@ -186,6 +193,94 @@ def time_attn_bwd(q, k, v, o, lse, dout, window, scale=None, fp32_grads=False,
     """Time attention backward -> (dQ, dK, dV) bf16 [, (dQ, dK, dV) fp32]."""
     return _bwd("od_time_attn_bwd", 1, q, k, v, o, lse, dout, window, scale, fp32_grads,
                 workspace, out, stream)
+
+
+def _check_packed(qkv, num_q_heads):
+    if not isinstance(qkv, torch.Tensor) or not qkv.is_cuda or qkv.dtype != torch.bfloat16:
+        raise TypeError("qkv must be a bf16 CUDA tensor")
+    if not qkv.is_contiguous() or qkv.dim() != 5:
+        raise ValueError("qkv must be a contiguous [B,T,S,Hq+2*Hkv,D] tensor")
+    B, T, S, P, D = qkv.shape
+    Hq = int(num_q_heads)
+    if Hq <= 0 or P <= Hq or (P - Hq) % 2:
+        raise ValueError("qkv head count %d does not split as Hq=%d + 2*Hkv" % (P, Hq))
+    return B, T, S, Hq, (P - Hq) // 2, D
+
+
+def _fwd_packed(name, qkv, num_q_heads, extra, scale, out, lse, stream):
+    B, T, S, Hq, Hkv, D = _check_packed(qkv, num_q_heads)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty((B, T, S, Hq, D), dtype=torch.bfloat16, device=qkv.device) if out is None else out
+    l = torch.empty((B, T, S, Hq), dtype=torch.float32, device=qkv.device) if lse is None else lse
+    if o.shape != (B, T, S, Hq, D) or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor [B,T,S,Hq,D]")
+    if l.shape != (B, T, S, Hq) or l.dtype != torch.float32 or not l.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,T,S,Hq]")
+    st = getattr(library(), name)(_ptr(qkv), _ptr(o), _ptr(l), B, T, S, Hq, Hkv, D, int(extra),
+                                  float(scale), _stream(stream))
+    if st:
+        raise ODError(st, name)
+    return o, l
+
+
+def space_attn_fwd_packed(qkv, num_q_heads, agent_idx=-1, scale=None, out=None, lse=None,
+                          stream=None):
+    """Space attention forward reading Q, K, V from one packed [B,T,S,Hq+2*Hkv,D] tensor."""
+    return _fwd_packed("od_space_attn_fwd_packed", qkv, num_q_heads, agent_idx, scale, out, lse,
+                       stream)
+
+
+def time_attn_fwd_packed(qkv, num_q_heads, window, scale=None, out=None, lse=None, stream=None):
+    """Time attention forward reading Q, K, V from one packed [B,T,S,Hq+2*Hkv,D] tensor."""
+    return _fwd_packed("od_time_attn_fwd_packed", qkv, num_q_heads, window, scale, out, lse,
+                       stream)
+
+
+def _bwd_packed(name, which, qkv, num_q_heads, o, lse, dout, extra, scale, fp32_grads,
+                workspace, out, stream):
+    B, T, S, Hq, Hkv, D = _check_packed(qkv, num_q_heads)
+    for nm, t in (("o", o), ("dout", dout)):
+        if t.shape != (B, T, S, Hq, D) or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous bf16 tensor [B,T,S,Hq,D]" % nm)
+    if lse.shape != (B, T, S, Hq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,T,S,Hq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dqkv = torch.empty_like(qkv) if out is None else out
+    if dqkv.shape != qkv.shape or dqkv.dtype != torch.bfloat16 or not dqkv.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like qkv")
+    f32 = (None, None, None)
+    if fp32_grads:
+        f32 = (torch.empty((B, T, S, Hq, D), dtype=torch.float32, device=qkv.device),
+               torch.empty((B, T, S, Hkv, D), dtype=torch.float32, device=qkv.device),
+               torch.empty((B, T, S, Hkv, D), dtype=torch.float32, device=qkv.device))
+    need = bwd_workspace_bytes(which, B, T, S, Hq, Hkv, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qkv.device)
+    st = getattr(library(), name)(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dqkv),
+                                  _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), B, T, S, Hq, Hkv, D,
+                                  int(extra), float(scale), _ptr(workspace),
+                                  ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if st:
+        raise ODError(st, name)
+    if fp32_grads:
+        return dqkv, f32
+    return dqkv
+
+
+def space_attn_bwd_packed(qkv, num_q_heads, o, lse, dout, agent_idx=-1, scale=None,
+                          fp32_grads=False, workspace=None, out=None, stream=None):
+    """Space attention backward on packed QKV -> dQKV (packed like qkv) [, fp32 dQ, dK, dV]."""
+    return _bwd_packed("od_space_attn_bwd_packed", 0, qkv, num_q_heads, o, lse, dout, agent_idx,
+                       scale, fp32_grads, workspace, out, stream)
+
+
+def time_attn_bwd_packed(qkv, num_q_heads, o, lse, dout, window, scale=None, fp32_grads=False,
+                         workspace=None, out=None, stream=None):
+    """Time attention backward on packed QKV -> dQKV (packed like qkv) [, fp32 dQ, dK, dV]."""
+    return _bwd_packed("od_time_attn_bwd_packed", 1, qkv, num_q_heads, o, lse, dout, window,
+                       scale, fp32_grads, workspace, out, stream)
 
 
 def time_attn_decode(q, k_new, v_new, k_cache, v_cache, t, scale=None, out=None, lse=None,

@@ -89,15 +89,17 @@ od_status check_shape(int B, int T, int S, int Hq, int Hkv, int D, float scale) 
   return OD_OK;
 }
 
-// 5-D tensor map over a [B,T,S,H,D] tensor of `elem` bytes per element.
+// 5-D tensor map over a [B,T,S,H,D] view of `elem` bytes per element whose consecutive tokens
+// (b, t, s) are `tok_rows` D-element rows apart (tok_rows = H for a contiguous tensor, more for
+// a view into a packed QKV tensor).
 od_status make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem, int B,
                    int T, int S, int H, int D, const uint32_t box[5],
-                   CUtensorMapSwizzle swizzle) {
+                   CUtensorMapSwizzle swizzle, int tok_rows) {
   cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)T,
                         (cuuint64_t)B};
   cuuint64_t strides[4];
   strides[0] = (cuuint64_t)D * elem;
-  strides[1] = strides[0] * H;
+  strides[1] = strides[0] * tok_rows;
   strides[2] = strides[1] * S;
   strides[3] = strides[2] * T;
   cuuint32_t bx[5] = {box[0], box[1], box[2], box[3], box[4]};
@@ -108,9 +110,11 @@ od_status make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int 
   return r == CUDA_SUCCESS ? OD_OK : OD_ERR_CUDA;
 }
 
+// qkv_rows: 0 for separate contiguous Q, K, V; else the D-element rows per token of the packed
+// [B,T,S,Hq+2Hkv,D] tensor that q, k and v point into.
 od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, void* o, float* lse,
                      int B, int T, int S, int Hq, int Hkv, int D, int agent, int window,
-                     float scale, void* stream) {
+                     float scale, void* stream, int qkv_rows = 0) {
   if (!q || !k || !v || !o || !lse) return OD_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return OD_ERR_INVALID_ARG;
@@ -155,9 +159,10 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   CUtensorMap tq, tk, tv;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, is_time ? qbox_time : qbox_space, sw)) ||
-      (st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw)) ||
-      (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw)))
+  const int q_rows = qkv_rows ? qkv_rows : Hq, kv_rows = qkv_rows ? qkv_rows : Hkv;
+  if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, is_time ? qbox_time : qbox_space, sw, q_rows)) ||
+      (st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw, kv_rows)) ||
+      (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw, kv_rows)))
     return st;
 
   const long long grid = p.nitems < dev->num_sms ? p.nitems : dev->num_sms;
@@ -170,7 +175,7 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S, int Hq,
                      int Hkv, int D, int agent, int window, float scale, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+                     size_t workspace_bytes, void* stream, int qkv_rows = 0) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
     return OD_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, workspace};
@@ -236,15 +241,16 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tq, tdo, tk, tv;
-  if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, qbox, sw)) ||
-      (st = make_map(&tdo, dout, bf, 2, B, T, S, Hq, D, qbox, sw)))
+  const int q_rows = qkv_rows ? qkv_rows : Hq, kv_rows = qkv_rows ? qkv_rows : Hkv;
+  if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, qbox, sw, q_rows)) ||
+      (st = make_map(&tdo, dout, bf, 2, B, T, S, Hq, D, qbox, sw, Hq)))
     return st;
   {
     const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kBN, 1, 1};
     const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kBN, 1};
     const uint32_t* kbox = is_time ? kbox_time : kbox_space;
-    if ((st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, kbox, sw)) ||
-        (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, kbox, sw)))
+    if ((st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)) ||
+        (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)))
       return st;
     od::DqParams dp{};
     dp.f = f;
@@ -252,6 +258,7 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     dp.delta = delta;
     dp.scale = scale;
     dp.dq = static_cast<__nv_bfloat16*>(dq);
+    dp.dq_rows = q_rows;
     dp.dq_f32 = dq_f32;
     dp.amax = amax;
     const long long grid = f.nitems < num_ctas ? f.nitems : num_ctas;
@@ -268,8 +275,8 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kKvBN, 1, 1};
     const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kKvBN, 1};
     const uint32_t* kbox = is_time ? kbox_time : kbox_space;
-    if ((st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, kbox, sw)) ||
-        (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, kbox, sw)))
+    if ((st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)) ||
+        (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)))
       return st;
     od::KvParams kp{};
     kp.f = f;
@@ -280,6 +287,7 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     kp.nitems = 1LL * B * f.F * Hkv * kp.nkb;
     kp.dk = static_cast<__nv_bfloat16*>(dk);
     kp.dv = static_cast<__nv_bfloat16*>(dv);
+    kp.kv_rows = kv_rows;
     kp.dk_f32 = dk_f32;
     kp.dv_f32 = dv_f32;
     kp.amax = amax;
@@ -437,6 +445,83 @@ od_status od_time_attn_decode(const void* q, const void* k_new, const void* v_ne
                               int D, int window, long long t, float scale, void* stream) {
   return launch_decode(q, k_new, v_new, k_cache, v_cache, o, lse, B, S, Hq, Hkv, D, window, t,
                        scale, stream);
+}
+
+// ---- packed QKV: q, k, v are the head ranges [0,Hq), [Hq,Hq+Hkv), [Hq+Hkv,Hq+2Hkv) of one
+// [B,T,S,Hq+2Hkv,D] tensor (the output of a fused QKV projection, viewed as heads).
+static od_status packed_views(const void* qkv, int B, int T, int S, int Hq, int Hkv, int D,
+                              const void** q, const void** k, const void** v, int* rows) {
+  if (!qkv || B <= 0 || T <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0)
+    return OD_ERR_INVALID_ARG;
+  if (D != 64) return OD_ERR_UNSUPPORTED;
+  *rows = Hq + 2 * Hkv;
+  if (1LL * B * T * S * (*rows) * D * 2 >= (1LL << 40)) return OD_ERR_UNSUPPORTED;
+  const uint8_t* base = static_cast<const uint8_t*>(qkv);
+  *q = base;
+  *k = base + static_cast<size_t>(Hq) * D * 2;
+  *v = base + static_cast<size_t>(Hq + Hkv) * D * 2;
+  return OD_OK;
+}
+
+static od_status fwd_packed(int is_time, const void* qkv, void* o, float* lse, int B, int T, int S,
+                            int Hq, int Hkv, int D, int agent, int window, float scale,
+                            void* stream) {
+  const void *q, *k, *v;
+  int rows = 0;
+  od_status st = packed_views(qkv, B, T, S, Hq, Hkv, D, &q, &k, &v, &rows);
+  if (st != OD_OK) return st;
+  return launch_fwd(is_time, q, k, v, o, lse, B, T, S, Hq, Hkv, D, agent, window, scale, stream,
+                    rows);
+}
+
+static od_status bwd_packed(int is_time, const void* qkv, const void* o, const float* lse,
+                            const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
+                            float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D, int agent,
+                            int window, float scale, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  const void *q, *k, *v, *dq, *dk, *dv;
+  int rows = 0;
+  od_status st = packed_views(qkv, B, T, S, Hq, Hkv, D, &q, &k, &v, &rows);
+  if (st != OD_OK) return st;
+  if (!dqkv) return OD_ERR_INVALID_ARG;
+  {  // the gradients must not overwrite the inputs they are computed from
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(qkv), b0 = reinterpret_cast<uintptr_t>(dqkv);
+    const uintptr_t n = static_cast<uintptr_t>(1ULL * B * T * S * rows * D * 2);
+    if (a0 < b0 + n && b0 < a0 + n) return OD_ERR_INVALID_ARG;
+  }
+  if ((st = packed_views(dqkv, B, T, S, Hq, Hkv, D, &dq, &dk, &dv, &rows)) != OD_OK) return st;
+  return launch_bwd(is_time, q, k, v, o, lse, dout, const_cast<void*>(dq), const_cast<void*>(dk),
+                    const_cast<void*>(dv), dq_f32, dk_f32, dv_f32, B, T, S, Hq, Hkv, D, agent,
+                    window, scale, workspace, workspace_bytes, stream, rows);
+}
+
+od_status od_space_attn_fwd_packed(const void* qkv, void* o, float* lse, int B, int T, int S,
+                                   int Hq, int Hkv, int D, int agent_idx, float scale,
+                                   void* stream) {
+  return fwd_packed(0, qkv, o, lse, B, T, S, Hq, Hkv, D, agent_idx, 1, scale, stream);
+}
+
+od_status od_time_attn_fwd_packed(const void* qkv, void* o, float* lse, int B, int T, int S,
+                                  int Hq, int Hkv, int D, int window, float scale, void* stream) {
+  return fwd_packed(1, qkv, o, lse, B, T, S, Hq, Hkv, D, -1, window, scale, stream);
+}
+
+od_status od_space_attn_bwd_packed(const void* qkv, const void* o, const float* lse,
+                                   const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
+                                   float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D,
+                                   int agent_idx, float scale, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return bwd_packed(0, qkv, o, lse, dout, dqkv, dq_f32, dk_f32, dv_f32, B, T, S, Hq, Hkv, D,
+                    agent_idx, 1, scale, workspace, workspace_bytes, stream);
+}
+
+od_status od_time_attn_bwd_packed(const void* qkv, const void* o, const float* lse,
+                                  const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
+                                  float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D,
+                                  int window, float scale, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return bwd_packed(1, qkv, o, lse, dout, dqkv, dq_f32, dk_f32, dv_f32, B, T, S, Hq, Hkv, D, -1,
+                    window, scale, workspace, workspace_bytes, stream);
 }
 
 od_status od_get_device_status_detail(void* stream, unsigned int* site_word) {

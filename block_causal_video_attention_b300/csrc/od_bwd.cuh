@@ -111,7 +111,8 @@ struct DqParams {
   int amax_slots;         // dQ pass: slots the Delta pass wrote (scales for the fp16 products)
   float scale;
   __nv_bfloat16* dq;
-  float* dq_f32;          // optional
+  int dq_rows;            // 64-element rows per token of dq (Hq, or Hq + 2 Hkv when packed)
+  float* dq_f32;          // optional, contiguous [B,T,S,Hq,64]
 };
 
 struct DqSmem {
@@ -643,7 +644,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             const long long t_idx = p.is_time ? ps : it.fixed;
             const long long s_idx = p.is_time ? it.fixed : ps;
             const long long rw =
-                ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + gg;
+                ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * dp.dq_rows + it.kvh * G + gg;
             const uint4 wv = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
             reinterpret_cast<uint4*>(dp.dq + rw * 64)[ch] = wv;
           }
@@ -700,7 +701,8 @@ struct KvParams {
   int nkb;                // 128-key blocks per unit
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* dk_f32;
+  int kv_rows;            // 64-element rows per token of dk / dv (Hkv, or Hq + 2 Hkv when packed)
+  float* dk_f32;          // optional, contiguous [B,T,S,Hkv,64]
   float* dv_f32;
 };
 
@@ -1217,8 +1219,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const float f = h ? ldexpf(1.f, -edo) : kp.scale * ldexpf(1.f, -(eds + eq));
         const long long t_idx = p.is_time ? kpos : it.fixed;
         const long long s_idx = p.is_time ? it.fixed : kpos;
-        const long long row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hkv + it.kvh;
-        uint4* out = reinterpret_cast<uint4*>((h ? kp.dv : kp.dk) + row * 64);
+        const long long tok = (static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx;
+        const long long row = tok * p.Hkv + it.kvh;
+        uint4* out = reinterpret_cast<uint4*>((h ? kp.dv : kp.dk) + (tok * kp.kv_rows + it.kvh) * 64);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint4 a;

@@ -94,6 +94,32 @@ od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const vo
                            int Hq, int Hkv, int D, int window, float scale, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* Packed-QKV forms.  Each layer of the block-causal backbone alternates space and time
+ * attention (7minutos.es page, section "Arquitectura: una columna vertebral, dos modelos"),
+ * and a fused QKV projection writes one [B, T, S, Hq + 2*Hkv, D] bf16 tensor per layer: per
+ * token the Hq query heads, then the Hkv key heads, then the Hkv value heads.  These calls
+ * read Q, K and V straight from that tensor (no split or copy) and compute exactly what the
+ * unpacked calls compute, with the same kernels.  O, LSE and dO keep their contiguous
+ * layouts; the backward writes dQ, dK and dV into `dqkv`, a second tensor of the packed shape
+ * (heads in the same order), which must not be `qkv` (it may not overlap it at all).  The
+ * optional fp32 gradient copies (dq_f32 ...) stay contiguous [B,T,S,H,D].  Errors as for the
+ * unpacked calls. */
+od_status od_space_attn_fwd_packed(const void* qkv, void* o, float* lse, int B, int T, int S,
+                                   int Hq, int Hkv, int D, int agent_idx, float scale,
+                                   void* stream);
+od_status od_time_attn_fwd_packed(const void* qkv, void* o, float* lse, int B, int T, int S,
+                                  int Hq, int Hkv, int D, int window, float scale, void* stream);
+od_status od_space_attn_bwd_packed(const void* qkv, const void* o, const float* lse,
+                                   const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
+                                   float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D,
+                                   int agent_idx, float scale, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+od_status od_time_attn_bwd_packed(const void* qkv, const void* o, const float* lse,
+                                  const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
+                                  float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D,
+                                  int window, float scale, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
 /* One rollout (decode) step of time attention over a ring-buffer KV cache.  A rollout
  * generates one frame at a time (the local rollout harness and the frame-by-frame demo,
  * 7minutos.es page, section "Lo que realmente se envió"); the time layer then needs, for

@@ -21,6 +21,8 @@ def test_every_declared_symbol_is_exported(lib):
     assert {"od_space_attn_fwd", "od_time_attn_fwd", "od_space_attn_bwd", "od_time_attn_bwd",
             "od_attn_bwd_workspace_bytes", "od_get_device_status", "od_get_device_status_detail",
             "od_status_string", "od_space_attn_bwd_static_ws", "od_time_attn_decode",
+            "od_space_attn_fwd_packed", "od_time_attn_fwd_packed", "od_space_attn_bwd_packed",
+            "od_time_attn_bwd_packed",
             "od_version"} <= declared
     for name in declared:
         assert hasattr(lib, name), name
@@ -105,6 +107,23 @@ def test_decode_rejects_invalid_arguments(lib):
     assert call(D=32) == 2
     assert call(Hq=34, Hkv=2) == 2                                  # G = 17 > 16
     assert call(W=(1 << 24) + 1) == 2
+
+
+def test_packed_calls_reject_invalid_arguments(lib):
+    f = lib.od_space_attn_fwd_packed
+    assert f(P(0), GOOD, GOOD, 1, 4, 8, 4, 2, 64, 0, 0.125, P(0)) == 1          # null qkv
+    assert f(GOOD, GOOD, GOOD, 1, 4, 8, 4, 2, 32, 0, 0.125, P(0)) == 2          # D != 64
+    assert f(GOOD, GOOD, GOOD, 1, 4, 8, 5, 2, 64, 0, 0.125, P(0)) == 1          # Hq % Hkv
+    assert lib.od_time_attn_fwd_packed(GOOD, GOOD, GOOD, 1, 4, 8, 4, 2, 64, 0, 0.125, P(0)) == 1
+    b = lib.od_space_attn_bwd_packed
+    ws = lib.od_attn_bwd_workspace_bytes(0, 1, 4, 8, 4, 2, 64)
+    n = 1 * 4 * 8 * (4 + 2 * 2) * 64 * 2          # bytes of one packed tensor
+    args = lambda qkv, dqkv: (qkv, GOOD, GOOD, GOOD, dqkv, P(0), P(0), P(0), 1, 4, 8, 4, 2, 64, 0,
+                              0.125, GOOD, ws, P(0))
+    assert b(*args(P(1 << 20), P(0))) == 1                                      # null dqkv
+    assert b(*args(P(1 << 20), P((1 << 20) + n - 16))) == 1                     # overlapping
+    assert b(*args(P((1 << 20) + n - 16), P(1 << 20))) == 1
+    assert lib.od_time_attn_bwd_packed(*args(P(1 << 20), P(1 << 20))) == 1      # aliased
 
 
 def test_binding_refuses_cpu_tensors():
