@@ -66,13 +66,20 @@ def bwd_bytes(w):
 
 
 # DRAM bytes (read + write) per call of an operator, summed over its kernels, from one ncu
-# capture of `python bench.py --op <op> --steps 1 --warmup 1` with
+# capture of `python bench.py --op <op> --steps 1 --warmup 1 --no-cpu-baseline` with
 # --metrics dram__bytes_read.sum,dram__bytes_write.sum (summary in profiles/).  They hold only
 # for the kernel sources they were measured on: any change to those sources voids them.
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "b1c82169971116aac0ab6bfffa1ae7d8c9e6c05ec8c393527c79c85c5a2f585c",
-    "minecraft_fwd_bwd": {"space_bwd": 700783104 + 17130496 + 722481664 + 258122752 + 645415168 + 47542272,
-                          "space_fwd": 389018880 + 260273920},
+    "csrc_sha256": "003634db7e40ed0f8f0a58ac8603ff146c6b0f1916c4c048b1cc35c1d4fcbf56",
+    "minecraft_fwd_bwd": {
+        # forward with the O residual; backward: Delta from O + O_lo, dQ, dK/dV
+        "space_fwd": 927257344,
+        "time_fwd": 924111104,
+        "space_bwd": 2883083520,
+        "time_bwd": 2898746368,
+    },
+    # decode: 4-rollout capture (176.43 MB read, 5.53 MB written) scaled by the units (x4)
+    "minecraft_decode": {"decode": 727837696},
 }
 
 
@@ -289,6 +296,11 @@ def run_ours(args, w, with_bwd):
                            dtype=torch.uint8, device=dev)
 
     ev = {op: [] for op in ops}
+    # the forward also writes O's rounding residual so that the backward reads Delta from
+    # memory (unless --no-residual: then the backward recomputes it from P and dP)
+    lo_s = lo_t = None
+    if with_bwd and not args.no_residual:
+        lo_s, lo_t = torch.empty_like(dq), torch.empty_like(dq)
 
     def step(record, Q=dq, K=dk, V=dv, DO=dd, QKV=None):
         if packed:
@@ -304,15 +316,19 @@ def run_ours(args, w, with_bwd):
             else:
                 fn()
         if "space_fwd" in run:
-            timed("space_fwd", lambda: api.space_attn_fwd(Q, K, V, w.agent, w.scale, o_s, l_s, stream))
+            timed("space_fwd", lambda: api.space_attn_fwd(Q, K, V, w.agent, w.scale, o_s, l_s, stream,
+                                                          o_lo=lo_s))
         if "time_fwd" in run:
-            timed("time_fwd", lambda: api.time_attn_fwd(Q, K, V, w.window, w.scale, o_t, l_t, stream))
+            timed("time_fwd", lambda: api.time_attn_fwd(Q, K, V, w.window, w.scale, o_t, l_t, stream,
+                                                        o_lo=lo_t))
         if "space_bwd" in run:
             timed("space_bwd", lambda: api.space_attn_bwd(Q, K, V, o_s, l_s, DO, w.agent, w.scale,
-                                                          workspace=ws_s, out=g[:3], stream=stream))
+                                                          workspace=ws_s, out=g[:3], stream=stream,
+                                                          o_lo=lo_s))
         if "time_bwd" in run:
             timed("time_bwd", lambda: api.time_attn_bwd(Q, K, V, o_t, l_t, DO, w.window, w.scale,
-                                                        workspace=ws_t, out=g[3:], stream=stream))
+                                                        workspace=ws_t, out=g[3:], stream=stream,
+                                                        o_lo=lo_t))
 
     def step_packed(record, QKV, DO):
         def timed(op, fn):
@@ -325,22 +341,26 @@ def run_ours(args, w, with_bwd):
             else:
                 fn()
         if "space_fwd" in run:
-            timed("space_fwd", lambda: api.space_attn_fwd_packed(QKV, w.Hq, w.agent, w.scale, o_s, l_s, stream))
+            timed("space_fwd", lambda: api.space_attn_fwd_packed(QKV, w.Hq, w.agent, w.scale, o_s, l_s,
+                                                                 stream, o_lo=lo_s))
         if "time_fwd" in run:
-            timed("time_fwd", lambda: api.time_attn_fwd_packed(QKV, w.Hq, w.window, w.scale, o_t, l_t, stream))
+            timed("time_fwd", lambda: api.time_attn_fwd_packed(QKV, w.Hq, w.window, w.scale, o_t, l_t,
+                                                               stream, o_lo=lo_t))
         if "space_bwd" in run:
             timed("space_bwd", lambda: api.space_attn_bwd_packed(
-                QKV, w.Hq, o_s, l_s, DO, w.agent, w.scale, workspace=ws_s, out=g_packed[0], stream=stream))
+                QKV, w.Hq, o_s, l_s, DO, w.agent, w.scale, workspace=ws_s, out=g_packed[0], stream=stream,
+                o_lo=lo_s))
         if "time_bwd" in run:
             timed("time_bwd", lambda: api.time_attn_bwd_packed(
-                QKV, w.Hq, o_t, l_t, DO, w.window, w.scale, workspace=ws_t, out=g_packed[1], stream=stream))
+                QKV, w.Hq, o_t, l_t, DO, w.window, w.scale, workspace=ws_t, out=g_packed[1], stream=stream,
+                o_lo=lo_t))
 
     if args.op and args.op.endswith("_bwd"):
         # the backward reads the forward's O and LSE: produce them once, outside the timing
         if args.op == "space_bwd":
-            api.space_attn_fwd(dq, dk, dv, w.agent, w.scale, o_s, l_s, stream)
+            api.space_attn_fwd(dq, dk, dv, w.agent, w.scale, o_s, l_s, stream, o_lo=lo_s)
         else:
-            api.time_attn_fwd(dq, dk, dv, w.window, w.scale, o_t, l_t, stream)
+            api.time_attn_fwd(dq, dk, dv, w.window, w.scale, o_t, l_t, stream, o_lo=lo_t)
     clk = Clocks(local).__enter__()
     for _ in range(args.warmup):
         step(False)
@@ -439,7 +459,9 @@ def run_ours(args, w, with_bwd):
                 "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "B": w.B, "T": w.T, "S": w.S, "Hq": w.Hq,
                            "Hkv": w.Hkv, "head_dim": w.D, "window": w.window, "agent": w.agent,
-                           "ops": ops, "qkv": "packed [B,T,S,Hq+2Hkv,D]" if packed else "separate",
+                           "ops": ops, "delta": ("recomputed from P and dP" if (not with_bwd or args.no_residual)
+                                                 else "from O + O_lo (forward writes the residual)"),
+                           "qkv": "packed [B,T,S,Hq+2Hkv,D]" if packed else "separate",
                            "l2": "inputs larger than L2 (Q alone %.0f MB)" %
                            (w.B * w.T * w.S * w.Hq * w.D * 2 / 1e6),
                            "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -631,6 +653,8 @@ def main():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--ref-units", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-residual", action="store_true",
+                    help="the forward does not write O's residual; the backward recomputes Delta")
     ap.add_argument("--packed", action="store_true",
                     help="read Q, K, V from one packed [B,T,S,Hq+2Hkv,D] tensor (fused QKV "
                          "projection layout) and write packed dQKV")

@@ -58,15 +58,15 @@ def library():
                 raise ODError(3, "libod_attn.so is not built (run __graft_entry__.build())")
             lib = ctypes.CDLL(_LIB_PATH)
             P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-            fwd = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
-            bwd = [P] * 12 + [I] * 7 + [F, P, Z, P]
+            fwd = [P] * 6 + [I] * 7 + [F, P]
+            bwd = [P] * 13 + [I] * 7 + [F, P, Z, P]
             for name, args in (("od_space_attn_fwd", fwd), ("od_time_attn_fwd", fwd),
                                ("od_space_attn_bwd", bwd), ("od_time_attn_bwd", bwd)):
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = I
-            fwdp = [P, P, P, I, I, I, I, I, I, I, F, P]
-            bwdp = [P] * 8 + [I] * 7 + [F, P, Z, P]
+            fwdp = [P] * 4 + [I] * 7 + [F, P]
+            bwdp = [P] * 9 + [I] * 7 + [F, P, Z, P]
             for name, args in (("od_space_attn_fwd_packed", fwdp), ("od_time_attn_fwd_packed", fwdp),
                                ("od_space_attn_bwd_packed", bwdp), ("od_time_attn_bwd_packed", bwdp)):
                 fn = getattr(lib, name)
@@ -74,7 +74,7 @@ def library():
                 fn.restype = I
             lib.od_time_attn_decode.argtypes = [P] * 7 + [I] * 6 + [ctypes.c_longlong, F, P]
             lib.od_time_attn_decode.restype = I
-            lib.od_space_attn_bwd_static_ws.argtypes = [P] * 12 + [I] * 7 + [F, P]
+            lib.od_space_attn_bwd_static_ws.argtypes = [P] * 13 + [I] * 7 + [F, P]
             lib.od_space_attn_bwd_static_ws.restype = I
             lib.od_attn_bwd_workspace_bytes.argtypes = [I] * 7
             lib.od_attn_bwd_workspace_bytes.restype = Z
@@ -117,7 +117,18 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _fwd(name, q, k, v, extra, scale, out, lse, stream):
+def _residual_out(o_lo, shape, device):
+    """o_lo: None (not requested), True (allocate) or a tensor to fill."""
+    if o_lo is None or o_lo is False:
+        return None
+    if o_lo is True:
+        return torch.empty(shape, dtype=torch.bfloat16, device=device)
+    if o_lo.shape != shape or o_lo.dtype != torch.bfloat16 or not o_lo.is_contiguous():
+        raise ValueError("o_lo must be a contiguous bf16 tensor shaped like O")
+    return o_lo
+
+
+def _fwd(name, q, k, v, extra, scale, out, lse, o_lo, stream):
     B, T, S, Hq, Hkv, D = _check_qkv(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
@@ -127,28 +138,33 @@ def _fwd(name, q, k, v, extra, scale, out, lse, stream):
         raise ValueError("out must be a contiguous bf16 tensor shaped like q")
     if l.shape != (B, T, S, Hq) or l.dtype != torch.float32 or not l.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor [B,T,S,Hq]")
-    st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, T, S, Hq,
-                                  Hkv, D, int(extra), float(scale), _stream(stream))
+    r = _residual_out(o_lo, tuple(q.shape), q.device)
+    st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(r), B, T, S,
+                                  Hq, Hkv, D, int(extra), float(scale), _stream(stream))
     if st:
         raise ODError(st, name)
-    return o, l
+    return (o, l) if r is None else (o, l, r)
 
 
-def space_attn_fwd(q, k, v, agent_idx=-1, scale=None, out=None, lse=None, stream=None):
-    """Masked space attention forward -> (O bf16, LSE fp32)."""
-    return _fwd("od_space_attn_fwd", q, k, v, agent_idx, scale, out, lse, stream)
+def space_attn_fwd(q, k, v, agent_idx=-1, scale=None, out=None, lse=None, stream=None, o_lo=None):
+    """Masked space attention forward -> (O bf16, LSE fp32) [, O_lo].
+
+    o_lo=True (or a bf16 tensor shaped like O) also returns O's rounding residual
+    bf16(O - o), which the backward can take to read Delta from memory."""
+    return _fwd("od_space_attn_fwd", q, k, v, agent_idx, scale, out, lse, o_lo, stream)
 
 
-def time_attn_fwd(q, k, v, window, scale=None, out=None, lse=None, stream=None):
-    """Sliding-window causal time attention forward -> (O bf16, LSE fp32)."""
-    return _fwd("od_time_attn_fwd", q, k, v, window, scale, out, lse, stream)
+def time_attn_fwd(q, k, v, window, scale=None, out=None, lse=None, stream=None, o_lo=None):
+    """Sliding-window causal time attention forward -> (O bf16, LSE fp32) [, O_lo]."""
+    return _fwd("od_time_attn_fwd", q, k, v, window, scale, out, lse, o_lo, stream)
 
 
 def bwd_workspace_bytes(which, B, T, S, Hq, Hkv, D=64):
     return int(library().od_attn_bwd_workspace_bytes(int(which), B, T, S, Hq, Hkv, D))
 
 
-def _bwd(name, which, q, k, v, o, lse, dout, extra, scale, fp32_grads, workspace, out, stream):
+def _bwd(name, which, q, k, v, o, lse, dout, extra, scale, fp32_grads, workspace, out, stream,
+         o_lo=None):
     B, T, S, Hq, Hkv, D = _check_qkv(q, k, v)
     for nm, t in (("o", o), ("dout", dout)):
         if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
@@ -169,7 +185,10 @@ def _bwd(name, which, q, k, v, o, lse, dout, extra, scale, fp32_grads, workspace
     need = bwd_workspace_bytes(which, B, T, S, Hq, Hkv, D)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+    if o_lo is not None and (o_lo.shape != q.shape or o_lo.dtype != torch.bfloat16
+                             or not o_lo.is_contiguous()):
+        raise ValueError("o_lo must be a contiguous bf16 tensor shaped like q")
+    st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_lo), _ptr(lse), _ptr(dout),
                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(f32[0]), _ptr(f32[1]),
                                   _ptr(f32[2]), B, T, S, Hq, Hkv, D, int(extra), float(scale),
                                   _ptr(workspace), ctypes.c_size_t(workspace.numel()),
@@ -182,17 +201,19 @@ def _bwd(name, which, q, k, v, o, lse, dout, extra, scale, fp32_grads, workspace
 
 
 def space_attn_bwd(q, k, v, o, lse, dout, agent_idx=-1, scale=None, fp32_grads=False,
-                   workspace=None, out=None, stream=None):
-    """Space attention backward -> (dQ, dK, dV) bf16 [, (dQ, dK, dV) fp32]."""
+                   workspace=None, out=None, stream=None, o_lo=None):
+    """Space attention backward -> (dQ, dK, dV) bf16 [, (dQ, dK, dV) fp32].
+
+    o_lo: the residual the forward returned (optional; Delta is recomputed without it)."""
     return _bwd("od_space_attn_bwd", 0, q, k, v, o, lse, dout, agent_idx, scale, fp32_grads,
-                workspace, out, stream)
+                workspace, out, stream, o_lo)
 
 
 def time_attn_bwd(q, k, v, o, lse, dout, window, scale=None, fp32_grads=False,
-                  workspace=None, out=None, stream=None):
+                  workspace=None, out=None, stream=None, o_lo=None):
     """Time attention backward -> (dQ, dK, dV) bf16 [, (dQ, dK, dV) fp32]."""
     return _bwd("od_time_attn_bwd", 1, q, k, v, o, lse, dout, window, scale, fp32_grads,
-                workspace, out, stream)
+                workspace, out, stream, o_lo)
 
 
 def _check_packed(qkv, num_q_heads):
@@ -207,7 +228,7 @@ def _check_packed(qkv, num_q_heads):
     return B, T, S, Hq, (P - Hq) // 2, D
 
 
-def _fwd_packed(name, qkv, num_q_heads, extra, scale, out, lse, stream):
+def _fwd_packed(name, qkv, num_q_heads, extra, scale, out, lse, stream, o_lo=None):
     B, T, S, Hq, Hkv, D = _check_packed(qkv, num_q_heads)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
@@ -217,28 +238,30 @@ def _fwd_packed(name, qkv, num_q_heads, extra, scale, out, lse, stream):
         raise ValueError("out must be a contiguous bf16 tensor [B,T,S,Hq,D]")
     if l.shape != (B, T, S, Hq) or l.dtype != torch.float32 or not l.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor [B,T,S,Hq]")
-    st = getattr(library(), name)(_ptr(qkv), _ptr(o), _ptr(l), B, T, S, Hq, Hkv, D, int(extra),
-                                  float(scale), _stream(stream))
+    r = _residual_out(o_lo, (B, T, S, Hq, D), qkv.device)
+    st = getattr(library(), name)(_ptr(qkv), _ptr(o), _ptr(l), _ptr(r), B, T, S, Hq, Hkv, D,
+                                  int(extra), float(scale), _stream(stream))
     if st:
         raise ODError(st, name)
-    return o, l
+    return (o, l) if r is None else (o, l, r)
 
 
 def space_attn_fwd_packed(qkv, num_q_heads, agent_idx=-1, scale=None, out=None, lse=None,
-                          stream=None):
+                          stream=None, o_lo=None):
     """Space attention forward reading Q, K, V from one packed [B,T,S,Hq+2*Hkv,D] tensor."""
     return _fwd_packed("od_space_attn_fwd_packed", qkv, num_q_heads, agent_idx, scale, out, lse,
-                       stream)
+                       stream, o_lo)
 
 
-def time_attn_fwd_packed(qkv, num_q_heads, window, scale=None, out=None, lse=None, stream=None):
+def time_attn_fwd_packed(qkv, num_q_heads, window, scale=None, out=None, lse=None, stream=None,
+                         o_lo=None):
     """Time attention forward reading Q, K, V from one packed [B,T,S,Hq+2*Hkv,D] tensor."""
     return _fwd_packed("od_time_attn_fwd_packed", qkv, num_q_heads, window, scale, out, lse,
-                       stream)
+                       stream, o_lo)
 
 
 def _bwd_packed(name, which, qkv, num_q_heads, o, lse, dout, extra, scale, fp32_grads,
-                workspace, out, stream):
+                workspace, out, stream, o_lo=None):
     B, T, S, Hq, Hkv, D = _check_packed(qkv, num_q_heads)
     for nm, t in (("o", o), ("dout", dout)):
         if t.shape != (B, T, S, Hq, D) or t.dtype != torch.bfloat16 or not t.is_contiguous():
@@ -258,7 +281,10 @@ def _bwd_packed(name, which, qkv, num_q_heads, o, lse, dout, extra, scale, fp32_
     need = bwd_workspace_bytes(which, B, T, S, Hq, Hkv, D)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qkv.device)
-    st = getattr(library(), name)(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dqkv),
+    if o_lo is not None and (o_lo.shape != o.shape or o_lo.dtype != torch.bfloat16
+                             or not o_lo.is_contiguous()):
+        raise ValueError("o_lo must be a contiguous bf16 tensor shaped like o")
+    st = getattr(library(), name)(_ptr(qkv), _ptr(o), _ptr(o_lo), _ptr(lse), _ptr(dout), _ptr(dqkv),
                                   _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), B, T, S, Hq, Hkv, D,
                                   int(extra), float(scale), _ptr(workspace),
                                   ctypes.c_size_t(workspace.numel()), _stream(stream))
@@ -270,17 +296,17 @@ def _bwd_packed(name, which, qkv, num_q_heads, o, lse, dout, extra, scale, fp32_
 
 
 def space_attn_bwd_packed(qkv, num_q_heads, o, lse, dout, agent_idx=-1, scale=None,
-                          fp32_grads=False, workspace=None, out=None, stream=None):
+                          fp32_grads=False, workspace=None, out=None, stream=None, o_lo=None):
     """Space attention backward on packed QKV -> dQKV (packed like qkv) [, fp32 dQ, dK, dV]."""
     return _bwd_packed("od_space_attn_bwd_packed", 0, qkv, num_q_heads, o, lse, dout, agent_idx,
-                       scale, fp32_grads, workspace, out, stream)
+                       scale, fp32_grads, workspace, out, stream, o_lo)
 
 
 def time_attn_bwd_packed(qkv, num_q_heads, o, lse, dout, window, scale=None, fp32_grads=False,
-                         workspace=None, out=None, stream=None):
+                         workspace=None, out=None, stream=None, o_lo=None):
     """Time attention backward on packed QKV -> dQKV (packed like qkv) [, fp32 dQ, dK, dV]."""
     return _bwd_packed("od_time_attn_bwd_packed", 1, qkv, num_q_heads, o, lse, dout, window,
-                       scale, fp32_grads, workspace, out, stream)
+                       scale, fp32_grads, workspace, out, stream, o_lo)
 
 
 def time_attn_decode(q, k_new, v_new, k_cache, v_cache, t, scale=None, out=None, lse=None,

@@ -28,6 +28,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
+  int delta_o_ctas = 0;  // resident CTAs of the Delta-from-O kernel (one wave), <= kAmaxSlots
   unsigned int* status = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
@@ -55,6 +56,14 @@ od_status device_state(DeviceState** out) {
         fa.numRegs != od::kFwdLaunchRegs)
       return OD_ERR_CUDA;
     if (od::bwd_setup() != cudaSuccess) return OD_ERR_CUDA;
+    {
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, od::od_bwd_delta_o_kernel,
+                                                        od::kDeltaOThreads, 0) != cudaSuccess ||
+          per_sm < 1)
+        return OD_ERR_CUDA;
+      d.delta_o_ctas = per_sm * d.num_sms < od::kAmaxSlots ? per_sm * d.num_sms : od::kAmaxSlots;
+    }
     if (cudaFuncSetAttribute(od::od_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(od::kDecSmemBytes)) != cudaSuccess)
       return OD_ERR_CUDA;
@@ -113,10 +122,11 @@ od_status make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int 
 // qkv_rows: 0 for separate contiguous Q, K, V; else the D-element rows per token of the packed
 // [B,T,S,Hq+2Hkv,D] tensor that q, k and v point into.
 od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, void* o, float* lse,
-                     int B, int T, int S, int Hq, int Hkv, int D, int agent, int window,
-                     float scale, void* stream, int qkv_rows = 0) {
+                     void* o_lo, int B, int T, int S, int Hq, int Hkv, int D, int agent,
+                     int window, float scale, void* stream, int qkv_rows = 0) {
   if (!q || !k || !v || !o || !lse) return OD_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (o_lo && !aligned16(o_lo)))
     return OD_ERR_INVALID_ARG;
   od_status st = check_shape(B, T, S, Hq, Hkv, D, scale);
   if (st != OD_OK) return st;
@@ -156,6 +166,7 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kFwdBN, 1, 1};
   const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kFwdBN, 1};
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.o_lo = static_cast<__nv_bfloat16*>(o_lo);
   CUtensorMap tq, tk, tv;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -172,13 +183,13 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
 }
 
 od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, const void* o,
-                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     const void* o_lo, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S, int Hq,
                      int Hkv, int D, int agent, int window, float scale, void* workspace,
                      size_t workspace_bytes, void* stream, int qkv_rows = 0) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
     return OD_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, workspace};
+  const void* ptrs[] = {q, k, v, o, o_lo, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, workspace};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return OD_ERR_INVALID_ARG;
   od_status st = check_shape(B, T, S, Hq, Hkv, D, scale);
@@ -264,8 +275,28 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     const long long grid = f.nitems < num_ctas ? f.nitems : num_ctas;
     amax_slots = static_cast<int>(grid);
     dp.amax_slots = amax_slots;
-    // 1. Delta pass, 2. dQ
-    od::od_bwd_dq_kernel<true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+    // 1. Delta (from O and its residual when the forward wrote it, else the Delta pass),
+    // 2. dQ
+    if (o_lo) {
+      od::DeltaOParams d{};
+      d.o = static_cast<const __nv_bfloat16*>(o);
+      d.o_lo = static_cast<const __nv_bfloat16*>(o_lo);
+      d.dout = static_cast<const __nv_bfloat16*>(dout);
+      d.q = static_cast<const __nv_bfloat16*>(q);
+      d.k = static_cast<const __nv_bfloat16*>(k);
+      d.v = static_cast<const __nv_bfloat16*>(v);
+      d.ntok = 1LL * B * T * S;
+      d.Hq = Hq; d.Hkv = Hkv; d.q_rows = q_rows; d.kv_rows = kv_rows;
+      d.delta = delta;
+      d.amax = amax;
+      // one wave of resident CTAs: every CTA streams an equal share
+      const long long dgrid = dev->delta_o_ctas;
+      amax_slots = static_cast<int>(dgrid);
+      dp.amax_slots = amax_slots;
+      od::od_bwd_delta_o_kernel<<<(unsigned)dgrid, od::kDeltaOThreads, 0, strm>>>(d);
+    } else {
+      od::od_bwd_dq_kernel<true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+    }
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
     od::od_bwd_dq_kernel<false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
@@ -388,7 +419,7 @@ od_status static_ws_pointer(void** out) {
 extern "C" {
 
 od_status od_space_attn_bwd_static_ws(const void* q, const void* k, const void* v, const void* o,
-                                      const float* lse, const void* dout, void* dq, void* dk,
+                                      const void* o_lo, const float* lse, const void* dout, void* dq, void* dk,
                                       void* dv, float* dq_f32, float* dk_f32, float* dv_f32, int B,
                                       int T, int S, int Hq, int Hkv, int D, int agent_idx,
                                       float scale, void* stream) {
@@ -400,21 +431,21 @@ od_status od_space_attn_bwd_static_ws(const void* q, const void* k, const void* 
   od_status st = static_ws_pointer(&ws);
   if (st != OD_OK) return st;
   // the scratch is written completely before it is read, so nothing needs clearing
-  return launch_bwd(0, q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
-                    Hkv, D, agent_idx, 1, scale, ws, OD_STATIC_WORKSPACE_BYTES, stream);
+  return launch_bwd(0, q, k, v, o, o_lo, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S,
+                    Hq, Hkv, D, agent_idx, 1, scale, ws, OD_STATIC_WORKSPACE_BYTES, stream);
 }
 
 
 od_status od_space_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
-                            float scale, void* stream) {
-  return launch_fwd(0, q, k, v, o, lse, B, T, S, Hq, Hkv, D, agent_idx, 1, scale, stream);
+                            void* o_lo, int B, int T, int S, int Hq, int Hkv, int D,
+                            int agent_idx, float scale, void* stream) {
+  return launch_fwd(0, q, k, v, o, lse, o_lo, B, T, S, Hq, Hkv, D, agent_idx, 1, scale, stream);
 }
 
 od_status od_time_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                           int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
-                           void* stream) {
-  return launch_fwd(1, q, k, v, o, lse, B, T, S, Hq, Hkv, D, -1, window, scale, stream);
+                           void* o_lo, int B, int T, int S, int Hq, int Hkv, int D, int window,
+                           float scale, void* stream) {
+  return launch_fwd(1, q, k, v, o, lse, o_lo, B, T, S, Hq, Hkv, D, -1, window, scale, stream);
 }
 
 size_t od_attn_bwd_workspace_bytes(int which, int B, int T, int S, int Hq, int Hkv, int D) {
@@ -423,20 +454,20 @@ size_t od_attn_bwd_workspace_bytes(int which, int B, int T, int S, int Hq, int H
 }
 
 od_status od_space_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                            float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S,
-                            int Hq, int Hkv, int D, int agent_idx, float scale, void* workspace,
-                            size_t workspace_bytes, void* stream) {
-  return launch_bwd(0, q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
+                            const void* o_lo, const float* lse, const void* dout, void* dq,
+                            void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return launch_bwd(0, q, k, v, o, o_lo, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
                     Hkv, D, agent_idx, 1, scale, workspace, workspace_bytes, stream);
 }
 
 od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                           float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S,
-                           int Hq, int Hkv, int D, int window, float scale, void* workspace,
-                           size_t workspace_bytes, void* stream) {
-  return launch_bwd(1, q, k, v, o, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
+                           const void* o_lo, const float* lse, const void* dout, void* dq,
+                           void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                           int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  return launch_bwd(1, q, k, v, o, o_lo, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
                     Hkv, D, -1, window, scale, workspace, workspace_bytes, stream);
 }
 
@@ -463,18 +494,19 @@ static od_status packed_views(const void* qkv, int B, int T, int S, int Hq, int 
   return OD_OK;
 }
 
-static od_status fwd_packed(int is_time, const void* qkv, void* o, float* lse, int B, int T, int S,
-                            int Hq, int Hkv, int D, int agent, int window, float scale,
-                            void* stream) {
+static od_status fwd_packed(int is_time, const void* qkv, void* o, float* lse, void* o_lo, int B,
+                            int T, int S, int Hq, int Hkv, int D, int agent, int window,
+                            float scale, void* stream) {
   const void *q, *k, *v;
   int rows = 0;
   od_status st = packed_views(qkv, B, T, S, Hq, Hkv, D, &q, &k, &v, &rows);
   if (st != OD_OK) return st;
-  return launch_fwd(is_time, q, k, v, o, lse, B, T, S, Hq, Hkv, D, agent, window, scale, stream,
-                    rows);
+  return launch_fwd(is_time, q, k, v, o, lse, o_lo, B, T, S, Hq, Hkv, D, agent, window, scale,
+                    stream, rows);
 }
 
-static od_status bwd_packed(int is_time, const void* qkv, const void* o, const float* lse,
+static od_status bwd_packed(int is_time, const void* qkv, const void* o, const void* o_lo,
+                            const float* lse,
                             const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
                             float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D, int agent,
                             int window, float scale, void* workspace, size_t workspace_bytes,
@@ -490,37 +522,40 @@ static od_status bwd_packed(int is_time, const void* qkv, const void* o, const f
     if (a0 < b0 + n && b0 < a0 + n) return OD_ERR_INVALID_ARG;
   }
   if ((st = packed_views(dqkv, B, T, S, Hq, Hkv, D, &dq, &dk, &dv, &rows)) != OD_OK) return st;
-  return launch_bwd(is_time, q, k, v, o, lse, dout, const_cast<void*>(dq), const_cast<void*>(dk),
+  return launch_bwd(is_time, q, k, v, o, o_lo, lse, dout, const_cast<void*>(dq), const_cast<void*>(dk),
                     const_cast<void*>(dv), dq_f32, dk_f32, dv_f32, B, T, S, Hq, Hkv, D, agent,
                     window, scale, workspace, workspace_bytes, stream, rows);
 }
 
-od_status od_space_attn_fwd_packed(const void* qkv, void* o, float* lse, int B, int T, int S,
-                                   int Hq, int Hkv, int D, int agent_idx, float scale,
+od_status od_space_attn_fwd_packed(const void* qkv, void* o, float* lse, void* o_lo, int B, int T,
+                                   int S, int Hq, int Hkv, int D, int agent_idx, float scale,
                                    void* stream) {
-  return fwd_packed(0, qkv, o, lse, B, T, S, Hq, Hkv, D, agent_idx, 1, scale, stream);
+  return fwd_packed(0, qkv, o, lse, o_lo, B, T, S, Hq, Hkv, D, agent_idx, 1, scale, stream);
 }
 
-od_status od_time_attn_fwd_packed(const void* qkv, void* o, float* lse, int B, int T, int S,
-                                  int Hq, int Hkv, int D, int window, float scale, void* stream) {
-  return fwd_packed(1, qkv, o, lse, B, T, S, Hq, Hkv, D, -1, window, scale, stream);
+od_status od_time_attn_fwd_packed(const void* qkv, void* o, float* lse, void* o_lo, int B, int T,
+                                  int S, int Hq, int Hkv, int D, int window, float scale,
+                                  void* stream) {
+  return fwd_packed(1, qkv, o, lse, o_lo, B, T, S, Hq, Hkv, D, -1, window, scale, stream);
 }
 
-od_status od_space_attn_bwd_packed(const void* qkv, const void* o, const float* lse,
+od_status od_space_attn_bwd_packed(const void* qkv, const void* o, const void* o_lo,
+                                   const float* lse,
                                    const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
                                    float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D,
                                    int agent_idx, float scale, void* workspace,
                                    size_t workspace_bytes, void* stream) {
-  return bwd_packed(0, qkv, o, lse, dout, dqkv, dq_f32, dk_f32, dv_f32, B, T, S, Hq, Hkv, D,
+  return bwd_packed(0, qkv, o, o_lo, lse, dout, dqkv, dq_f32, dk_f32, dv_f32, B, T, S, Hq, Hkv, D,
                     agent_idx, 1, scale, workspace, workspace_bytes, stream);
 }
 
-od_status od_time_attn_bwd_packed(const void* qkv, const void* o, const float* lse,
+od_status od_time_attn_bwd_packed(const void* qkv, const void* o, const void* o_lo,
+                                  const float* lse,
                                   const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
                                   float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D,
                                   int window, float scale, void* workspace,
                                   size_t workspace_bytes, void* stream) {
-  return bwd_packed(1, qkv, o, lse, dout, dqkv, dq_f32, dk_f32, dv_f32, B, T, S, Hq, Hkv, D, -1,
+  return bwd_packed(1, qkv, o, o_lo, lse, dout, dqkv, dq_f32, dk_f32, dv_f32, B, T, S, Hq, Hkv, D, -1,
                     window, scale, workspace, workspace_bytes, stream);
 }
 

@@ -7,9 +7,11 @@
 // dV_j += P_j dO  (dK, dV summed over the G query heads of a KV head).
 //
 // Three launches, no atomics, no zeroed workspace (results are deterministic):
-//   1. od_bwd_dq_kernel<true>: Delta = sum_j P_j dP_j per row in fp32 into the caller's
-//        workspace.  It equals <dO, O> for the exact O; the bf16 O passed in would give
-//        Delta only to ~1e-2 absolute, which the gradients inherit.
+//   1. Delta per row in fp32 into the caller's workspace, and the operand ranges.  Given O's
+//        rounding residual O_lo from the forward: od_bwd_delta_o_kernel, Delta = <dO, O + O_lo>
+//        streamed from memory.  Otherwise od_bwd_dq_kernel<true>, Delta = sum_j P_j dP_j
+//        (equal to <dO, O> for the exact O; the bf16 O alone would give Delta only to ~1e-2
+//        absolute, which the gradients inherit).
 //   2. od_bwd_dq_kernel<false>: Q-tile stationary (the forward's work items and warp roles):
 //        S = Q K^T and dP = dO V^T per 96-key block in TMEM; dS written in place over S as
 //        fp16 times 2^eds; dQ += dS K into one fp32 accumulator, written once per tile.  Q
@@ -37,7 +39,7 @@ constexpr int kKVTile = kBN * 128;  // bytes of one K or V stage
 // The dK/dV products run on fp16 operands scaled by powers of two: every bf16 input value
 // is exactly representable in fp16 once the tensor's largest magnitude is brought just
 // below 2^15 (only values 2^25 times smaller than that largest one lose bits as fp16
-// subnormals), and power-of-two scales cancel exactly after accumulation.  The Delta pass
+// subnormals), and power-of-two scales cancel exactly after accumulation.  The first kernel
 // records max|Q|, max|K|, max|V|, max|dO| per CTA (kAmaxSlots slots of 4 floats after the
 // Delta array in the workspace); the dK/dV kernel reduces the slots and derives the scales.
 constexpr int kAmaxSlots = 1024;
@@ -1274,6 +1276,141 @@ inline cudaError_t bwd_setup() {
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
+}
+
+// ============================================================================ Delta from O
+// When the forward also wrote O's rounding residual O_lo (O ~ o + o_lo to about 16 significant
+// bits), Delta = <dO, O> is a row-wise dot product of tensors in HBM and needs no recompute of
+// P and dP: this streaming kernel replaces the Delta pass.  It also records the operand
+// ranges max|Q|, max|K|, max|V|, max|dO| per CTA, in the slots the Delta pass would fill.
+// One warp takes 4 query rows at a time (8 lanes x 16 bytes per 128-byte row); every byte of
+// dO, O, O_lo, Q, K and V is read once.
+constexpr int kDeltaOThreads = 256;
+
+struct DeltaOParams {
+  const __nv_bfloat16* o;       // [rows, 64] contiguous
+  const __nv_bfloat16* o_lo;    // [rows, 64] contiguous
+  const __nv_bfloat16* dout;    // [rows, 64] contiguous
+  const __nv_bfloat16* q;       // views: token i starts at row i * q_rows (or kv_rows)
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  long long ntok;               // B * T * S
+  int Hq, Hkv, q_rows, kv_rows;
+  float* delta;                 // [rows]
+  float* amax;                  // 4 floats per CTA
+};
+
+__device__ __forceinline__ float bf16x2_dot3(uint32_t d, uint32_t o, uint32_t l, float acc) {
+  const float d0 = __uint_as_float(d << 16), d1 = __uint_as_float(d & 0xFFFF0000u);
+  const float o0 = __uint_as_float(o << 16) + __uint_as_float(l << 16);
+  const float o1 = __uint_as_float(o & 0xFFFF0000u) + __uint_as_float(l & 0xFFFF0000u);
+  return fmaf(d1, o1, fmaf(d0, o0, acc));
+}
+
+__global__ void __launch_bounds__(kDeltaOThreads)
+    od_bwd_delta_o_kernel(const DeltaOParams p) {
+  __shared__ float red[kDeltaOThreads / 32][4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long gw = static_cast<long long>(blockIdx.x) * (kDeltaOThreads / 32) + warp;
+  const long long nw = static_cast<long long>(gridDim.x) * (kDeltaOThreads / 32);
+  const int sub = lane >> 3, ch = lane & 7;
+  uint32_t mq = 0, mk = 0, mv = 0, md = 0;
+
+  // Delta: groups of 4 rows, four groups in flight per warp
+  const long long nrows = p.ntok * p.Hq;
+  const long long ngroups = (nrows + 3) >> 2;
+  const uint4* D4 = reinterpret_cast<const uint4*>(p.dout);
+  const uint4* O4 = reinterpret_cast<const uint4*>(p.o);
+  const uint4* L4 = reinterpret_cast<const uint4*>(p.o_lo);
+  for (long long g0 = gw; g0 < ngroups; g0 += 4 * nw) {
+    uint4 d[4], o[4], l[4];
+    long long r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      r[u] = 4 * (g0 + u * nw) + sub;
+      if (g0 + u * nw < ngroups && r[u] < nrows) {
+        d[u] = __ldg(D4 + r[u] * 8 + ch);
+        o[u] = __ldg(O4 + r[u] * 8 + ch);
+        l[u] = __ldg(L4 + r[u] * 8 + ch);
+      } else {
+        d[u] = o[u] = l[u] = make_uint4(0, 0, 0, 0);
+        r[u] = -1;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      md = __vmaxu2(md, d[u].x & 0x7FFF7FFFu);
+      md = __vmaxu2(md, d[u].y & 0x7FFF7FFFu);
+      md = __vmaxu2(md, d[u].z & 0x7FFF7FFFu);
+      md = __vmaxu2(md, d[u].w & 0x7FFF7FFFu);
+      float acc = bf16x2_dot3(d[u].x, o[u].x, l[u].x, 0.f);
+      acc = bf16x2_dot3(d[u].y, o[u].y, l[u].y, acc);
+      acc = bf16x2_dot3(d[u].z, o[u].z, l[u].z, acc);
+      acc = bf16x2_dot3(d[u].w, o[u].w, l[u].w, acc);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      if (ch == 0 && r[u] >= 0) p.delta[r[u]] = acc;
+    }
+  }
+
+  // operand ranges of Q, K, V.  A contiguous tensor is one flat array (four 16-byte loads in
+  // flight per thread); a packed view is walked token by token (the token's head rows are
+  // contiguous), again four loads in flight per lane.
+  auto vmax4 = [](uint32_t m, const uint4& x) {
+    m = __vmaxu2(m, x.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, x.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, x.z & 0x7FFF7FFFu);
+    return __vmaxu2(m, x.w & 0x7FFF7FFFu);
+  };
+  auto scan = [&](const __nv_bfloat16* base, int rows_per_tok, int heads, uint32_t m) {
+    const uint4* src = reinterpret_cast<const uint4*>(base);
+    if (rows_per_tok == heads) {
+      const long long n = p.ntok * heads * 8;
+      const long long nt = static_cast<long long>(gridDim.x) * kDeltaOThreads;
+      const long long t0 = static_cast<long long>(blockIdx.x) * kDeltaOThreads + threadIdx.x;
+      for (long long c = t0; c < n; c += 4 * nt) {
+        uint4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          x[u] = (c + u * nt < n) ? __ldg(src + c + u * nt) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) m = vmax4(m, x[u]);
+      }
+    } else {
+      const int nchunk = heads * 8;
+      for (long long t = gw; t < p.ntok; t += nw) {
+        const uint4* row = src + t * rows_per_tok * 8;
+        for (int c = lane; c < nchunk; c += 128) {
+          uint4 x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            x[u] = (c + 32 * u < nchunk) ? __ldg(row + c + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) m = vmax4(m, x[u]);
+        }
+      }
+    }
+    return m;
+  };
+  mq = scan(p.q, p.q_rows, p.Hq, mq);
+  mk = scan(p.k, p.kv_rows, p.Hkv, mk);
+  mv = scan(p.v, p.kv_rows, p.Hkv, mv);
+
+  const float a[4] = {amax_reduce(mq), amax_reduce(mk), amax_reduce(mv), amax_reduce(md)};
+  if (lane == 0)
+    for (int c = 0; c < 4; ++c) red[warp][c] = a[c];
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    float m = 0.f;
+    bool nan = false;
+    for (int w = 0; w < kDeltaOThreads / 32; ++w) {
+      const float x = red[w][threadIdx.x];
+      nan |= !(x == x);
+      m = fmaxf(m, x);
+    }
+    p.amax[4 * blockIdx.x + threadIdx.x] = nan ? __int_as_float(0x7fc00000) : m;
+  }
 }
 
 // workspace: Delta (fp32, one per query row), then kAmaxSlots x 4 fp32 operand ranges

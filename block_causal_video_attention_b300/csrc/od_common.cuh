@@ -53,6 +53,7 @@ struct FwdParams {
   // d >= 2^16, where the plain division is used)
   unsigned long long rcp_npairs, rcp_hkv, rcp_f;
   __nv_bfloat16* o;
+  __nv_bfloat16* o_lo;   // optional: O - bf16(O), rounded to bf16 (for the backward's Delta)
   float* lse;
   unsigned int* status;
 };

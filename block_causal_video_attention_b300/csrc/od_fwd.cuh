@@ -597,10 +597,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             (M + log2f(lsum)) * 0.69314718055994531f;
       }
       // This half writes output columns [32 hf, 32 hf + 32): each warp stages its 32 rows
-      // (64 bytes each, 16-byte chunks XOR-swizzled by row) and stores them coalesced.
+      // (64 bytes each, 16-byte chunks XOR-swizzled by row) and stores them coalesced.  When
+      // requested, the residual O - bf16(O) (rounded to bf16) follows through the same
+      // staging buffer; it is kept in registers meanwhile.
       uint8_t* stg = sOst + warp * 2048;
       const uint32_t tOa = tX + 128u + 32u * hf, tOb = tOa + 64u;
-#pragma unroll 1
+      uint32_t wl[2][8];
+#pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         float oa[16], ob[16];
         tmem_ld16(tOa + 16 * c2, oa);
@@ -612,7 +615,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int j = 0; j < 8; ++j) {
           const float2 y = __ffma2_rn(make_float2(oa[2 * j], oa[2 * j + 1]), make_float2(wa, wa),
                                       __fmul2_rn(make_float2(ob[2 * j], ob[2 * j + 1]), make_float2(wb, wb)));
-          w[j] = pack_bf16x2(y.x, y.y);
+          w[j] = split_bf16x2(y.x, y.y, &wl[c2][j]);
         }
         *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * c2) ^ (lane & 3)) << 4)) =
             make_uint4(w[0], w[1], w[2], w[3]);
@@ -621,7 +624,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       __syncwarp();
       OD_TP(34, (int)i, 0);
-      {
+      const int nparts = p.o_lo ? 2 : 1;
+#pragma unroll 1
+      for (int part = 0; part < nparts; ++part) {
+        if (part) {
+          // the residual into the staging buffer (the O rows have been stored)
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * c2) ^ (lane & 3)) << 4)) =
+                make_uint4(wl[c2][0], wl[c2][1], wl[c2][2], wl[c2][3]);
+            *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * c2 + 1) ^ (lane & 3)) << 4)) =
+                make_uint4(wl[c2][4], wl[c2][5], wl[c2][6], wl[c2][7]);
+          }
+          __syncwarp();
+        }
+        __nv_bfloat16* dst = part ? p.o_lo : p.o;
         const int sub = lane >> 2, ch = lane & 3;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -636,11 +653,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const long long row =
                 ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + gg;
             const uint4 wv = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((ch ^ (rr & 3)) << 4));
-            reinterpret_cast<uint4*>(p.o + row * 64 + 32 * hf)[ch] = wv;
+            reinterpret_cast<uint4*>(dst + row * 64 + 32 * hf)[ch] = wv;
           }
         }
+        __syncwarp();
       }
-      __syncwarp();
       OD_TP(31, (int)i, 0);
     }
   }

@@ -64,35 +64,44 @@ typedef enum {
   OD_ERR_WORKSPACE = 5
 } od_status;
 
-/* Space attention forward.  Writes O [B,T,S,Hq,D] (bf16) and LSE [B,T,S,Hq] (fp32). */
+/* Space attention forward.  Writes O [B,T,S,Hq,D] (bf16) and LSE [B,T,S,Hq] (fp32).
+ * o_lo (optional, may be NULL): if given, also receives O's rounding residual, [B,T,S,Hq,D]
+ * bf16: o_lo = bf16(O - o) with O the fp32 result, so o + o_lo holds O to about 16
+ * significant bits.  Passing it on to the backward lets the backward take Delta = <dO, O>
+ * from memory instead of recomputing P and dP for it (a faster backward). */
 od_status od_space_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
-                            float scale, void* stream);
+                            void* o_lo, int B, int T, int S, int Hq, int Hkv, int D,
+                            int agent_idx, float scale, void* stream);
 
-/* Time attention forward (window >= 1; keys t-window+1 .. t).  Writes O and LSE. */
+/* Time attention forward (window >= 1; keys t-window+1 .. t).  Writes O and LSE (and o_lo,
+ * as for the space forward). */
 od_status od_time_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                           int B, int T, int S, int Hq, int Hkv, int D, int window,
+                           void* o_lo, int B, int T, int S, int Hq, int Hkv, int D, int window,
                            float scale, void* stream);
 
-/* Space attention backward.  Inputs: Q, K, V, the forward's O and LSE, and dO.  Outputs
- * dQ [B,T,S,Hq,D], dK and dV [B,T,S,Hkv,D] in bf16 (overwritten).  `workspace` is
+/* Space attention backward.  Inputs: Q, K, V, the forward's O, o_lo and LSE, and dO.  Outputs
+ * dQ [B,T,S,Hq,D], dK and dV [B,T,S,Hkv,D] in bf16 (overwritten).
+ * o_lo may be NULL: Delta = <dO, O> per query row is then recomputed from P and dP (an extra
+ * pass over Q, K, V, dO with two matrix products), because bf16 O alone does not give Delta
+ * to the accuracy the gradients need; O is not read in that case.  With o_lo (the residual
+ * the forward wrote), Delta is the row-wise dot product of dO with o + o_lo, read from memory.  `workspace` is
  * caller-owned device scratch of at least od_attn_bwd_workspace_bytes(0, ...) bytes
  * (Delta per query row in fp32, rounded up to 256 bytes, then 16 KiB of per-CTA operand
  * ranges); its contents on entry do not matter.
  * If dq_f32/dk_f32/dv_f32 are non-NULL, the gradients are also written there in fp32
  * (same layouts), before rounding to bf16. */
 od_status od_space_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                            float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S,
-                            int Hq, int Hkv, int D, int agent_idx, float scale,
-                            void* workspace, size_t workspace_bytes, void* stream);
+                            const void* o_lo, const float* lse, const void* dout, void* dq,
+                            void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                            float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Time attention backward; as od_space_attn_bwd with `window` in place of agent_idx. */
 od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                           float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S,
-                           int Hq, int Hkv, int D, int window, float scale, void* workspace,
-                           size_t workspace_bytes, void* stream);
+                           const void* o_lo, const float* lse, const void* dout, void* dq,
+                           void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                           int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* Packed-QKV forms.  Each layer of the block-causal backbone alternates space and time
  * attention (7minutos.es page, section "Arquitectura: una columna vertebral, dos modelos"),
@@ -104,17 +113,20 @@ od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const vo
  * (heads in the same order), which must not be `qkv` (it may not overlap it at all).  The
  * optional fp32 gradient copies (dq_f32 ...) stay contiguous [B,T,S,H,D].  Errors as for the
  * unpacked calls. */
-od_status od_space_attn_fwd_packed(const void* qkv, void* o, float* lse, int B, int T, int S,
-                                   int Hq, int Hkv, int D, int agent_idx, float scale,
+od_status od_space_attn_fwd_packed(const void* qkv, void* o, float* lse, void* o_lo, int B, int T,
+                                   int S, int Hq, int Hkv, int D, int agent_idx, float scale,
                                    void* stream);
-od_status od_time_attn_fwd_packed(const void* qkv, void* o, float* lse, int B, int T, int S,
-                                  int Hq, int Hkv, int D, int window, float scale, void* stream);
-od_status od_space_attn_bwd_packed(const void* qkv, const void* o, const float* lse,
+od_status od_time_attn_fwd_packed(const void* qkv, void* o, float* lse, void* o_lo, int B, int T,
+                                  int S, int Hq, int Hkv, int D, int window, float scale,
+                                  void* stream);
+od_status od_space_attn_bwd_packed(const void* qkv, const void* o, const void* o_lo,
+                                   const float* lse,
                                    const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
                                    float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D,
                                    int agent_idx, float scale, void* workspace,
                                    size_t workspace_bytes, void* stream);
-od_status od_time_attn_bwd_packed(const void* qkv, const void* o, const float* lse,
+od_status od_time_attn_bwd_packed(const void* qkv, const void* o, const void* o_lo,
+                                  const float* lse,
                                   const void* dout, void* dqkv, float* dq_f32, float* dk_f32,
                                   float* dv_f32, int B, int T, int S, int Hq, int Hkv, int D,
                                   int window, float scale, void* workspace,
@@ -161,7 +173,7 @@ od_status od_time_attn_decode(const void* q, const void* k_new, const void* v_ne
  * and must be serialised by the caller.  The scratch is fully rewritten by each call before
  * it is read, so no clearing is needed. */
 od_status od_space_attn_bwd_static_ws(const void* q, const void* k, const void* v, const void* o,
-                                      const float* lse, const void* dout, void* dq, void* dk,
+                                      const void* o_lo, const float* lse, const void* dout, void* dq, void* dk,
                                       void* dv, float* dq_f32, float* dk_f32, float* dv_f32, int B,
                                       int T, int S, int Hq, int Hkv, int D, int agent_idx,
                                       float scale, void* stream);

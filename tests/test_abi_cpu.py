@@ -48,10 +48,11 @@ def test_forward_rejects_invalid_arguments(lib, fn):
     def call(ptrs=None, **kw):
         a = dict(base, **kw)
         q, k, v, o, l = ptrs or (GOOD, GOOD, GOOD, GOOD, GOOD)
-        return f(q, k, v, o, l, a["B"], a["T"], a["S"], a["Hq"], a["Hkv"], a["D"], a["extra"],
+        return f(q, k, v, o, l, a.get("o_lo", P(0)), a["B"], a["T"], a["S"], a["Hq"], a["Hkv"], a["D"], a["extra"],
                  a["scale"], P(0))
     assert call(ptrs=(P(0), GOOD, GOOD, GOOD, GOOD)) == 1
     assert call(ptrs=(GOOD, GOOD, GOOD, P(4097), GOOD)) == 1      # misaligned
+    assert call(o_lo=P(4100)) == 1                                  # misaligned residual
     assert call(B=0) == 1
     assert call(S=-3) == 1
     assert call(Hq=5, Hkv=2) == 1                                  # Hq % Hkv
@@ -69,14 +70,17 @@ def test_forward_rejects_invalid_arguments(lib, fn):
 def test_backward_rejects_invalid_arguments(lib, fn):
     f = getattr(lib, fn)
     extra = 0 if fn == "od_space_attn_bwd" else 4
-    ptrs = [GOOD] * 9 + [P(0)] * 3
+    ptrs = [GOOD] * 4 + [P(0)] + [GOOD] * 5 + [P(0)] * 3   # q k v o (no o_lo) lse dO dq dk dv
     ws = lib.od_attn_bwd_workspace_bytes(0 if "space" in fn else 1, 1, 4, 8, 4, 2, 64)
     assert ws > 0
     assert f(*ptrs, 1, 4, 8, 4, 2, 64, extra, 0.125, GOOD, ws - 16, P(0)) == 5  # too small
     bad = list(ptrs)
-    bad[5] = P(0)                                                   # null dO
+    bad[6] = P(0)                                                   # null dO
     assert f(*bad, 1, 4, 8, 4, 2, 64, extra, 0.125, GOOD, ws, P(0)) == 1
     assert f(*ptrs, 1, 4, 8, 4, 3, 64, extra, 0.125, GOOD, ws, P(0)) == 1           # Hq % Hkv
+    bad = list(ptrs)
+    bad[4] = P(4104)                                                # misaligned o_lo
+    assert f(*bad, 1, 4, 8, 4, 2, 64, extra, 0.125, GOOD, ws, P(0)) == 1
     assert lib.od_attn_bwd_workspace_bytes(2, 1, 4, 8, 4, 2, 64) == 0
     # Delta (fp32 per query row, 256-byte rounded) + 1024 slots x 4 fp32 operand ranges
     for dims in ((1, 4, 8, 4), (2, 7, 33, 12), (1, 256, 290, 30)):
@@ -111,15 +115,16 @@ def test_decode_rejects_invalid_arguments(lib):
 
 def test_packed_calls_reject_invalid_arguments(lib):
     f = lib.od_space_attn_fwd_packed
-    assert f(P(0), GOOD, GOOD, 1, 4, 8, 4, 2, 64, 0, 0.125, P(0)) == 1          # null qkv
-    assert f(GOOD, GOOD, GOOD, 1, 4, 8, 4, 2, 32, 0, 0.125, P(0)) == 2          # D != 64
-    assert f(GOOD, GOOD, GOOD, 1, 4, 8, 5, 2, 64, 0, 0.125, P(0)) == 1          # Hq % Hkv
-    assert lib.od_time_attn_fwd_packed(GOOD, GOOD, GOOD, 1, 4, 8, 4, 2, 64, 0, 0.125, P(0)) == 1
+    assert f(P(0), GOOD, GOOD, P(0), 1, 4, 8, 4, 2, 64, 0, 0.125, P(0)) == 1    # null qkv
+    assert f(GOOD, GOOD, GOOD, P(0), 1, 4, 8, 4, 2, 32, 0, 0.125, P(0)) == 2    # D != 64
+    assert f(GOOD, GOOD, GOOD, P(0), 1, 4, 8, 5, 2, 64, 0, 0.125, P(0)) == 1    # Hq % Hkv
+    assert lib.od_time_attn_fwd_packed(GOOD, GOOD, GOOD, P(0), 1, 4, 8, 4, 2, 64, 0, 0.125,
+                                       P(0)) == 1
     b = lib.od_space_attn_bwd_packed
     ws = lib.od_attn_bwd_workspace_bytes(0, 1, 4, 8, 4, 2, 64)
     n = 1 * 4 * 8 * (4 + 2 * 2) * 64 * 2          # bytes of one packed tensor
-    args = lambda qkv, dqkv: (qkv, GOOD, GOOD, GOOD, dqkv, P(0), P(0), P(0), 1, 4, 8, 4, 2, 64, 0,
-                              0.125, GOOD, ws, P(0))
+    args = lambda qkv, dqkv: (qkv, GOOD, P(0), GOOD, GOOD, dqkv, P(0), P(0), P(0), 1, 4, 8, 4, 2,
+                              64, 0, 0.125, GOOD, ws, P(0))
     assert b(*args(P(1 << 20), P(0))) == 1                                      # null dqkv
     assert b(*args(P(1 << 20), P((1 << 20) + n - 16))) == 1                     # overlapping
     assert b(*args(P((1 << 20) + n - 16), P(1 << 20))) == 1

@@ -15,17 +15,23 @@ from helpers import assert_close, inputs, to_dev, to_f64
 pytestmark = pytest.mark.gpu
 
 
-def run_bwd(oracle_mod, kind, bits, extra, scale=0.125):
+def run_bwd(oracle_mod, kind, bits, extra, scale=0.125, with_lo=False):
+    """with_lo: the forward also writes O's residual and the backward takes Delta from
+    O + O_lo (instead of recomputing it from P and dP)."""
     q, k, v, do = bits
     Q, K, V, DO = to_dev(q), to_dev(k), to_dev(v), to_dev(do)
     X = oracle_mod.from_bf16
+    fwd = api.space_attn_fwd if kind == "space" else api.time_attn_fwd
+    bwd = api.space_attn_bwd if kind == "space" else api.time_attn_bwd
+    lo = None
+    if with_lo:
+        o, l, lo = fwd(Q, K, V, extra, scale, o_lo=True)
+    else:
+        o, l = fwd(Q, K, V, extra, scale)
+    dq, dk, dv, (fq, fk, fv) = bwd(Q, K, V, o, l, DO, extra, scale, fp32_grads=True, o_lo=lo)
     if kind == "space":
-        o, l = api.space_attn_fwd(Q, K, V, extra, scale)
-        dq, dk, dv, (fq, fk, fv) = api.space_attn_bwd(Q, K, V, o, l, DO, extra, scale, fp32_grads=True)
         ref = oracle_mod.space_bwd(X(q), X(k), X(v), X(do), extra, scale)
     else:
-        o, l = api.time_attn_fwd(Q, K, V, extra, scale)
-        dq, dk, dv, (fq, fk, fv) = api.time_attn_bwd(Q, K, V, o, l, DO, extra, scale, fp32_grads=True)
         ref = oracle_mod.time_bwd(X(q), X(k), X(v), X(do), extra, scale)
     torch.cuda.synchronize()
     st, site = api.get_device_status_detail()
@@ -33,8 +39,9 @@ def run_bwd(oracle_mod, kind, bits, extra, scale=0.125):
     return (to_f64(dq), to_f64(dk), to_f64(dv)), (to_f64(fq), to_f64(fk), to_f64(fv)), ref[2:]
 
 
-def check_bwd(oracle_mod, kind, bits, extra, scale=0.125, what=""):
-    bf, f32, ref = run_bwd(oracle_mod, kind, bits, extra, scale)
+def check_bwd(oracle_mod, kind, bits, extra, scale=0.125, what="", with_lo=False):
+    bf, f32, ref = run_bwd(oracle_mod, kind, bits, extra, scale, with_lo)
+    what = "%s%s" % (what, " (Delta from O + O_lo)" if with_lo else "")
     for name, g, gb, r in zip(("dQ", "dK", "dV"), f32, bf, ref):
         assert_close(g, r, "%s %s %s fp32" % (what, kind, name), bf16_out=False)
         assert_close(gb, r, "%s %s %s bf16" % (what, kind, name), mean_rel=3e-3)
@@ -61,11 +68,12 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("with_lo", [False, True])
 @pytest.mark.parametrize("B,T,S,Hq,Hkv,agent,window", SHAPES)
-def test_backward_shapes(oracle_mod, B, T, S, Hq, Hkv, agent, window):
+def test_backward_shapes(oracle_mod, B, T, S, Hq, Hkv, agent, window, with_lo):
     bits = inputs(B, T, S, Hq, Hkv, seed=7 * B + T + 3 * S, with_dout=True)
-    check_bwd(oracle_mod, "space", bits, agent, what=str((B, T, S, Hq, Hkv)))
-    check_bwd(oracle_mod, "time", bits, window, what=str((B, T, S, Hq, Hkv)))
+    check_bwd(oracle_mod, "space", bits, agent, what=str((B, T, S, Hq, Hkv)), with_lo=with_lo)
+    check_bwd(oracle_mod, "time", bits, window, what=str((B, T, S, Hq, Hkv)), with_lo=with_lo)
 
 
 def test_backward_gradient_invariants_on_gpu():

@@ -182,3 +182,29 @@ def test_v_outside_fp16_range_uses_bf16(oracle_mod, vscale):
     assert np.abs(go - ro).max() / sc <= 5e-2
     assert np.abs(go - ro).mean() / sc <= 3e-3
     assert np.abs(gl - rl).max() <= LSE_ERR
+
+
+@pytest.mark.parametrize("kind", ["space", "time"])
+def test_output_residual(oracle_mod, kind):
+    """o_lo = bf16(O - o): requesting it leaves O and LSE bit-identical, and o + o_lo holds the
+    kernel's fp32 O, much closer to the exact O than bf16 O alone."""
+    B, T, S, Hq, Hkv, agent, window = 1, 40, 290, 30, 3, 289, 24
+    bits = inputs(B, T, S, Hq, Hkv, seed=4242)
+    Q, K, V = (to_dev(x) for x in bits[:3])
+    fwd = api.space_attn_fwd if kind == "space" else api.time_attn_fwd
+    extra = agent if kind == "space" else window
+    o1, l1 = fwd(Q, K, V, extra, 0.125)
+    o2, l2, lo = fwd(Q, K, V, extra, 0.125, o_lo=True)
+    torch.cuda.synchronize()
+    assert api.get_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    X = oracle_mod.from_bf16
+    ro, _ = (oracle_mod.space_fwd if kind == "space" else oracle_mod.time_fwd)(
+        X(bits[0]), X(bits[1]), X(bits[2]), extra, 0.125)
+    hi, both = to_f64(o2), to_f64(o2) + to_f64(lo)
+    # the residual is below half a bf16 ulp of o
+    from helpers import bf16_ulp
+    assert (np.abs(to_f64(lo)) <= 0.5 * bf16_ulp(hi) + 1e-30).all()
+    e_hi = np.abs(hi - ro).mean() / np.abs(ro).mean()
+    e_both = np.abs(both - ro).mean() / np.abs(ro).mean()
+    assert e_both < 0.25 * e_hi and np.abs(both - ro).max() <= 2e-3, (e_hi, e_both)

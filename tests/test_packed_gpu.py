@@ -74,3 +74,26 @@ def test_packed_gradients_leave_the_inputs_untouched():
     assert torch.isfinite(dqkv.float()).all()   # every head range of every token was written
     with pytest.raises(api.ODError):
         api.space_attn_bwd_packed(qkv, 6, o, l, do, 29, out=qkv)
+
+
+def test_packed_with_output_residual_equals_unpacked():
+    """Delta from O + O_lo, with Q/K/V (and the operand-range scan) read through the packed
+    views: bit-identical to the separate tensors."""
+    B, T, S, Hq, Hkv, agent, window = 1, 12, 290, 30, 3, 289, 8
+    w = synth.custom(B, T, S, Hq, Hkv, window=window, agent=agent, seed=79)
+    q_b, k_b, v_b, do_b = synth.make_inputs(w, with_dout=True)
+    q, k, v, do = to_dev(q_b), to_dev(k_b), to_dev(v_b), to_dev(do_b)
+    qkv = pack(q, k, v)
+    for kind, extra in (("space", agent), ("time", window)):
+        fwd = api.space_attn_fwd if kind == "space" else api.time_attn_fwd
+        fwdp = api.space_attn_fwd_packed if kind == "space" else api.time_attn_fwd_packed
+        bwd = api.space_attn_bwd if kind == "space" else api.time_attn_bwd
+        bwdp = api.space_attn_bwd_packed if kind == "space" else api.time_attn_bwd_packed
+        o1, l1, r1 = fwd(q, k, v, extra, 0.125, o_lo=True)
+        o2, l2, r2 = fwdp(qkv, Hq, extra, 0.125, o_lo=True)
+        assert torch.equal(r1, r2)
+        g1 = bwd(q, k, v, o1, l1, do, extra, 0.125, o_lo=r1)
+        g2 = bwdp(qkv, Hq, o2, l2, do, extra, 0.125, o_lo=r2)
+        torch.cuda.synchronize()
+        assert api.get_device_status() == 0
+        assert torch.equal(pack(*g1), g2), kind

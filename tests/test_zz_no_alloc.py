@@ -33,7 +33,7 @@ def _static_ws_bwd(lib, Q, K, V, O, L, DO, agent, scale, stream):
     fv = torch.empty(V.shape, dtype=torch.float32, device=Q.device)
     B, T, S, Hq, D = Q.shape
     st = lib.od_space_attn_bwd_static_ws(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), _ptr(DO), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), P(0), _ptr(L), _ptr(DO), _ptr(dq), _ptr(dk), _ptr(dv),
         _ptr(fq), _ptr(fk), _ptr(fv), B, T, S, Hq, K.shape[3], D, agent, ctypes.c_float(scale),
         P(stream.cuda_stream))
     assert st == 0, api.STATUS.get(st, st)
@@ -65,7 +65,7 @@ def test_static_workspace_refuses_sizes_beyond_the_fixed_array():
     small = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
     B, T, S, Hq, Hkv = 1, 1024, 1024, 8, 8     # 8M query rows x 4 bytes > the fixed array
     assert B * T * S * Hq * 4 > 16 << 20
-    ptrs = [_ptr(small)] * 9 + [P(0)] * 3
+    ptrs = [_ptr(small)] * 4 + [P(0)] + [_ptr(small)] * 5 + [P(0)] * 3
     st = lib.od_space_attn_bwd_static_ws(*ptrs, B, T, S, Hq, Hkv, 64, -1, ctypes.c_float(0.125),
                                          P(torch.cuda.current_stream().cuda_stream))
     assert st == 5   # OD_ERR_WORKSPACE
