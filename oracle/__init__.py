@@ -141,6 +141,50 @@ def time_bwd(q, k, v, dout, window, scale=None, nthreads=0):
     return _bwd("oracle_time_bwd", q, k, v, dout, window, scale, nthreads)
 
 
+def _varlen_blocks(shape_q, seqlen):
+    B, T, S = shape_q[:3]
+    L = np.clip(np.asarray(seqlen, dtype=np.int64).reshape(B, T), 0, S)
+    return B, T, S, L
+
+
+def space_fwd_varlen(q, k, v, seqlen, agent=-1, scale=None, nthreads=0):
+    """Space attention over variable-length timestep blocks: block (b, t) holds its first
+    seqlen[b, t] tokens (clamped to [0, S]) and is plain space attention over them (the agent
+    rule applies when agent < seqlen).  Returns (O, LSE) with NaN in the padding rows."""
+    B, T, S, L = _varlen_blocks(np.shape(q), seqlen)
+    o = np.full(np.shape(q), np.nan)
+    lse = np.full(np.shape(q)[:4], np.nan)
+    for b in range(B):
+        for t in range(T):
+            n = int(L[b, t])
+            if n == 0:
+                continue
+            a = agent if 0 <= agent < n else -1
+            ob, lb = space_fwd(q[b:b + 1, t:t + 1, :n], k[b:b + 1, t:t + 1, :n],
+                               v[b:b + 1, t:t + 1, :n], a, scale, nthreads)
+            o[b, t, :n] = ob[0, 0]
+            lse[b, t, :n] = lb[0, 0]
+    return o, lse
+
+
+def space_bwd_varlen(q, k, v, dout, seqlen, agent=-1, scale=None, nthreads=0):
+    """Backward of space_fwd_varlen.  Returns (O, LSE, dQ, dK, dV), NaN in padding rows."""
+    B, T, S, L = _varlen_blocks(np.shape(q), seqlen)
+    out = [np.full(np.shape(q), np.nan), np.full(np.shape(q)[:4], np.nan),
+           np.full(np.shape(q), np.nan), np.full(np.shape(k), np.nan), np.full(np.shape(v), np.nan)]
+    for b in range(B):
+        for t in range(T):
+            n = int(L[b, t])
+            if n == 0:
+                continue
+            a = agent if 0 <= agent < n else -1
+            res = space_bwd(q[b:b + 1, t:t + 1, :n], k[b:b + 1, t:t + 1, :n],
+                            v[b:b + 1, t:t + 1, :n], dout[b:b + 1, t:t + 1, :n], a, scale, nthreads)
+            for dst, r in zip(out, res):
+                dst[b, t, :n] = r[0, 0]
+    return tuple(out)
+
+
 def time_decode(q, k_new, v_new, k_cache, v_cache, t, scale=None):
     """Decode step of time attention with a ring-buffer KV cache of W = k_cache.shape[1]
     frames: stores the new frame (absolute index t) in slot t mod W, then attends over frames

@@ -343,6 +343,74 @@ def test_backward_causal_and_agent_zero_gradients(oracle_mod):
 
 
 # ----------------------------------------------------------------------------
+# variable-length space attention
+# ----------------------------------------------------------------------------
+def test_varlen_space_attention_is_the_dense_rule_per_block(oracle_mod):
+    """Each block equals the independent dense-mask formulation over its first L tokens;
+    full lengths reproduce the fixed-length oracle bit for bit; padding tokens affect nothing."""
+    B, T, S, Hq, Hkv, D, a, sc = 2, 3, 11, 4, 2, 8, 3, 0.3
+    q, k, v = rnd((B, T, S, Hq, D), 80), rnd((B, T, S, Hkv, D), 81), rnd((B, T, S, Hkv, D), 82)
+    L = np.array([[11, 1, 4], [0, 7, 3]])
+    o, lse = oracle_mod.space_fwd_varlen(q, k, v, L, a, sc)
+    for b in range(B):
+        for t in range(T):
+            n = L[b, t]
+            assert np.isnan(o[b, t, n:]).all() and np.isnan(lse[b, t, n:]).all()
+            if n == 0:
+                continue
+            sl = (slice(b, b + 1), slice(t, t + 1), slice(0, n))
+            m = dense_mask(1, 1, n, Hq, Hkv, "space", a if a < n else -1)
+            O, LSE, _ = dense_attention(q[sl], k[sl], v[sl], m, sc)
+            np.testing.assert_allclose(o[b, t, :n], O[0, 0], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[b, t, :n], LSE[0, 0], rtol=0, atol=1e-12)
+    full = np.full((B, T), S)
+    o1, l1 = oracle_mod.space_fwd_varlen(q, k, v, full, a, sc)
+    o2, l2 = oracle_mod.space_fwd(q, k, v, a, sc)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    # padding tokens (past each block's length) change no valid output
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    for b in range(B):
+        for t in range(T):
+            n = L[b, t]
+            q2[b, t, n:] += 5.0
+            k2[b, t, n:] -= 3.0
+            v2[b, t, n:] *= 7.0
+    o3, l3 = oracle_mod.space_fwd_varlen(q2, k2, v2, L, a, sc)
+    np.testing.assert_array_equal(np.nan_to_num(o3, nan=9.0), np.nan_to_num(o, nan=9.0))
+    np.testing.assert_array_equal(np.nan_to_num(l3, nan=9.0), np.nan_to_num(lse, nan=9.0))
+    # a one-token block reads only itself
+    G = Hq // Hkv
+    np.testing.assert_array_equal(o[0, 1, 0], np.repeat(v[0, 1, 0], G, axis=0))
+
+
+def test_varlen_space_backward_matches_autograd_per_block(oracle_mod):
+    B, T, S, Hq, Hkv, D, a, sc = 1, 2, 9, 4, 2, 8, 8, 0.25
+    q, k, v = rnd((B, T, S, Hq, D), 83), rnd((B, T, S, Hkv, D), 84), rnd((B, T, S, Hkv, D), 85)
+    do = rnd((B, T, S, Hq, D), 86)
+    L = np.array([[9, 5]])
+    _, _, dq, dk, dv = oracle_mod.space_bwd_varlen(q, k, v, do, L, a, sc)
+    G = Hq // Hkv
+    for t in range(T):
+        n = L[0, t]
+        qt = torch.tensor(q[0, t, :n], requires_grad=True)
+        kt = torch.tensor(k[0, t, :n], requires_grad=True)
+        vt = torch.tensor(v[0, t, :n], requires_grad=True)
+        m = torch.ones(n, n, dtype=torch.bool)
+        if a < n:
+            m[:, a] = False
+            m[a, a] = True
+        kr, vr = kt.repeat_interleave(G, dim=1), vt.repeat_interleave(G, dim=1)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qt.transpose(0, 1), kr.transpose(0, 1), vr.transpose(0, 1), attn_mask=m, scale=sc)
+        o.backward(torch.tensor(do[0, t, :n]).transpose(0, 1))
+        np.testing.assert_allclose(dq[0, t, :n], qt.grad.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dk[0, t, :n], kt.grad.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv[0, t, :n], vt.grad.numpy(), rtol=0, atol=1e-12)
+        assert np.isnan(dq[0, t, n:]).all() and np.isnan(dk[0, t, n:]).all()
+
+
+# ----------------------------------------------------------------------------
 # decode step over a ring-buffer KV cache
 # ----------------------------------------------------------------------------
 def _rollout(oracle_mod, q, k, v, W, scale, fill=0.0):
