@@ -7,6 +7,7 @@ Metric: algorithmic TFLOP/s (allowed query-key pairs only; a backward counts 2.5
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --workload minecraft_decode     # the rollout decode step (GB/s)
+    python bench.py --workload tokenizer_enc --varlen   # space attention, dropped MAE patches
 
 --impl reference times the fp64 CPU oracle (the only reference this project has) on a
 bounded sample of the same workload.  Under torchrun each rank runs an independent replica
@@ -476,6 +477,179 @@ def run_ours(args, w, with_bwd):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- varlen space
+VARLEN_METRIC = ("variable-length space attention TFLOP/s (fwd+bwd, tokenizer encoder with "
+                 "dropped MAE patches) and % of B300 bf16 roofline")
+
+
+def varlen_space_flops(w, L):
+    """Algorithmic FLOPs of one varlen space fwd and bwd: 4*D per allowed pair per head."""
+    L = np.asarray(L, dtype=np.float64)
+    pairs = L * L
+    if w.agent >= 0:
+        pairs = pairs - np.where(w.agent < L, L - 1, 0)
+    fwd = 4.0 * w.D * w.Hq * float(pairs.sum())
+    return fwd, 2.5 * fwd
+
+
+def run_varlen(args, w):
+    """Space attention forward + backward over timestep blocks of seeded MAE lengths (the
+    padded [B,T,S,H,D] layout), timed next to the same calls with every block full."""
+    import torch
+    from block_causal_video_attention_b300 import api
+
+    rank, world, local = dist_info()
+    lengths = synth.mae_block_lengths(w.B, w.T, w.seed + 100)
+    fl_f, fl_b = varlen_space_flops(w, lengths)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        q, k, v, dout = synth.make_inputs(w, with_dout=True)
+        X = oracle.from_bf16
+        vals = []
+        for i in range(args.steps):
+            b, t = i % w.B, (i // w.B) % w.T   # one whole block per step
+            sl = (slice(b, b + 1), slice(t, t + 1))
+            t0 = time.perf_counter()
+            oracle.space_bwd_varlen(X(q[sl]), X(k[sl]), X(v[sl]), X(dout[sl]),
+                                    lengths[b:b + 1, t:t + 1], w.agent, w.scale)
+            s = time.perf_counter() - t0
+            f, bb = varlen_space_flops(w, lengths[b:b + 1, t:t + 1])
+            vals.append((f + bb, s))
+        value = sum(v_[0] for v_ in vals) / sum(v_[1] for v_ in vals) / 1e12
+        line = {"impl": "reference", "metric": VARLEN_METRIC, "value": value, "unit": UNIT,
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * sum(v_[1] for v_ in vals) / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "config": {"workload": w.name + "_varlen"},
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(0),
+                                 "kind": "oracle", "sample": "one whole timestep block per step"},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v, dout = synth.make_inputs(w, with_dout=True)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    hq, hk, hv, hd = (to(a).pin_memory() for a in (q, k, v, dout))
+    dq, dk, dv, dd = (t.to(dev) for t in (hq, hk, hv, hd))
+    hL = torch.from_numpy(lengths.reshape(-1).copy()).pin_memory()
+    dL = hL.to(dev)
+    full = torch.full_like(dL, w.S)
+    stream = torch.cuda.current_stream()
+    o = torch.zeros_like(dq)
+    lse = torch.zeros(dq.shape[:4], dtype=torch.float32, device=dev)
+    lo = torch.zeros_like(dq)
+    g = [torch.zeros_like(x) for x in (dq, dk, dv)]
+    ws = torch.empty(max(api.bwd_workspace_bytes(0, w.B, w.T, w.S, w.Hq, w.Hkv), 16),
+                     dtype=torch.uint8, device=dev)
+
+    def step(Lt, ev=None, Q=dq, K=dk, V=dv, DO=dd):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if ev is not None else None
+        if e:
+            e[0].record(stream)
+        api.space_attn_fwd_varlen(Q, K, V, Lt, w.agent, w.scale, o, lse, stream, o_lo=lo)
+        if e:
+            e[1].record(stream)
+        api.space_attn_bwd_varlen(Q, K, V, o, lse, DO, Lt, w.agent, w.scale, workspace=ws, out=g,
+                                  stream=stream, o_lo=lo)
+        if e:
+            e[2].record(stream)
+            ev.append(e)
+
+    def timed(Lt):
+        for _ in range(args.warmup):
+            step(Lt)
+        torch.cuda.synchronize()
+        if api.get_device_status() != 0:
+            raise RuntimeError("device timeout")
+        ev = []
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step(Lt, ev)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if api.get_device_status() != 0:
+            raise RuntimeError("device timeout")
+        fwd = float(np.mean([x[0].elapsed_time(x[1]) for x in ev]))
+        bwd = float(np.mean([x[1].elapsed_time(x[2]) for x in ev]))
+        return a.elapsed_time(b) / args.steps, fwd, bwd
+
+    clk = Clocks(local).__enter__()
+    ms, fwd_ms, bwd_ms = timed(dL)
+    dense_ms, dense_fwd, dense_bwd = timed(full)
+    # end to end: Q, K, V, dO and the lengths in from pinned host memory, O, LSE and the
+    # gradients back
+    hin = [hq, hk, hv, hd, hL]
+    din = [torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv), torch.empty_like(dd),
+           torch.empty_like(dL)]
+    outs = [o, lse] + g
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step():
+        for h_, d_ in zip(hin, din):
+            d_.copy_(h_, non_blocking=True)
+        step(din[4], None, din[0], din[1], din[2], din[3])
+        for d_, h_ in zip(outs, hout):
+            h_.copy_(d_, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clk.__exit__()
+    e2e_ms = a.elapsed_time(b) / args.steps
+    value = (fl_f + fl_b) / (ms * 1e-3) / 1e12
+    _, tc, _, src = load_peaks()
+    bwd_tf = fl_b / (bwd_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": bwd_tf, "peak": tc, "unit": "TFLOP/s",
+            "frac": bwd_tf / tc, "traffic": None, "kernel": "space_bwd (varlen)",
+            "peak_source": "%s bf16 burst" % src}
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        X = oracle.from_bf16
+        t0 = time.perf_counter()
+        sl = (slice(0, 1), slice(0, 1))
+        oracle.space_bwd_varlen(X(q[sl]), X(k[sl]), X(v[sl]), X(dout[sl]), lengths[:1, :1],
+                                w.agent, w.scale)
+        s_ = time.perf_counter() - t0
+        f_, b_ = varlen_space_flops(w, lengths[:1, :1])
+        cpu = {"value": (f_ + b_) / s_ / 1e12, "unit": UNIT, "cores": oracle.num_threads(0),
+               "kind": "oracle", "sample": "timestep block (0, 0), %d tokens, fwd+bwd" %
+               int(lengths[0, 0])}
+    line = {"metric": VARLEN_METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name + "_varlen", "B": w.B, "T": w.T, "S_max": w.S,
+                       "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D,
+                       "tokens_per_block": {"mean": float(lengths.mean()),
+                                            "min": int(lengths.min()), "max": int(lengths.max())},
+                       "ops": ["space_fwd", "space_bwd"], "l2": "inputs larger than L2",
+                       "parallelism": "single GPU"},
+            "per_op": {"space_fwd": {"ms": fwd_ms, "tflops": fl_f / (fwd_ms * 1e-3) / 1e12},
+                       "space_bwd": {"ms": bwd_ms, "tflops": bwd_tf}},
+            "dense": {"ms_per_step": dense_ms, "fwd_ms": dense_fwd, "bwd_ms": dense_bwd,
+                      "note": "same calls with every block holding all %d slots" % w.S},
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": (fl_f + fl_b) / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 4 * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- decode step
 DECODE_METRIC = "rollout decode step (time attention over a ring-buffer KV cache) GB/s and % of B300 HBM roofline"
 
@@ -653,6 +827,9 @@ def main():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--ref-units", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--varlen", action="store_true",
+                    help="variable-length space attention (fwd+bwd) over seeded MAE block "
+                         "lengths, e.g. with --workload tokenizer_enc")
     ap.add_argument("--no-residual", action="store_true",
                     help="the forward does not write O's residual; the backward recomputes Delta")
     ap.add_argument("--packed", action="store_true",
@@ -670,6 +847,9 @@ def main():
         w = dataclasses.replace(w, B=args.batch, name="%s_b%d" % (w.name, args.batch))
     if name.endswith("_decode"):
         run_decode(args, w)
+        return
+    if args.varlen:
+        run_varlen(args, w)
         return
     with_bwd = w.backward and not args.fwd_only
     if args.impl == "reference":

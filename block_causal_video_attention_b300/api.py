@@ -72,6 +72,10 @@ def library():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = I
+            lib.od_space_attn_fwd_varlen.argtypes = [P] * 7 + [I] * 7 + [F, P]
+            lib.od_space_attn_fwd_varlen.restype = I
+            lib.od_space_attn_bwd_varlen.argtypes = [P] * 14 + [I] * 7 + [F, P, Z, P]
+            lib.od_space_attn_bwd_varlen.restype = I
             lib.od_time_attn_decode.argtypes = [P] * 7 + [I] * 6 + [ctypes.c_longlong, F, P]
             lib.od_time_attn_decode.restype = I
             lib.od_space_attn_bwd_static_ws.argtypes = [P] * 13 + [I] * 7 + [F, P]
@@ -307,6 +311,72 @@ def time_attn_bwd_packed(qkv, num_q_heads, o, lse, dout, window, scale=None, fp3
     """Time attention backward on packed QKV -> dQKV (packed like qkv) [, fp32 dQ, dK, dV]."""
     return _bwd_packed("od_time_attn_bwd_packed", 1, qkv, num_q_heads, o, lse, dout, window,
                        scale, fp32_grads, workspace, out, stream, o_lo)
+
+
+def _check_seqlen(seqlen, B, T, device):
+    if not isinstance(seqlen, torch.Tensor) or seqlen.dtype != torch.int32 or not seqlen.is_cuda:
+        raise TypeError("seqlen must be an int32 CUDA tensor of B*T block lengths")
+    if seqlen.numel() != B * T or not seqlen.is_contiguous() or seqlen.data_ptr() % 16:
+        raise ValueError("seqlen must be a contiguous, 16-byte aligned tensor of B*T lengths")
+
+
+def space_attn_fwd_varlen(q, k, v, seqlen, agent_idx=-1, scale=None, out=None, lse=None,
+                          stream=None, o_lo=None):
+    """Space attention over variable-length timestep blocks on the padded [B,T,S,H,D] layout:
+    block (b, t) holds its first seqlen[b*T+t] tokens.  Padding rows of the outputs are left
+    as they were (allocate `out`/`lse` yourself to control them)."""
+    B, T, S, Hq, Hkv, D = _check_qkv(q, k, v)
+    _check_seqlen(seqlen, B, T, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.zeros_like(q) if out is None else out
+    l = torch.zeros((B, T, S, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if l.shape != (B, T, S, Hq) or l.dtype != torch.float32 or not l.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,T,S,Hq]")
+    r = _residual_out(o_lo, tuple(q.shape), q.device)
+    st = library().od_space_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(r),
+                                            _ptr(seqlen), B, T, S, Hq, Hkv, D, int(agent_idx),
+                                            float(scale), _stream(stream))
+    if st:
+        raise ODError(st, "od_space_attn_fwd_varlen")
+    return (o, l) if r is None else (o, l, r)
+
+
+def space_attn_bwd_varlen(q, k, v, o, lse, dout, seqlen, agent_idx=-1, scale=None,
+                          fp32_grads=False, workspace=None, out=None, stream=None, o_lo=None):
+    """Backward of space_attn_fwd_varlen -> (dQ, dK, dV) [, fp32 copies]; padding rows of
+    the gradients are left as they were (zeros when allocated here)."""
+    B, T, S, Hq, Hkv, D = _check_qkv(q, k, v)
+    _check_seqlen(seqlen, B, T, q.device)
+    for nm, t in (("o", o), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous bf16 tensor shaped like q" % nm)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        dq, dk, dv = torch.zeros_like(q), torch.zeros_like(k), torch.zeros_like(v)
+    else:
+        dq, dk, dv = out
+    f32 = (None, None, None)
+    if fp32_grads:
+        f32 = (torch.zeros(q.shape, dtype=torch.float32, device=q.device),
+               torch.zeros(k.shape, dtype=torch.float32, device=q.device),
+               torch.zeros(v.shape, dtype=torch.float32, device=q.device))
+    need = bwd_workspace_bytes(0, B, T, S, Hq, Hkv, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = library().od_space_attn_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_lo), _ptr(lse), _ptr(dout), _ptr(seqlen),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), B, T, S, Hq, Hkv,
+        D, int(agent_idx), float(scale), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+        _stream(stream))
+    if st:
+        raise ODError(st, "od_space_attn_bwd_varlen")
+    if fp32_grads:
+        return dq, dk, dv, f32
+    return dq, dk, dv
 
 
 def time_attn_decode(q, k_new, v_new, k_cache, v_cache, t, scale=None, out=None, lse=None,

@@ -123,7 +123,8 @@ od_status make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int 
 // [B,T,S,Hq+2Hkv,D] tensor that q, k and v point into.
 od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, void* o, float* lse,
                      void* o_lo, int B, int T, int S, int Hq, int Hkv, int D, int agent,
-                     int window, float scale, void* stream, int qkv_rows = 0) {
+                     int window, float scale, void* stream, int qkv_rows = 0,
+                     const int* seqlen = nullptr) {
   if (!q || !k || !v || !o || !lse) return OD_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       (o_lo && !aligned16(o_lo)))
@@ -167,6 +168,7 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kFwdBN, 1};
   p.o = static_cast<__nv_bfloat16*>(o);
   p.o_lo = static_cast<__nv_bfloat16*>(o_lo);
+  p.seqlen = is_time ? nullptr : seqlen;
   CUtensorMap tq, tk, tv;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -186,7 +188,8 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
                      const void* o_lo, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      float* dq_f32, float* dk_f32, float* dv_f32, int B, int T, int S, int Hq,
                      int Hkv, int D, int agent, int window, float scale, void* workspace,
-                     size_t workspace_bytes, void* stream, int qkv_rows = 0) {
+                     size_t workspace_bytes, void* stream, int qkv_rows = 0,
+                     const int* seqlen = nullptr) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
     return OD_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, o, o_lo, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, workspace};
@@ -237,6 +240,7 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   f.bn = od::kBN;
   f.nkb = (f.L + od::kBN - 1) / od::kBN;
   f.resident = 0;
+  f.seqlen = is_time ? nullptr : seqlen;
   f.status = dev->status;
   if (f.nitems >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
   if (1LL * B * f.F * Hkv * ((f.L + od::kKvBN - 1) / od::kKvBN) >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
@@ -557,6 +561,27 @@ od_status od_time_attn_bwd_packed(const void* qkv, const void* o, const void* o_
                                   size_t workspace_bytes, void* stream) {
   return bwd_packed(1, qkv, o, o_lo, lse, dout, dqkv, dq_f32, dk_f32, dv_f32, B, T, S, Hq, Hkv, D, -1,
                     window, scale, workspace, workspace_bytes, stream);
+}
+
+// ---- variable-length space attention: block (b, t) holds its first seqlen[b*T + t] tokens
+od_status od_space_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, void* o_lo, const int* seqlen, int B, int T, int S,
+                                   int Hq, int Hkv, int D, int agent_idx, float scale,
+                                   void* stream) {
+  if (!seqlen || !aligned16(seqlen)) return OD_ERR_INVALID_ARG;
+  return launch_fwd(0, q, k, v, o, lse, o_lo, B, T, S, Hq, Hkv, D, agent_idx, 1, scale, stream, 0,
+                    seqlen);
+}
+
+od_status od_space_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                                   const void* o_lo, const float* lse, const void* dout,
+                                   const int* seqlen, void* dq, void* dk, void* dv, float* dq_f32,
+                                   float* dk_f32, float* dv_f32, int B, int T, int S, int Hq,
+                                   int Hkv, int D, int agent_idx, float scale, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!seqlen || !aligned16(seqlen)) return OD_ERR_INVALID_ARG;
+  return launch_bwd(0, q, k, v, o, o_lo, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S,
+                    Hq, Hkv, D, agent_idx, 1, scale, workspace, workspace_bytes, stream, 0, seqlen);
 }
 
 od_status od_get_device_status_detail(void* stream, unsigned int* site_word) {

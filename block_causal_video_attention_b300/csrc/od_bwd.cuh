@@ -154,9 +154,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const long long i0 = (p.nitems * blockIdx.x) / gridDim.x;
-  const long long i1 = (p.nitems * (blockIdx.x + 1)) / gridDim.x;
   const bool resident = p.nkb <= kDqStages;
+  // items of this CTA: a contiguous range when a unit's K/V stay resident (its consecutive
+  // items reuse them); otherwise every gridDim.x-th item, so that the CTAs running at the
+  // same time work on the same units (their streamed K/V blocks are shared through L2) and
+  // items of unequal cost (variable-length blocks) spread over all CTAs
+  const bool strided = p.seqlen != nullptr || !resident;
+  const long long istep = strided ? gridDim.x : 1;
+  const long long i0 = strided ? blockIdx.x : (p.nitems * blockIdx.x) / gridDim.x;
+  const long long i1 = strided ? p.nitems : (p.nitems * (blockIdx.x + 1)) / gridDim.x;
 
   {  // zero the tile rows TMA never writes
     const int pad = (kBM - p.rows) * 128;
@@ -247,8 +253,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (lane == 0) mbar_arrive(&sm.k16[stage]);
         return true;
       };
-      for (long long i = i0; i < i1 && ok; ++i) {
+      for (long long i = i0; i < i1 && ok; i += istep) {
         const FwdItem it = fwd_decode(p, i);
+        if (!it.validA) continue;  // past the unit's length: no role touches it
         const int nb = it.kb_hi - it.kb_lo + 1;
         for (int x = 0; x < 2 && ok; ++x) {
           if (x == 1 && !it.validB) break;
@@ -283,8 +290,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       long long prev_unit = -1;
       uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
       bool ok = true;
-      for (long long i = i0; i < i1 && ok; ++i) {
+      for (long long i = i0; i < i1 && ok; i += istep) {
         const FwdItem it = fwd_decode(p, i);
+        if (!it.validA) continue;  // past the unit's length: no role touches it
         const int nb = it.kb_hi - it.kb_lo + 1;
         for (int x = 0; x < 2 && ok; ++x) {
           if (x == 1 && !it.validB) break;
@@ -340,8 +348,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         long long prev_unit = -1;
         uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
         bool ok = true;
-        for (long long i = i0; i < i1 && ok; ++i) {
+        for (long long i = i0; i < i1 && ok; i += istep) {
           const FwdItem it = fwd_decode(p, i);
+          if (!it.validA) continue;  // past the unit's length: no role touches it
           const int nb = it.kb_hi - it.kb_lo + 1;
           auto load_kv = [&](int stage, int kb) {
             const int kp = kb * kBN;
@@ -424,8 +433,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         uint32_t js = 0, jd = 0, qn = 0, unit_loads = 0, sbase = 0;
         long long prev_unit = -1;
         bool ok = true;
-        for (long long i = i0; i < i1 && ok; ++i) {
+        for (long long i = i0; i < i1 && ok; i += istep) {
           const FwdItem it = fwd_decode(p, i);
+          if (!it.validA) continue;  // past the unit's length: no role touches it
           const int nb = it.kb_hi - it.kb_lo + 1;
           if (resident && it.unit != prev_unit) {
             if (prev_unit >= 0)
@@ -522,13 +532,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const float lg2e = 1.4426950408889634f;
     uint32_t jS = 0, jD = 0;
     bool ok = true;
-    for (long long i = i0; i < i1 && ok; ++i) {
+    for (long long i = i0; i < i1 && ok; i += istep) {
       const FwdItem it = fwd_decode(p, i);
+      if (!it.validA) continue;  // past the unit's length: no role touches it
       if (x == 1 && !it.validB) continue;
       const int nb = it.kb_hi - it.kb_lo + 1;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
       const int pos = mytok0 + tok;
-      const bool row_ok = (r < p.rows) && (pos < p.L);
+      const bool row_ok = (r < p.rows) && (pos < it.L);
       long long row = 0;
       float lse2 = INFINITY, ndl = 0.f;
       float dacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -642,7 +653,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const int tk = rt / G;
           const int gg = rt - tk * G;
           const int ps = mytok0 + tk;
-          if (rt < p.rows && ps < p.L) {
+          if (rt < p.rows && ps < it.L) {
             const long long t_idx = p.is_time ? ps : it.fixed;
             const long long s_idx = p.is_time ? it.fixed : ps;
             const long long rw =
@@ -732,6 +743,8 @@ static_assert(2 * 128 * kKvElemRegs + 128 * kKvCtrlRegs == kKvThreads * kQsLaunc
 
 struct KvItem {
   int b, fixed, kvh, kb;
+  int L;           // the unit's sequence length
+  int valid;       // 0: the key block starts past the unit's length (skipped by every role)
   int t_lo, t_hi;  // Q tiles [t_lo, t_hi] that can see the key block
 };
 __device__ __forceinline__ KvItem kv_decode(const KvParams& kp, long long i) {
@@ -745,14 +758,18 @@ __device__ __forceinline__ KvItem kv_decode(const KvParams& kp, long long i) {
   const uint32_t bq = r / static_cast<uint32_t>(p.F);
   it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
   it.b = static_cast<int>(bq);
+  int L = p.L;
+  if (p.seqlen) L = min(max(__ldg(p.seqlen + static_cast<long long>(it.b) * p.T + it.fixed), 0), p.L);
+  it.L = L;
   const int k0 = it.kb * kKvBN;
-  const int k1 = min(p.L, k0 + kKvBN) - 1;
+  it.valid = k0 < L;
+  const int k1 = min(L, k0 + kKvBN) - 1;
   if (p.is_time) {
     it.t_lo = k0 / p.nTok;
-    it.t_hi = min(p.L - 1, k1 + p.window - 1) / p.nTok;
+    it.t_hi = min(L - 1, k1 + p.window - 1) / p.nTok;
   } else {
     it.t_lo = 0;
-    it.t_hi = p.ntiles - 1;
+    it.t_hi = (L - 1) / p.nTok;
   }
   return it;
 }
@@ -769,7 +786,7 @@ struct KvSeq {
       ++round;
       if (base + c < kp.nitems) {
         *it = kv_decode(kp, base + c);
-        return true;
+        if (it->valid) return true;  // key blocks past the unit's length: no role sees them
       }
     }
   }
@@ -951,7 +968,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           for (int rr = lane; rr < p.rows; rr += 32) {
             const int tk = rr / p.G;
             const int ps = t0 + tk;
-            if (ps < p.L) {
+            if (ps < it.L) {
               const long long t_idx = p.is_time ? ps : it.fixed;
               const long long s_idx = p.is_time ? it.fixed : ps;
               const long long row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq +
@@ -1094,7 +1111,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             float* rowv = which ? sm.ndel[q] : sm.nlse2[q];
             const int t0 = tq * p.nTok;
             for (int rr = lane; rr < 128; rr += 32) {
-              const bool valid = rr < p.rows && t0 + rr / p.G < p.L;
+              const bool valid = rr < p.rows && t0 + rr / p.G < it.L;
               rowv[rr] = valid ? rowv[rr] * rowf : 0.f;
             }
           }
@@ -1162,7 +1179,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tmem_ld32(tS + 32, sv + 32);
         tmem_ld32(tD, dv);
         tmem_ld32(tD + 32, dv + 32);
-        // rows [r_lo, r_hi) of the tile may read this key (invalid rows have -inf LSE2)
+        // rows [r_lo, r_hi) of the tile may read this key (rows past the sequence end of a
+        // fixed-length unit hold zero Q and dO and contribute nothing)
         const int t0 = tq * p.nTok;
         int r_lo = 0, r_hi = 128;
         if (p.is_time) {
@@ -1174,6 +1192,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           r_lo = static_cast<int>(min(max(d * p.G, 0LL), 128LL));
           r_hi = static_cast<int>(min(max((d + 1) * p.G, 0LL), 128LL));
         }
+        // rows past the unit's length (padding of a variable-length block) read nothing
+        if (it.L < p.L) r_hi = min(r_hi, static_cast<int>(min(max(static_cast<long long>(it.L - t0) * p.G, 0LL), 128LL)));
         tmem_wait_ld_dep32(sv);
         tmem_wait_ld_dep32(sv + 32);
         tmem_wait_ld_dep32(dv);
@@ -1217,7 +1237,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.acc_free);
-      if (kpos < p.L) {
+      if (kpos < it.L) {
         const float f = h ? ldexpf(1.f, -edo) : kp.scale * ldexpf(1.f, -(eds + eq));
         const long long t_idx = p.is_time ? kpos : it.fixed;
         const long long s_idx = p.is_time ? it.fixed : kpos;

@@ -52,6 +52,10 @@ struct FwdParams {
   // reciprocals for the item decode: floor(2^64 / d) + 1 for d = npairs, Hkv, F (0 when
   // d >= 2^16, where the plain division is used)
   unsigned long long rcp_npairs, rcp_hkv, rcp_f;
+  // space attention with variable-length timestep blocks: block (b, t) holds its first
+  // seqlen[b * T + t] tokens (clamped to [0, S]); the rest of the S slots are padding that
+  // is neither read as a key nor written as a query row.  NULL: every block holds S tokens.
+  const int* seqlen;
   __nv_bfloat16* o;
   __nv_bfloat16* o_lo;   // optional: O - bf16(O), rounded to bf16 (for the backward's Delta)
   float* lse;
@@ -61,7 +65,9 @@ struct FwdParams {
 struct FwdItem {
   uint32_t unit;
   int b, fixed, kvh;
+  int L;               // the unit's sequence length (p.L, or its block's length)
   int tok0[2];
+  int validA;          // 0: tile A starts past the unit's length -- nothing to do
   int validB;
   int key_lo, key_hi;  // allowed key positions of the item lie in [key_lo, key_hi)
   int kb_lo, kb_hi;    // inclusive key-block range
@@ -91,20 +97,24 @@ __device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
   const uint32_t bq = div_rcp(r, static_cast<uint32_t>(p.F), p.rcp_f);
   it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
   it.b = static_cast<int>(bq);
+  int L = p.L;
+  if (p.seqlen) L = min(max(__ldg(p.seqlen + static_cast<long long>(it.b) * p.T + it.fixed), 0), p.L);
+  it.L = L;
   const int tA = 2 * pair;
   it.tok0[0] = tA * p.nTok;
   it.tok0[1] = (tA + 1) * p.nTok;
-  it.validB = (tA + 1) < p.ntiles;
-  const int last = min(p.L, (it.validB ? tA + 2 : tA + 1) * p.nTok) - 1;
+  it.validA = it.tok0[0] < L;
+  it.validB = (tA + 1) < p.ntiles && it.tok0[1] < L;
+  const int last = min(L, (it.validB ? tA + 2 : tA + 1) * p.nTok) - 1;
   if (p.is_time) {
     it.key_lo = max(0, it.tok0[0] - p.window + 1);
     it.key_hi = last + 1;
   } else {
     it.key_lo = 0;
-    it.key_hi = p.L;
+    it.key_hi = L;
   }
   it.kb_lo = it.key_lo / p.bn;
-  it.kb_hi = (it.key_hi - 1) / p.bn;
+  it.kb_hi = it.validA ? (it.key_hi - 1) / p.bn : it.kb_lo - 1;  // no blocks when skipped
   return it;
 }
 

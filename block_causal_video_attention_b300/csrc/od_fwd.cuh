@@ -109,8 +109,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  const long long i0 = (p.nitems * blockIdx.x) / gridDim.x;
-  const long long i1 = (p.nitems * (blockIdx.x + 1)) / gridDim.x;
+  // items of this CTA: a contiguous range when a unit's K/V stay resident (its consecutive
+  // items reuse them); otherwise every gridDim.x-th item, so that the CTAs running at the
+  // same time work on the same units (their streamed K/V blocks are shared through L2) and
+  // items of unequal cost (variable-length blocks) spread over all CTAs
+  const bool strided = p.seqlen != nullptr || !p.resident;
+  const long long istep = strided ? gridDim.x : 1;
+  const long long i0 = strided ? blockIdx.x : (p.nitems * blockIdx.x) / gridDim.x;
+  const long long i1 = strided ? p.nitems : (p.nitems * (blockIdx.x + 1)) / gridDim.x;
   OD_TRACE_INIT();
 
   // zero the Q-tile rows that TMA never writes (rows >= p.rows)
@@ -167,8 +173,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         long long prev_unit = -1;
         uint32_t unit_loads = 0, stream_cnt = 0, qn0 = 0, qn1 = 0;
         bool ok = true;
-        for (long long i = i0; i < i1 && ok; ++i) {
+        for (long long i = i0; i < i1 && ok; i += istep) {
           const FwdItem it = fwd_decode(p, i);
+          if (!it.validA) continue;  // past the unit's length: no role touches it
           auto load_kv = [&](int stage, int kb) {
             const int kp = kb * kFwdBN;
             mbar_arrive_expect_tx(&sm.k_full[stage], kFwdKVTile);
@@ -290,8 +297,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!p.resident) mma_commit_w(&sm.kv_empty[jb.stage]);
           return true;
         };
-        for (long long i = i0; i < i1 && ok; ++i) {
+        for (long long i = i0; i < i1 && ok; i += istep) {
           const FwdItem it = fwd_decode(p, i);
+          if (!it.validA) continue;  // past the unit's length: no role touches it
           const int nb = it.kb_hi - it.kb_lo + 1;
           if (p.resident && it.unit != prev_unit) {
             if (prev_unit >= 0) {
@@ -405,8 +413,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (lane == 0) mbar_arrive(&sm.v16_ready[stage]);
         return true;
       };
-      for (long long i = i0; i < i1 && ok; ++i) {
+      for (long long i = i0; i < i1 && ok; i += istep) {
         const FwdItem it = fwd_decode(p, i);
+        if (!it.validA) continue;  // past the unit's length: no role touches it
         if (p.resident) {
           if (it.unit != prev_unit) {
             ++unit_loads;
@@ -439,8 +448,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     long long prev_unit = -1;
     uint32_t unit_loads = 0, stream_next = 0;
     bool ok = true;
-    for (long long i = i0; i < i1 && ok; ++i) {
+    for (long long i = i0; i < i1 && ok; i += istep) {
       const FwdItem it = fwd_decode(p, i);
+      if (!it.validA) continue;  // past the unit's length: no role touches it
       if (p.resident && it.unit != prev_unit) {
         ++unit_loads;
         prev_unit = it.unit;
@@ -451,7 +461,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (x == 1 && !it.validB) continue;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
       const int pos = mytok0 + tok;
-      const bool row_ok = (r < p.rows) && (pos < p.L);
+      const bool row_ok = (r < p.rows) && (pos < it.L);
       float m_used = -INFINITY, l = 0.f;
       for (int bi = 0; bi < nb; ++bi) {
         const int kb = it.kb_lo + bi;
@@ -647,7 +657,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int tg = sm.rowtg[rt];
           const int gg = tg & 0xFF;
           const int ps = mytok0 + (tg >> 8);
-          if (rt < p.rows && ps < p.L) {
+          if (rt < p.rows && ps < it.L) {
             const long long t_idx = p.is_time ? ps : it.fixed;
             const long long s_idx = p.is_time ? it.fixed : ps;
             const long long row =

@@ -156,11 +156,25 @@ WORKLOADS = {
     # frame; d_model 1536 as 24 heads x 64; no agent; window = T = 32.
     "tokenizer_enc": Workload("tokenizer_enc", 2, 32, 1432, 24, 24, 64, 32, -1, 4, True,
                               "tokenizer encoder layer, forward + backward"),
+    # Tokenizer decoder: the same 1432 tokens per frame at d_model 1024, read as 16 heads x 64
+    # (the pages give the width, not the head split).
+    "tokenizer_dec": Workload("tokenizer_dec", 2, 32, 1432, 16, 16, 64, 32, -1, 6, True,
+                              "tokenizer decoder layer, forward + backward"),
     # Rollout decode of the Minecraft dynamics layer: 16 concurrent rollouts, one new frame
     # per step attending to a full 192-frame window (T = absolute index of the new frame + 1).
     "minecraft_decode": Workload("minecraft_decode", 16, 501, 290, 30, 3, 64, 192, 289, 5, False,
                                  "Minecraft 1.6B dynamics layer, rollout decode step"),
 }
+
+
+def mae_block_lengths(B: int, T: int, seed: int, patches: int = 920, latents: int = 512,
+                      max_mask: float = 0.9) -> np.ndarray:
+    """Tokens per timestep block of a tokenizer encoder that drops its masked patches: the
+    512 latents plus the kept patches, with a mask ratio drawn uniformly from [0, max_mask]
+    per block (splitmix64 uniforms of stream `seed`).  int32 [B, T]."""
+    u = _uniform(seed, 0, B * T)
+    kept = np.rint(patches * (1.0 - max_mask * u)).astype(np.int64)
+    return (latents + kept).astype(np.int32).reshape(B, T)
 
 
 def make_decode_inputs(w: Workload):

@@ -132,6 +132,29 @@ od_status od_time_attn_bwd_packed(const void* qkv, const void* o, const void* o_
                                   int window, float scale, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/* Variable-length space attention.  The tokenizer is a masked autoencoder (7minutos.es page,
+ * section "Arquitectura: una columna vertebral, dos modelos"; up to 90 % of the patches
+ * masked); an encoder that drops the masked patches instead of replacing them sees a
+ * different number of tokens in each timestep block.  These calls take the padded layout
+ * [B, T, S, H, D] (S = the longest block) and `seqlen`, a device array of B*T int32 (16-byte
+ * aligned): block (b, t) holds its first seqlen[b*T + t] tokens (values are clamped to
+ * [0, S]); the remaining slots are padding.  Per block the result is exactly space attention
+ * over its first seqlen tokens (the agent rule applies when agent_idx < seqlen).  Work
+ * scales with the lengths: tiles and key blocks past a block's length are never loaded or
+ * computed.  Padding rows of Q, K, V and dO must hold finite values (zeros will do); the
+ * outputs' padding rows (O, LSE, o_lo, dQ, dK, dV and the fp32 copies) are left unchanged.
+ * The backward takes the forward's o_lo like od_space_attn_bwd. */
+od_status od_space_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, void* o_lo, const int* seqlen, int B, int T, int S,
+                                   int Hq, int Hkv, int D, int agent_idx, float scale,
+                                   void* stream);
+od_status od_space_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                                   const void* o_lo, const float* lse, const void* dout,
+                                   const int* seqlen, void* dq, void* dk, void* dv, float* dq_f32,
+                                   float* dk_f32, float* dv_f32, int B, int T, int S, int Hq,
+                                   int Hkv, int D, int agent_idx, float scale, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
 /* One rollout (decode) step of time attention over a ring-buffer KV cache.  A rollout
  * generates one frame at a time (the local rollout harness and the frame-by-frame demo,
  * 7minutos.es page, section "Lo que realmente se envió"); the time layer then needs, for

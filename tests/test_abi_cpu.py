@@ -22,7 +22,7 @@ def test_every_declared_symbol_is_exported(lib):
             "od_attn_bwd_workspace_bytes", "od_get_device_status", "od_get_device_status_detail",
             "od_status_string", "od_space_attn_bwd_static_ws", "od_time_attn_decode",
             "od_space_attn_fwd_packed", "od_time_attn_fwd_packed", "od_space_attn_bwd_packed",
-            "od_time_attn_bwd_packed",
+            "od_time_attn_bwd_packed", "od_space_attn_fwd_varlen", "od_space_attn_bwd_varlen",
             "od_version"} <= declared
     for name in declared:
         assert hasattr(lib, name), name
@@ -129,6 +129,19 @@ def test_packed_calls_reject_invalid_arguments(lib):
     assert b(*args(P(1 << 20), P((1 << 20) + n - 16))) == 1                     # overlapping
     assert b(*args(P((1 << 20) + n - 16), P(1 << 20))) == 1
     assert lib.od_time_attn_bwd_packed(*args(P(1 << 20), P(1 << 20))) == 1      # aliased
+
+
+def test_varlen_calls_reject_invalid_arguments(lib):
+    f = lib.od_space_attn_fwd_varlen
+    good = (GOOD,) * 5 + (P(0),)
+    assert f(*good, P(0), 1, 4, 8, 4, 2, 64, 0, 0.125, P(0)) == 1               # no lengths
+    assert f(*good, P(4100), 1, 4, 8, 4, 2, 64, 0, 0.125, P(0)) == 1            # misaligned
+    assert f(*good, GOOD, 1, 4, 8, 4, 2, 64, 9, 0.125, P(0)) == 1               # agent >= S
+    b = lib.od_space_attn_bwd_varlen
+    ws = lib.od_attn_bwd_workspace_bytes(0, 1, 4, 8, 4, 2, 64)
+    ptrs = [GOOD] * 4 + [P(0), GOOD, GOOD]        # q k v o (no o_lo) lse dO
+    assert b(*ptrs, P(0), *([GOOD] * 3), *([P(0)] * 3), 1, 4, 8, 4, 2, 64, 0, 0.125, GOOD, ws,
+             P(0)) == 1
 
 
 def test_binding_refuses_cpu_tensors():

@@ -94,7 +94,7 @@ def test_backward_gradient_invariants_on_gpu():
     assert torch.count_nonzero(dq[:, 3:]) == 0
 
 
-@pytest.mark.parametrize("name", ["minecraft_fwd_bwd", "tokenizer_enc"])
+@pytest.mark.parametrize("name", ["minecraft_fwd_bwd", "tokenizer_enc", "tokenizer_dec"])
 def test_backward_full_size_sampled_units(oracle_mod, name):
     """Full-size backward (the bench's configuration): every gradient element is written and
     finite; whole sampled units are checked against the oracle."""

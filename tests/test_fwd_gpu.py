@@ -125,7 +125,7 @@ def test_causality_on_gpu():
     assert torch.equal(o1[:, 16:], o3[:, 16:])   # rows t >= 16 never see frames < 10
 
 
-@pytest.mark.parametrize("name", ["coinrun", "minecraft_fwd", "tokenizer_enc"])
+@pytest.mark.parametrize("name", ["coinrun", "minecraft_fwd", "tokenizer_enc", "tokenizer_dec"])
 def test_full_size_sampled_units(oracle_mod, name):
     """Full-size launch (the bench's configuration); every element is checked for being
     written and finite, and whole sampled units are checked against the oracle."""

@@ -516,6 +516,16 @@ def test_workload_shapes_follow_the_pages():
     p = facts["patch_size"]
     assert tk.S == (h // p) * (w // p) + facts["tokenizer_latents_per_frame"]
     assert tk.Hq * tk.D == facts["tokenizer_encoder_d_model"]
+    td = synth.WORKLOADS["tokenizer_dec"]
+    assert td.S == tk.S and td.Hq * td.D == facts["tokenizer_decoder_d_model"]
+    assert (h // p) * (w // p) == facts["tokenizer_patches_per_frame"]
+    # blocks of an encoder that drops its masked patches: 512 latents + the kept patches,
+    # a mask ratio of at most 0.9 keeping at least 92 of the 920
+    lat, pat = facts["tokenizer_latents_per_frame"], facts["tokenizer_patches_per_frame"]
+    L = synth.mae_block_lengths(64, 32, 7)
+    kept_min = round(pat * (1 - facts["mae_max_mask_probability"]))
+    assert L.dtype == np.int32 and L.min() >= lat + kept_min and L.max() <= lat + pat
+    assert L.max() - L.min() > 0.7 * pat   # the ratios cover most of [0, 0.9]
     assert synth.WORKLOADS["minecraft_fwd_bwd"].q_shape() == mc.q_shape()
 
 
