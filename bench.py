@@ -71,13 +71,13 @@ def bwd_bytes(w):
 # --metrics dram__bytes_read.sum,dram__bytes_write.sum (summary in profiles/).  They hold only
 # for the kernel sources they were measured on: any change to those sources voids them.
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "003634db7e40ed0f8f0a58ac8603ff146c6b0f1916c4c048b1cc35c1d4fcbf56",
+    "csrc_sha256": "35e77ff810e8342725e3640f489d60df06c7ea9c2d26bf3b408628b7169929f6",
     "minecraft_fwd_bwd": {
         # forward with the O residual; backward: Delta from O + O_lo, dQ, dK/dV
-        "space_fwd": 927257344,
-        "time_fwd": 924111104,
-        "space_bwd": 2883083520,
-        "time_bwd": 2898746368,
+        "space_fwd": 927417856,
+        "time_fwd": 924072960,
+        "space_bwd": 2883421184,
+        "time_bwd": 2898779904,
     },
     # decode: 4-rollout capture (176.43 MB read, 5.53 MB written) scaled by the units (x4)
     "minecraft_decode": {"decode": 727837696},
