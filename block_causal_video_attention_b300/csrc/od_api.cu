@@ -46,15 +46,18 @@ od_status device_state(DeviceState** out) {
     void* sp = nullptr;
     if (cudaGetSymbolAddress(&sp, g_od_status) != cudaSuccess) return OD_ERR_CUDA;
     d.status = static_cast<unsigned int*>(sp);
-    if (cudaFuncSetAttribute(od::od_attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(od::kFwdSmemBytes)) != cudaSuccess)
-      return OD_ERR_CUDA;
-    // The forward kernel redistributes its launch registers between warpgroups
-    // (setmaxnreg); that split is only valid for the register count it was designed for.
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, od::od_attn_fwd_kernel) != cudaSuccess ||
-        fa.numRegs != od::kFwdLaunchRegs)
-      return OD_ERR_CUDA;
+    // The forward kernel redistributes its launch registers between warpgroups (setmaxnreg);
+    // that split is only valid for the register count it was designed for.
+    for (int varlen = 0; varlen < 2; ++varlen) {
+      const void* fn = varlen ? reinterpret_cast<const void*>(od::od_attn_fwd_kernel<true>)
+                              : reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false>);
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(od::kFwdSmemBytes)) != cudaSuccess)
+        return OD_ERR_CUDA;
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess || fa.numRegs != od::kFwdLaunchRegs)
+        return OD_ERR_CUDA;
+    }
     if (od::bwd_setup() != cudaSuccess) return OD_ERR_CUDA;
     {
       int per_sm = 0;
@@ -179,8 +182,12 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
     return st;
 
   const long long grid = p.nitems < dev->num_sms ? p.nitems : dev->num_sms;
-  od::od_attn_fwd_kernel<<<(unsigned)grid, od::kFwdThreads, od::kFwdSmemBytes,
-                           static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, p);
+  if (p.seqlen)
+    od::od_attn_fwd_kernel<true><<<(unsigned)grid, od::kFwdThreads, od::kFwdSmemBytes,
+                                   static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, p);
+  else
+    od::od_attn_fwd_kernel<false><<<(unsigned)grid, od::kFwdThreads, od::kFwdSmemBytes,
+                                    static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? OD_OK : OD_ERR_CUDA;
 }
 
@@ -299,10 +306,16 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
       dp.amax_slots = amax_slots;
       od::od_bwd_delta_o_kernel<<<(unsigned)dgrid, od::kDeltaOThreads, 0, strm>>>(d);
     } else {
-      od::od_bwd_dq_kernel<true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+      if (f.seqlen)
+        od::od_bwd_dq_kernel<true, true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+      else
+        od::od_bwd_dq_kernel<true, false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
     }
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
-    od::od_bwd_dq_kernel<false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+    if (f.seqlen)
+      od::od_bwd_dq_kernel<false, true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+    else
+      od::od_bwd_dq_kernel<false, false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
   }
   // 3. dK, dV
@@ -328,7 +341,10 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     kp.amax = amax;
     kp.amax_slots = amax_slots;
     const long long grid = kp.nitems < num_ctas ? kp.nitems : num_ctas;
-    od::od_bwd_dkdv_kernel<<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
+    if (f.seqlen)
+      od::od_bwd_dkdv_kernel<true><<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
+    else
+      od::od_bwd_dkdv_kernel<false><<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
   }
   return OD_OK;

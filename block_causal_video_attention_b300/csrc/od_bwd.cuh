@@ -135,7 +135,7 @@ static_assert(kDqSmemBytes <= 227 * 1024, "shared memory budget");
 // kDelta = true: the Delta pass -- S and dP per key block, Delta = sum_j P_j dP_j accumulated
 // in fp32 per row and written to the workspace (no dS, no dQ).  This is <dO, O> for the exact
 // forward output, which the bf16 O given to the backward only approximates.
-template <bool kDelta>
+template <bool kDelta, bool kVarlen>
 __global__ void __launch_bounds__(kDqThreads, 1)
     od_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -155,11 +155,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const bool resident = p.nkb <= kDqStages;
-  // items of this CTA: a contiguous range when a unit's K/V stay resident (its consecutive
-  // items reuse them); otherwise every gridDim.x-th item, so that the CTAs running at the
-  // same time work on the same units (their streamed K/V blocks are shared through L2) and
-  // items of unequal cost (variable-length blocks) spread over all CTAs
-  const bool strided = p.seqlen != nullptr || !resident;
+  // items of this CTA: a contiguous range (consecutive items of a unit share its K/V); for
+  // variable-length blocks every gridDim.x-th item, so that items of unequal cost spread
+  // over all CTAs
+  const bool strided = kVarlen;
   const long long istep = strided ? gridDim.x : 1;
   const long long i0 = strided ? blockIdx.x : (p.nitems * blockIdx.x) / gridDim.x;
   const long long i1 = strided ? p.nitems : (p.nitems * (blockIdx.x + 1)) / gridDim.x;
@@ -254,8 +253,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         return true;
       };
       for (long long i = i0; i < i1 && ok; i += istep) {
-        const FwdItem it = fwd_decode(p, i);
-        if (!it.validA) continue;  // past the unit's length: no role touches it
+        const FwdItem it = fwd_decode<kVarlen>(p, i);
+        if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
         const int nb = it.kb_hi - it.kb_lo + 1;
         for (int x = 0; x < 2 && ok; ++x) {
           if (x == 1 && !it.validB) break;
@@ -291,8 +290,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
       bool ok = true;
       for (long long i = i0; i < i1 && ok; i += istep) {
-        const FwdItem it = fwd_decode(p, i);
-        if (!it.validA) continue;  // past the unit's length: no role touches it
+        const FwdItem it = fwd_decode<kVarlen>(p, i);
+        if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
         const int nb = it.kb_hi - it.kb_lo + 1;
         for (int x = 0; x < 2 && ok; ++x) {
           if (x == 1 && !it.validB) break;
@@ -349,8 +348,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
         bool ok = true;
         for (long long i = i0; i < i1 && ok; i += istep) {
-          const FwdItem it = fwd_decode(p, i);
-          if (!it.validA) continue;  // past the unit's length: no role touches it
+          const FwdItem it = fwd_decode<kVarlen>(p, i);
+          if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
           const int nb = it.kb_hi - it.kb_lo + 1;
           auto load_kv = [&](int stage, int kb) {
             const int kp = kb * kBN;
@@ -434,8 +433,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         long long prev_unit = -1;
         bool ok = true;
         for (long long i = i0; i < i1 && ok; i += istep) {
-          const FwdItem it = fwd_decode(p, i);
-          if (!it.validA) continue;  // past the unit's length: no role touches it
+          const FwdItem it = fwd_decode<kVarlen>(p, i);
+          if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
           const int nb = it.kb_hi - it.kb_lo + 1;
           if (resident && it.unit != prev_unit) {
             if (prev_unit >= 0)
@@ -533,13 +532,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint32_t jS = 0, jD = 0;
     bool ok = true;
     for (long long i = i0; i < i1 && ok; i += istep) {
-      const FwdItem it = fwd_decode(p, i);
-      if (!it.validA) continue;  // past the unit's length: no role touches it
+      const FwdItem it = fwd_decode<kVarlen>(p, i);
+      if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
       if (x == 1 && !it.validB) continue;
       const int nb = it.kb_hi - it.kb_lo + 1;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
       const int pos = mytok0 + tok;
-      const bool row_ok = (r < p.rows) && (pos < it.L);
+      const bool row_ok = (r < p.rows) && (pos < (kVarlen ? it.L : p.L));
       long long row = 0;
       float lse2 = INFINITY, ndl = 0.f;
       float dacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -653,7 +652,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const int tk = rt / G;
           const int gg = rt - tk * G;
           const int ps = mytok0 + tk;
-          if (rt < p.rows && ps < it.L) {
+          if (rt < p.rows && ps < (kVarlen ? it.L : p.L)) {
             const long long t_idx = p.is_time ? ps : it.fixed;
             const long long s_idx = p.is_time ? it.fixed : ps;
             const long long rw =
@@ -747,6 +746,7 @@ struct KvItem {
   int valid;       // 0: the key block starts past the unit's length (skipped by every role)
   int t_lo, t_hi;  // Q tiles [t_lo, t_hi] that can see the key block
 };
+template <bool kVarlen>
 __device__ __forceinline__ KvItem kv_decode(const KvParams& kp, long long i) {
   const FwdParams& p = kp.f;
   KvItem it;
@@ -759,22 +759,23 @@ __device__ __forceinline__ KvItem kv_decode(const KvParams& kp, long long i) {
   it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
   it.b = static_cast<int>(bq);
   int L = p.L;
-  if (p.seqlen) L = min(max(__ldg(p.seqlen + static_cast<long long>(it.b) * p.T + it.fixed), 0), p.L);
+  if (kVarlen) L = min(max(__ldg(p.seqlen + static_cast<long long>(it.b) * p.T + it.fixed), 0), p.L);
   it.L = L;
   const int k0 = it.kb * kKvBN;
-  it.valid = k0 < L;
+  it.valid = kVarlen ? k0 < L : 1;
   const int k1 = min(L, k0 + kKvBN) - 1;
   if (p.is_time) {
     it.t_lo = k0 / p.nTok;
     it.t_hi = min(L - 1, k1 + p.window - 1) / p.nTok;
   } else {
     it.t_lo = 0;
-    it.t_hi = (L - 1) / p.nTok;
+    it.t_hi = kVarlen ? (L - 1) / p.nTok : p.ntiles - 1;
   }
   return it;
 }
 
 // The CTA's item sequence: round r takes item r*grid + c (r even) or r*grid + grid-1-c.
+template <bool kVarlen>
 struct KvSeq {
   long long round = 0;
   __device__ __forceinline__ bool next(const KvParams& kp, KvItem* it) {
@@ -785,8 +786,8 @@ struct KvSeq {
                                       : static_cast<long long>(blockIdx.x);
       ++round;
       if (base + c < kp.nitems) {
-        *it = kv_decode(kp, base + c);
-        if (it->valid) return true;  // key blocks past the unit's length: no role sees them
+        *it = kv_decode<kVarlen>(kp, base + c);
+        if (!kVarlen || it->valid) return true;  // blocks past the length: no role sees them
       }
     }
   }
@@ -825,6 +826,7 @@ __device__ __forceinline__ void dkdv_chunk(const float* sv, const float* dv, con
 }
 
 
+template <bool kVarlen>
 __global__ void __launch_bounds__(kKvThreads, 1)
     od_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -917,7 +919,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     regs_dec<kKvCtrlRegs>();
     if (warp == kKvProducerWarp) {
       // ---------------------------------------------------------- producer (whole warp)
-      KvSeq seq;
+      KvSeq<kVarlen> seq;
       KvItem it;
       uint32_t n = 0, tau = 0;
       bool ok = true;
@@ -968,7 +970,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           for (int rr = lane; rr < p.rows; rr += 32) {
             const int tk = rr / p.G;
             const int ps = t0 + tk;
-            if (ps < it.L) {
+            if (ps < (kVarlen ? it.L : p.L)) {
               const long long t_idx = p.is_time ? ps : it.fixed;
               const long long s_idx = p.is_time ? it.fixed : ps;
               const long long row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq +
@@ -1001,7 +1003,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const uint32_t idesc_sp = idesc_fp16(128, 64, 0, 0);   // M keys, N 64 tile rows
         const uint32_t idesc_acc = idesc_fp16(128, 64, 0, 1);  // M keys, N head dim, B MN-major
         const uint32_t tDK = tmem + 256, tDV = tmem + 320;
-        KvSeq seq;
+        KvSeq<kVarlen> seq;
         KvItem cur, nxt;
         bool ok = seq.next(kp, &cur);
         uint32_t n = 0, tau = 0;      // item and tile ordinals of the current tile
@@ -1094,7 +1096,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int which = warp - kKvConvWarp;  // 0: Q, 1: dO
       const float sqd = ldexpf(1.f, which ? edo : eq);
       const float rowf = which ? -ldexpf(1.f, eds) : -1.4426950408889634f;
-      KvSeq seq;
+      KvSeq<kVarlen> seq;
       KvItem it;
       uint32_t n = 0, tau = 0;
       bool ok = true;
@@ -1111,7 +1113,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             float* rowv = which ? sm.ndel[q] : sm.nlse2[q];
             const int t0 = tq * p.nTok;
             for (int rr = lane; rr < 128; rr += 32) {
-              const bool valid = rr < p.rows && t0 + rr / p.G < it.L;
+              const bool valid = rr < p.rows && t0 + rr / p.G < (kVarlen ? it.L : p.L);
               rowv[rr] = valid ? rowv[rr] * rowf : 0.f;
             }
           }
@@ -1134,7 +1136,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const float2 sl2 = make_float2(slx, slx), c12 = make_float2(c1, c1);
     const int Weff = min(p.window, p.L);
     const float skv = ldexpf(1.f, h ? ev : ek);
-    KvSeq seq;
+    KvSeq<kVarlen> seq;
     KvItem it;
     uint32_t n = 0, tau = 0;
     bool ok = true;
@@ -1193,7 +1195,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           r_hi = static_cast<int>(min(max((d + 1) * p.G, 0LL), 128LL));
         }
         // rows past the unit's length (padding of a variable-length block) read nothing
-        if (it.L < p.L) r_hi = min(r_hi, static_cast<int>(min(max(static_cast<long long>(it.L - t0) * p.G, 0LL), 128LL)));
+        if (kVarlen && it.L < p.L) r_hi = min(r_hi, static_cast<int>(min(max(static_cast<long long>(it.L - t0) * p.G, 0LL), 128LL)));
         tmem_wait_ld_dep32(sv);
         tmem_wait_ld_dep32(sv + 32);
         tmem_wait_ld_dep32(dv);
@@ -1237,7 +1239,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.acc_free);
-      if (kpos < it.L) {
+      if (kpos < (kVarlen ? it.L : p.L)) {
         const float f = h ? ldexpf(1.f, -edo) : kp.scale * ldexpf(1.f, -(eds + eq));
         const long long t_idx = p.is_time ? kpos : it.fixed;
         const long long s_idx = p.is_time ? it.fixed : kpos;
@@ -1274,28 +1276,36 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 }
 
 // ============================================================================ host side
-inline cudaError_t bwd_setup() {
-  cudaError_t e = cudaFuncSetAttribute(od_bwd_dq_kernel<false>,
+template <bool kVarlen>
+inline cudaError_t bwd_setup_one() {
+  cudaError_t e = cudaFuncSetAttribute(od_bwd_dq_kernel<false, kVarlen>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kDqSmemBytes));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(od_bwd_dq_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(od_bwd_dq_kernel<true, kVarlen>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kDqSmemBytes));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(od_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(od_bwd_dkdv_kernel<kVarlen>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kKvSmemBytes));
   if (e != cudaSuccess) return e;
+  // each kernel redistributes its launch registers between warpgroups (setmaxnreg); the split
+  // is only valid for the register count it was designed for
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<false>);
+  e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<false, kVarlen>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<true>);
+  e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<true, kVarlen>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncGetAttributes(&fa, od_bwd_dkdv_kernel);
+  e = cudaFuncGetAttributes(&fa, od_bwd_dkdv_kernel<kVarlen>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
+}
+inline cudaError_t bwd_setup() {
+  cudaError_t e = bwd_setup_one<false>();
+  return e != cudaSuccess ? e : bwd_setup_one<true>();
 }
 
 // ============================================================================ Delta from O

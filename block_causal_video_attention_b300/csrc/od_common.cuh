@@ -85,6 +85,9 @@ inline unsigned long long host_div_rcp(int d) {
   return (~0ull) / static_cast<unsigned long long>(d) + 1ull;
 }
 
+// kVarlen: space attention over variable-length blocks (p.seqlen); false compiles the
+// fixed-length decode with no trace of the per-unit length.
+template <bool kVarlen>
 __device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
   // the host guarantees nitems < 2^31, so 32-bit unsigned division suffices
   FwdItem it;
@@ -98,13 +101,13 @@ __device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
   it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
   it.b = static_cast<int>(bq);
   int L = p.L;
-  if (p.seqlen) L = min(max(__ldg(p.seqlen + static_cast<long long>(it.b) * p.T + it.fixed), 0), p.L);
+  if (kVarlen) L = min(max(__ldg(p.seqlen + static_cast<long long>(it.b) * p.T + it.fixed), 0), p.L);
   it.L = L;
   const int tA = 2 * pair;
   it.tok0[0] = tA * p.nTok;
   it.tok0[1] = (tA + 1) * p.nTok;
-  it.validA = it.tok0[0] < L;
-  it.validB = (tA + 1) < p.ntiles && it.tok0[1] < L;
+  it.validA = kVarlen ? it.tok0[0] < L : 1;
+  it.validB = (tA + 1) < p.ntiles && (!kVarlen || it.tok0[1] < L);
   const int last = min(L, (it.validB ? tA + 2 : tA + 1) * p.nTok) - 1;
   if (p.is_time) {
     it.key_lo = max(0, it.tok0[0] - p.window + 1);
@@ -114,7 +117,7 @@ __device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
     it.key_hi = L;
   }
   it.kb_lo = it.key_lo / p.bn;
-  it.kb_hi = it.validA ? (it.key_hi - 1) / p.bn : it.kb_lo - 1;  // no blocks when skipped
+  it.kb_hi = (!kVarlen || it.validA) ? (it.key_hi - 1) / p.bn : it.kb_lo - 1;  // none if skipped
   return it;
 }
 

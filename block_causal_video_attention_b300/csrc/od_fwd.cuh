@@ -92,6 +92,7 @@ struct PvJob {
   uint8_t stage, vpar, ksteps, acc_a, acc_b;
 };
 
+template <bool kVarlen>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     od_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -109,11 +110,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // items of this CTA: a contiguous range when a unit's K/V stay resident (its consecutive
-  // items reuse them); otherwise every gridDim.x-th item, so that the CTAs running at the
-  // same time work on the same units (their streamed K/V blocks are shared through L2) and
-  // items of unequal cost (variable-length blocks) spread over all CTAs
-  const bool strided = p.seqlen != nullptr || !p.resident;
+  // items of this CTA: a contiguous range (consecutive items of a unit share its K/V); for
+  // variable-length blocks every gridDim.x-th item, so that items of unequal cost spread
+  // over all CTAs
+  const bool strided = kVarlen;
   const long long istep = strided ? gridDim.x : 1;
   const long long i0 = strided ? blockIdx.x : (p.nitems * blockIdx.x) / gridDim.x;
   const long long i1 = strided ? p.nitems : (p.nitems * (blockIdx.x + 1)) / gridDim.x;
@@ -174,8 +174,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint32_t unit_loads = 0, stream_cnt = 0, qn0 = 0, qn1 = 0;
         bool ok = true;
         for (long long i = i0; i < i1 && ok; i += istep) {
-          const FwdItem it = fwd_decode(p, i);
-          if (!it.validA) continue;  // past the unit's length: no role touches it
+          const FwdItem it = fwd_decode<kVarlen>(p, i);
+          if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
           auto load_kv = [&](int stage, int kb) {
             const int kp = kb * kFwdBN;
             mbar_arrive_expect_tx(&sm.k_full[stage], kFwdKVTile);
@@ -298,8 +298,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           return true;
         };
         for (long long i = i0; i < i1 && ok; i += istep) {
-          const FwdItem it = fwd_decode(p, i);
-          if (!it.validA) continue;  // past the unit's length: no role touches it
+          const FwdItem it = fwd_decode<kVarlen>(p, i);
+          if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
           const int nb = it.kb_hi - it.kb_lo + 1;
           if (p.resident && it.unit != prev_unit) {
             if (prev_unit >= 0) {
@@ -414,8 +414,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         return true;
       };
       for (long long i = i0; i < i1 && ok; i += istep) {
-        const FwdItem it = fwd_decode(p, i);
-        if (!it.validA) continue;  // past the unit's length: no role touches it
+        const FwdItem it = fwd_decode<kVarlen>(p, i);
+        if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
         if (p.resident) {
           if (it.unit != prev_unit) {
             ++unit_loads;
@@ -449,8 +449,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint32_t unit_loads = 0, stream_next = 0;
     bool ok = true;
     for (long long i = i0; i < i1 && ok; i += istep) {
-      const FwdItem it = fwd_decode(p, i);
-      if (!it.validA) continue;  // past the unit's length: no role touches it
+      const FwdItem it = fwd_decode<kVarlen>(p, i);
+      if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
       if (p.resident && it.unit != prev_unit) {
         ++unit_loads;
         prev_unit = it.unit;
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (x == 1 && !it.validB) continue;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
       const int pos = mytok0 + tok;
-      const bool row_ok = (r < p.rows) && (pos < it.L);
+      const bool row_ok = (r < p.rows) && (pos < (kVarlen ? it.L : p.L));
       float m_used = -INFINITY, l = 0.f;
       for (int bi = 0; bi < nb; ++bi) {
         const int kb = it.kb_lo + bi;
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int tg = sm.rowtg[rt];
           const int gg = tg & 0xFF;
           const int ps = mytok0 + (tg >> 8);
-          if (rt < p.rows && ps < it.L) {
+          if (rt < p.rows && ps < (kVarlen ? it.L : p.L)) {
             const long long t_idx = p.is_time ? ps : it.fixed;
             const long long s_idx = p.is_time ? it.fixed : ps;
             const long long row =
