@@ -82,6 +82,8 @@ def library():
             lib.od_space_attn_bwd_static_ws.restype = I
             lib.od_attn_bwd_workspace_bytes.argtypes = [I] * 7
             lib.od_attn_bwd_workspace_bytes.restype = Z
+            lib.od_selftest_expired_wait.argtypes = [P]
+            lib.od_selftest_expired_wait.restype = I
             lib.od_get_device_status.argtypes = [P]
             lib.od_get_device_status.restype = I
             lib.od_get_device_status_detail.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
@@ -413,6 +415,13 @@ def time_attn_decode(q, k_new, v_new, k_cache, v_cache, t, scale=None, out=None,
     if st:
         raise ODError(st, "od_time_attn_decode")
     return o, l
+
+
+def selftest_expired_wait(stream=None) -> None:
+    """Enqueue the failure-path self-test (a bounded wait that runs out after ~2 s)."""
+    st = library().od_selftest_expired_wait(_stream(stream))
+    if st:
+        raise ODError(st, "od_selftest_expired_wait")
 
 
 def get_device_status(stream=None) -> int:

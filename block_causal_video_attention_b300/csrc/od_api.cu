@@ -21,6 +21,23 @@
 // expired; [1] holds the first such wait's site word (site << 24 | parity << 23 | block).
 __device__ unsigned int g_od_status[2];
 
+namespace od {
+// Exercises the failure path of the bounded waits: one warp waits on an mbarrier that nothing
+// ever arrives on, gives up after the wait limit, records the timeout (site 120) and returns.
+constexpr int kSelftestSite = 120;
+__global__ void od_selftest_wait_kernel(unsigned int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ Ctl ctl;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    ctl.abort = 0;
+  }
+  __syncthreads();
+  (void)wait_bar(&bar, 0u, &ctl, status, kSelftestSite);
+}
+}  // namespace od
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -598,6 +615,14 @@ od_status od_space_attn_bwd_varlen(const void* q, const void* k, const void* v, 
   if (!seqlen || !aligned16(seqlen)) return OD_ERR_INVALID_ARG;
   return launch_bwd(0, q, k, v, o, o_lo, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S,
                     Hq, Hkv, D, agent_idx, 1, scale, workspace, workspace_bytes, stream, 0, seqlen);
+}
+
+od_status od_selftest_expired_wait(void* stream) {
+  DeviceState* dev = nullptr;
+  od_status st = device_state(&dev);
+  if (st != OD_OK) return st;
+  od::od_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status);
+  return cudaGetLastError() == cudaSuccess ? OD_OK : OD_ERR_CUDA;
 }
 
 od_status od_get_device_status_detail(void* stream, unsigned int* site_word) {

@@ -215,6 +215,13 @@ od_status od_get_device_status(void* stream);
  * kernel, bit 23 the phase parity waited for, bits 22-0 the CTA index.  For diagnosis. */
 od_status od_get_device_status_detail(void* stream, unsigned int* site_word);
 
+/* Self-test of the device-side failure path: enqueues one warp that waits on a barrier
+ * nothing will complete.  The wait gives up after the library's wait limit (2 s), records a
+ * timeout with site 120 and returns, so that the next od_get_device_status reports
+ * OD_ERR_TIMEOUT while the context stays usable.  No fault, trap or unbounded wait is
+ * involved.  For tests of error handling only. */
+od_status od_selftest_expired_wait(void* stream);
+
 /* Static description of a status code. */
 const char* od_status_string(od_status s);
 

@@ -22,7 +22,7 @@ def test_every_declared_symbol_is_exported(lib):
             "od_attn_bwd_workspace_bytes", "od_get_device_status", "od_get_device_status_detail",
             "od_status_string", "od_space_attn_bwd_static_ws", "od_time_attn_decode",
             "od_space_attn_fwd_packed", "od_time_attn_fwd_packed", "od_space_attn_bwd_packed",
-            "od_time_attn_bwd_packed", "od_space_attn_fwd_varlen", "od_space_attn_bwd_varlen",
+            "od_time_attn_bwd_packed", "od_space_attn_fwd_varlen", "od_space_attn_bwd_varlen", "od_selftest_expired_wait",
             "od_version"} <= declared
     for name in declared:
         assert hasattr(lib, name), name
