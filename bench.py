@@ -71,13 +71,13 @@ def bwd_bytes(w):
 # --metrics dram__bytes_read.sum,dram__bytes_write.sum (summary in profiles/).  They hold only
 # for the kernel sources they were measured on: any change to those sources voids them.
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "35e77ff810e8342725e3640f489d60df06c7ea9c2d26bf3b408628b7169929f6",
+    "csrc_sha256": "d24ac3a803e215ec7a737f5956c88c4d2dcf319f3c91715c7312e0993ec84b9b",
     "minecraft_fwd_bwd": {
         # forward with the O residual; backward: Delta from O + O_lo, dQ, dK/dV
-        "space_fwd": 927417856,
-        "time_fwd": 924072960,
-        "space_bwd": 2883421184,
-        "time_bwd": 2898779904,
+        "space_fwd": 927340032,
+        "time_fwd": 924028160,
+        "space_bwd": 2883450624,
+        "time_bwd": 2898101760,
     },
     # decode: 4-rollout capture (176.43 MB read, 5.53 MB written) scaled by the units (x4)
     "minecraft_decode": {"decode": 727837696},
