@@ -199,12 +199,25 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
     return st;
 
   const long long grid = p.nitems < dev->num_sms ? p.nitems : dev->num_sms;
+  // fixed-length calls write O (and O_lo) by TMA store: one box per tile half (32 columns x
+  // the tile's rows), 64-byte swizzle
+  CUtensorMap to = tq, tlo = tq;
+  p.tma_out = p.seqlen ? 0 : 1;
+  if (p.tma_out) {
+    const uint32_t obox_space[5] = {32, (uint32_t)p.G, (uint32_t)p.nTok, 1, 1};
+    const uint32_t obox_time[5] = {32, (uint32_t)p.G, 1, (uint32_t)p.nTok, 1};
+    const uint32_t* obox = is_time ? obox_time : obox_space;
+    if ((st = make_map(&to, o, bf, 2, B, T, S, Hq, D, obox, CU_TENSOR_MAP_SWIZZLE_64B, Hq)))
+      return st;
+    if (o_lo && (st = make_map(&tlo, o_lo, bf, 2, B, T, S, Hq, D, obox, CU_TENSOR_MAP_SWIZZLE_64B, Hq)))
+      return st;
+  }
   if (p.seqlen)
     od::od_attn_fwd_kernel<true><<<(unsigned)grid, od::kFwdThreads, od::kFwdSmemBytes,
-                                   static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, p);
+                                   static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, tlo, p);
   else
     od::od_attn_fwd_kernel<false><<<(unsigned)grid, od::kFwdThreads, od::kFwdSmemBytes,
-                                    static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, p);
+                                    static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, tlo, p);
   return cudaGetLastError() == cudaSuccess ? OD_OK : OD_ERR_CUDA;
 }
 

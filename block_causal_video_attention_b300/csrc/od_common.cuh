@@ -58,6 +58,7 @@ struct FwdParams {
   const int* seqlen;
   __nv_bfloat16* o;
   __nv_bfloat16* o_lo;   // optional: O - bf16(O), rounded to bf16 (for the backward's Delta)
+  int tma_out;           // forward: O (and O_lo) leave by TMA store of staged tile halves
   float* lse;
   unsigned int* status;
 };

@@ -51,7 +51,7 @@
 namespace od {
 
 constexpr int kFwdBN = 64;                    // keys per key block
-constexpr int kFwdStages = 6;                 // K/V shared-memory stages
+constexpr int kFwdStages = 5;                 // K/V shared-memory stages
 constexpr int kFwdKVTile = kFwdBN * 128;      // bytes of one K or V stage
 constexpr int kFwdThreads = 640;
 constexpr int kFwdLaunchRegs = 96;
@@ -72,6 +72,9 @@ struct FwdSmem {
   // barrier outstanding: receiving scores j implies P V j-2 has completed)
   uint64_t s_full[2], s_taken[2], p_full[2], ml_ready[2];
   uint64_t o_done[2][2];
+  // per tile and half (4 warps): output rows staged for the TMA stores; staging free again
+  // (the previous stores have read it)
+  uint64_t st_full[2][2], st_free[2][2];
   uint64_t drain[2];
   uint32_t tmem_base;
   Ctl ctl;
@@ -80,8 +83,8 @@ struct FwdSmem {
   float2 ml[2][2][128];         // per tile, half, row: (running max, row sum)
 };
 // dynamic smem: [Q: tile A slots 0 1, tile B slots 0 1][K stages][V stages]
-//               [O staging, 2 KB per softmax warp][FwdSmem]
-constexpr size_t kFwdStageBytes = 16 * 2048;
+//               [O staging, 2 KB per softmax warp][O residual staging, likewise][FwdSmem]
+constexpr size_t kFwdStageBytes = 2 * 16 * 2048;
 constexpr size_t kFwdTileBytes =
     size_t(4) * kTile + size_t(2 * kFwdStages) * kFwdKVTile + kFwdStageBytes;
 constexpr size_t kFwdSmemBytes = kFwdTileBytes + 1024 + sizeof(FwdSmem) + 64;
@@ -96,7 +99,9 @@ template <bool kVarlen>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     od_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_o,
+                       const __grid_constant__ CUtensorMap tm_lo, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -104,6 +109,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint8_t* sK = base + 4 * kTile;
   uint8_t* sV = sK + kFwdStages * kFwdKVTile;
   uint8_t* sOst = sV + kFwdStages * kFwdKVTile;
+  uint8_t* sLst = sOst + 16 * 2048;
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(base + kFwdTileBytes);
 
   const int tid = threadIdx.x;
@@ -140,6 +146,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&sm.p_full[x], 8);
       mbar_init(&sm.ml_ready[x], 8);
       mbar_init(&sm.drain[x], 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(&sm.st_full[x][h], 4);
+        mbar_init(&sm.st_free[x][h], 1);
+      }
     }
     for (int s = 0; s < kFwdStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
@@ -444,7 +454,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int G = p.G;
     const int tok = r / G;
     const int g = r - tok * G;
-    uint32_t jS = 0, jP = 0, jM = 0;
+    uint32_t jS = 0, jP = 0, jM = 0, jE = 0;
     long long prev_unit = -1;
     uint32_t unit_loads = 0, stream_next = 0;
     bool ok = true;
@@ -606,12 +616,73 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         p.lse[((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + hq] =
             (M + log2f(lsum)) * 0.69314718055994531f;
       }
-      // This half writes output columns [32 hf, 32 hf + 32): each warp stages its 32 rows
-      // (64 bytes each, 16-byte chunks XOR-swizzled by row) and stores them coalesced.  When
-      // requested, the residual O - bf16(O) (rounded to bf16) follows through the same
-      // staging buffer; it is kept in registers meanwhile.
-      uint8_t* stg = sOst + warp * 2048;
       const uint32_t tOa = tX + 128u + 32u * hf, tOb = tOa + 64u;
+      if (!kVarlen && p.tma_out) {
+        // This half's columns [32 hf, 32 hf + 32) of the tile's rows r = tok * G + g leave by
+        // TMA store: the 4 warps of the half stage their rows (64 bytes each, 16-byte chunk c
+        // of row r at c ^ ((r >> 1) & 3): the 64-byte TMA swizzle) in the half's 8 KB block,
+        // bf16(O) and the residual O - bf16(O) side by side, and the half's first warp stores
+        // each block as one box once all 4 warps have arrived.  Rows past the sequence fall
+        // outside the tensor and are not written.  The staging is reused one item later,
+        // after the issuing thread has seen the stores read it.
+        if (jE > 0) {
+          if ((warp & 3) == 0 && lane == 0) {
+            bulk_wait_read0();
+            mbar_arrive(&sm.st_free[x][hf]);
+          }
+          ok = __all_sync(0xffffffffu, wait_bar(&sm.st_free[x][hf], (jE - 1) & 1u, ctl, status, 21));
+          if (!ok) break;
+        }
+        uint8_t* so = sOst + warp * 2048;
+        uint8_t* sl = sLst + warp * 2048;
+        const int swz = (lane >> 1) & 3;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          float oa[16], ob[16];
+          tmem_ld16(tOa + 16 * c2, oa);
+          tmem_ld16(tOb + 16 * c2, ob);
+          tmem_wait_ld_dep16(oa);
+          tmem_wait_ld_dep16(ob);
+          uint32_t w[8], wl[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float2 y = __ffma2_rn(make_float2(oa[2 * j], oa[2 * j + 1]), make_float2(wa, wa),
+                                        __fmul2_rn(make_float2(ob[2 * j], ob[2 * j + 1]), make_float2(wb, wb)));
+            w[j] = split_bf16x2(y.x, y.y, &wl[j]);
+          }
+          *reinterpret_cast<uint4*>(so + lane * 64 + (((2 * c2) ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(so + lane * 64 + (((2 * c2 + 1) ^ swz) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+          if (p.o_lo) {
+            *reinterpret_cast<uint4*>(sl + lane * 64 + (((2 * c2) ^ swz) << 4)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            *reinterpret_cast<uint4*>(sl + lane * 64 + (((2 * c2 + 1) ^ swz) << 4)) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+          }
+        }
+        fence_proxy_async_smem();  // the staged rows, visible to the TMA stores
+        __syncwarp();
+        OD_TP(34, (int)i, 0);
+        if (lane == 0) mbar_arrive(&sm.st_full[x][hf]);
+        if ((warp & 3) == 0) {
+          ok = __all_sync(0xffffffffu, wait_bar(&sm.st_full[x][hf], jE & 1u, ctl, status, 22));
+          if (!ok) break;
+          if (lane == 0) {
+            const int c1 = it.kvh * G;
+            const int c2s = p.is_time ? it.fixed : mytok0, c3t = p.is_time ? mytok0 : it.fixed;
+            tma_store_5d(&tm_o, sOst + warp * 2048, 32 * hf, c1, c2s, c3t, it.b);
+            if (p.o_lo) tma_store_5d(&tm_lo, sLst + warp * 2048, 32 * hf, c1, c2s, c3t, it.b);
+            bulk_commit();
+          }
+          __syncwarp();
+        }
+        ++jE;
+        OD_TP(31, (int)i, 0);
+        continue;
+      }
+      // Generic stores (variable-length blocks, whose padding rows must stay untouched, or when
+      // the host chose them): this half writes output columns [32 hf, 32 hf + 32); each warp
+      // stages its 32 rows (64 bytes each, 16-byte chunks XOR-swizzled by row) and stores them
+      // coalesced.  When requested, the residual O - bf16(O) (rounded to bf16) follows through
+      // the same staging buffer; it is kept in registers meanwhile.
+      uint8_t* stg = sOst + warp * 2048;
       uint32_t wl[2][8];
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
@@ -672,6 +743,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   }
 
+  // output stores issued by this thread: complete before the CTA's shared memory goes
+  if (!kVarlen && p.tma_out && warp < 16 && (warp & 3) == 0 && lane == 0) bulk_wait0();
   __syncwarp();
   tc_fence_before();
   __syncthreads();
