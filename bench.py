@@ -71,13 +71,13 @@ def bwd_bytes(w):
 # --metrics dram__bytes_read.sum,dram__bytes_write.sum (summary in profiles/).  They hold only
 # for the kernel sources they were measured on: any change to those sources voids them.
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "d24ac3a803e215ec7a737f5956c88c4d2dcf319f3c91715c7312e0993ec84b9b",
+    "csrc_sha256": "4abfe484a1de6fd79952b5dcbfb66e712f9295f68266f8949b1d9a949f12a0c5",
     "minecraft_fwd_bwd": {
         # forward with the O residual; backward: Delta from O + O_lo, dQ, dK/dV
-        "space_fwd": 927340032,
-        "time_fwd": 924028160,
-        "space_bwd": 2883450624,
-        "time_bwd": 2898101760,
+        "space_fwd": 927212800,
+        "time_fwd": 924575744,
+        "space_bwd": 2883645440,
+        "time_bwd": 2897797888,
     },
     # decode: 4-rollout capture (176.43 MB read, 5.53 MB written) scaled by the units (x4)
     "minecraft_decode": {"decode": 727837696},
