@@ -12,8 +12,8 @@
 // which in the [B,T,S,H,D] layout is one 5-D TMA box (64, G, nTok) -- rows r = tok*G + g.
 // K/V of a unit are loaded once per CTA visit and reused by all G heads and all Q tiles.
 //
-// One persistent CTA per SM walks a contiguous range of work items; an item is
-// (unit, pair of Q tiles A and B).  Keys come in blocks of 64.  Every score row is split
+// One persistent CTA per SM walks a contiguous range of work items (every gridDim.x-th item
+// for variable-length blocks); an item is (unit, pair of Q tiles A and B).  Keys come in blocks of 64.  Every score row is split
 // between two threads: one takes columns 0-31 of each block ("half a"), the other columns
 // 32-63 ("half b").  Each half keeps its own running maximum, its own row sum and its own
 // output accumulator (O_a, O_b in TMEM), so the halves never synchronise per block; at the
@@ -44,7 +44,9 @@
 // fully masked for the whole item are never loaded; partial blocks are masked per element.
 // Online softmax with a lazy rescale: a half's running maximum only moves when a block's
 // maximum exceeds it by more than 8 (log2 units); that half's O is then rescaled in TMEM.
-// Statistics are fp32; LSE (natural log) and O are written from registers.
+// Statistics are fp32; LSE (natural log) is written from registers; O (and, on request, its
+// rounding residual) leaves by TMA store of the tile halves staged in shared memory, or by
+// per-thread stores for variable-length blocks, whose padding rows must stay untouched.
 #pragma once
 #include "od_common.cuh"
 
