@@ -36,7 +36,7 @@ def test_minecraft_step_flops():
     f = bench.flops(w)
     # 290 x 290 pairs minus the 289 world rows that may not read the agent, per (t, head)
     assert bench.pairs_space(w) == (290 * 290 - 289) * 256 * 30
-    # the first 191 steps see t + 1 keys, the remaining 65 see 192
+    # steps t = 0..191 see t + 1 keys, the remaining 64 steps see 192
     assert bench.pairs_time(w) == (sum(range(1, 193)) + 64 * 192) * 290 * 30
     assert abs(sum(f.values()) - 816.94384128e9) < 1.0   # GFLOP per bench step
 
