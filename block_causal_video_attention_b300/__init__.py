@@ -14,7 +14,7 @@ from __future__ import annotations
 _API = (
     "space_attn_fwd", "space_attn_bwd", "time_attn_fwd", "time_attn_bwd", "time_attn_decode",
     "space_attn_fwd_packed", "time_attn_fwd_packed", "space_attn_bwd_packed", "time_attn_bwd_packed",
-    "space_attn_fwd_varlen", "space_attn_bwd_varlen",
+    "space_attn_fwd_varlen", "space_attn_bwd_varlen", "selftest_expired_wait",
     "bwd_workspace_bytes", "get_device_status", "get_device_status_detail", "library", "library_path",
     "ODError", "EXPORTED_SYMBOLS",
 )

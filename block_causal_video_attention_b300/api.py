@@ -4,6 +4,14 @@ Tensors are torch CUDA tensors: Q, O, dO, dQ [B,T,S,Hq,D] bf16; K, V, dK, dV
 [B,T,S,Hkv,D] bf16; LSE [B,T,S,Hq] fp32.  Every call enqueues on the current torch
 stream (or the `stream` given) and returns without synchronising.  All computation
 happens in the CUDA library; there is no other implementation to fall back to.
+
+    space_attn_fwd / time_attn_fwd            O, LSE (and O's residual with o_lo=True)
+    space_attn_bwd / time_attn_bwd            dQ, dK, dV (fp32 copies with fp32_grads=True)
+    *_fwd_packed / *_bwd_packed               Q, K, V from one [B,T,S,Hq+2Hkv,D] tensor
+    space_attn_fwd_varlen / _bwd_varlen       per-timestep-block lengths (padded layout)
+    time_attn_decode                          one rollout step over a ring-buffer KV cache
+    get_device_status[_detail]                device-side timeouts since the last read
+    selftest_expired_wait                     exercises the timeout path (no fault)
 """
 from __future__ import annotations
 

@@ -37,9 +37,13 @@ def _worker(rank, world, port, results):
         ran = None
         if rank != 0:
             class A:
-                steps, warmup, ref_units = 1, 0, 1
+                steps, warmup, ref_units, impl = 1, 0, 1, "reference"
+            from block_causal_video_attention_b300 import synth
             with contextlib.redirect_stdout(out):
                 ran = bench.run_reference(A, None, False)
+                # the decode and variable-length reference arms likewise
+                assert bench.run_decode(A, synth.WORKLOADS["minecraft_decode"]) is None
+                assert bench.run_varlen(A, synth.WORKLOADS["tokenizer_enc"]) is None
         dist.barrier()
         results[rank] = (slowest, value, out.getvalue(), ran)
     finally:
