@@ -1,5 +1,6 @@
 """fp64 CPU oracle for masked space attention and windowed causal time attention
-(training forward/backward and the rollout decode step).
+(training forward/backward, the rollout decode step, and space attention over
+variable-length timestep blocks as per-block calls of the fixed-length operator).
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's CPU
 baseline may import this package; the CUDA library never calls it, and it shares
