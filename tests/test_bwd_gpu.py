@@ -155,3 +155,23 @@ def test_backward_operands_far_from_unit_range(oracle_mod, kind):
         assert np.isfinite(g).all() and np.isfinite(gb).all()
         assert_close(g / f, r / f, "scaled %s %s fp32" % (kind, name), bf16_out=False)
         assert_close(gb / f, r / f, "scaled %s %s bf16" % (kind, name), mean_rel=3e-3)
+
+
+@pytest.mark.parametrize("with_lo", [False, True])
+def test_backward_is_deterministic(with_lo):
+    """No atomics anywhere in the backward: reruns give bit-identical bf16 and fp32 gradients
+    (both Delta routes)."""
+    B, T, S, Hq, Hkv, agent, window = 1, 12, 290, 30, 3, 289, 8
+    q, k, v, do = (to_dev(x) for x in inputs(B, T, S, Hq, Hkv, seed=2025, with_dout=True))
+    for kind, extra in (("space", agent), ("time", window)):
+        fwd = api.space_attn_fwd if kind == "space" else api.time_attn_fwd
+        bwd = api.space_attn_bwd if kind == "space" else api.time_attn_bwd
+        res = fwd(q, k, v, extra, 0.125, o_lo=(True if with_lo else None))
+        o, l = res[0], res[1]
+        lo = res[2] if with_lo else None
+        runs = [bwd(q, k, v, o, l, do, extra, 0.125, fp32_grads=True, o_lo=lo) for _ in range(3)]
+        torch.cuda.synchronize()
+        assert api.get_device_status() == 0
+        for r in runs[1:]:
+            for a, b in zip(runs[0][:3] + tuple(runs[0][3]), r[:3] + tuple(r[3])):
+                assert torch.equal(a, b), kind
