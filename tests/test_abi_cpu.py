@@ -150,3 +150,17 @@ def test_binding_refuses_cpu_tensors():
     k = torch.zeros(1, 2, 3, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         api.space_attn_fwd(q, k, k, agent_idx=-1)
+
+
+def test_every_operator_has_a_binding():
+    """Each operator entry point of the C ABI has a same-named Python function (without the
+    od_ prefix) exported by the package."""
+    import block_causal_video_attention_b300 as pkg
+    ops = [s for s in api.EXPORTED_SYMBOLS
+           if re.match(r"od_(space|time)_attn_(fwd|bwd|decode)", s) and not s.endswith("static_ws")]
+    assert len(ops) == 11
+    for sym in ops + ["od_selftest_expired_wait", "od_get_device_status",
+                      "od_get_device_status_detail"]:
+        name = sym[3:]
+        assert callable(getattr(api, name)), name
+        assert name in pkg.__all__, name
