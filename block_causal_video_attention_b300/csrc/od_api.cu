@@ -65,9 +65,15 @@ od_status device_state(DeviceState** out) {
     d.status = static_cast<unsigned int*>(sp);
     // The forward kernel redistributes its launch registers between warpgroups (setmaxnreg);
     // that split is only valid for the register count it was designed for.
-    for (int varlen = 0; varlen < 2; ++varlen) {
-      const void* fn = varlen ? reinterpret_cast<const void*>(od::od_attn_fwd_kernel<true>)
-                              : reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false>);
+    const void* fwd_fns[7] = {
+        reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false, od::kModeSpace, true>),
+        reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false, od::kModeSpace, false>),
+        reinterpret_cast<const void*>(od::od_attn_fwd_kernel<true, od::kModeSpace, true>),
+        reinterpret_cast<const void*>(od::od_attn_fwd_kernel<true, od::kModeSpace, false>),
+        reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false, od::kModeTime, true>),
+        reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false, od::kModeTime, false>),
+        reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false, od::kModeTimePacked, true>)};
+    for (const void* fn : fwd_fns) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(od::kFwdSmemBytes)) != cudaSuccess)
         return OD_ERR_CUDA;
@@ -159,33 +165,57 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != OD_OK) return st;
 
-  od::FwdParams p{};
+  od::AttnFwdParams p{};
   p.B = B; p.T = T; p.S = S; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv;
-  p.is_time = is_time;
+  // short time sequences: several token positions share a tile (G * T <= 64)
+  const bool packed = is_time && p.G * T <= 64;
+  p.mode = packed ? od::kModeTimePacked : (is_time ? od::kModeTime : od::kModeSpace);
   p.L = is_time ? T : S;
-  p.F = is_time ? S : T;
   p.agent = is_time ? -1 : agent;
   p.window = is_time ? window : 1;
   p.sl = scale * 1.4426950408889634f;
-  p.nTok = od::kBM / p.G;
-  p.rows = p.nTok * p.G;
-  p.ntiles = (p.L + p.nTok - 1) / p.nTok;
-  p.npairs = (p.ntiles + 1) / 2;
+  if (packed) {
+    p.pk = od::kBM / (p.G * T);
+    p.nTok = T;
+    p.rows = p.pk * T * p.G;
+    p.F = (S + 2 * p.pk - 1) / (2 * p.pk);
+    p.ntiles = 2;
+    p.npairs = 1;
+    p.nkb = 2;
+    p.kvb = p.pk * T;
+  } else {
+    p.pk = 1;
+    p.nTok = od::kBM / p.G;
+    p.rows = p.nTok * p.G;
+    p.F = is_time ? S : T;
+    p.ntiles = (p.L + p.nTok - 1) / p.nTok;
+    p.npairs = (p.ntiles + 1) / 2;
+    p.nkb = (p.L + od::kFwdBN - 1) / od::kFwdBN;
+    p.kvb = od::kFwdBN;
+  }
   p.nitems = 1LL * B * p.F * Hkv * p.npairs;
   if (p.nitems >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
   p.rcp_npairs = od::host_div_rcp(p.npairs);
   p.rcp_hkv = od::host_div_rcp(p.Hkv);
   p.rcp_f = od::host_div_rcp(p.F);
-  p.bn = od::kFwdBN;
-  p.nkb = (p.L + od::kFwdBN - 1) / od::kFwdBN;
   p.resident = p.nkb <= od::kFwdStages;
   p.lse = lse;
   p.status = dev->status;
 
-  const uint32_t qbox_space[5] = {64, (uint32_t)p.G, (uint32_t)p.nTok, 1, 1};
-  const uint32_t qbox_time[5] = {64, (uint32_t)p.G, 1, (uint32_t)p.nTok, 1};
-  const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kFwdBN, 1, 1};
-  const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kFwdBN, 1};
+  uint32_t qbox[5], kbox[5];
+  if (p.mode == od::kModeSpace) {
+    const uint32_t qb[5] = {64, (uint32_t)p.G, (uint32_t)p.nTok, 1, 1};
+    const uint32_t kb[5] = {64, 1, (uint32_t)od::kFwdBN, 1, 1};
+    for (int i = 0; i < 5; ++i) { qbox[i] = qb[i]; kbox[i] = kb[i]; }
+  } else if (p.mode == od::kModeTime) {
+    const uint32_t qb[5] = {64, (uint32_t)p.G, 1, (uint32_t)p.nTok, 1};
+    const uint32_t kb[5] = {64, 1, 1, (uint32_t)od::kFwdBN, 1};
+    for (int i = 0; i < 5; ++i) { qbox[i] = qb[i]; kbox[i] = kb[i]; }
+  } else {
+    const uint32_t qb[5] = {64, (uint32_t)p.G, (uint32_t)p.pk, (uint32_t)T, 1};
+    const uint32_t kb[5] = {64, 1, (uint32_t)p.pk, (uint32_t)T, 1};
+    for (int i = 0; i < 5; ++i) { qbox[i] = qb[i]; kbox[i] = kb[i]; }
+  }
   p.o = static_cast<__nv_bfloat16*>(o);
   p.o_lo = static_cast<__nv_bfloat16*>(o_lo);
   p.seqlen = is_time ? nullptr : seqlen;
@@ -193,31 +223,36 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int q_rows = qkv_rows ? qkv_rows : Hq, kv_rows = qkv_rows ? qkv_rows : Hkv;
-  if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, is_time ? qbox_time : qbox_space, sw, q_rows)) ||
-      (st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw, kv_rows)) ||
-      (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, is_time ? kbox_time : kbox_space, sw, kv_rows)))
+  if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, qbox, sw, q_rows)) ||
+      (st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)) ||
+      (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)))
     return st;
 
   const long long grid = p.nitems < dev->num_sms ? p.nitems : dev->num_sms;
-  // fixed-length calls write O (and O_lo) by TMA store: one box per tile half (32 columns x
-  // the tile's rows), 64-byte swizzle
+  // fixed-length calls write O (and O_lo) by TMA store of whole staged tiles (the Q tile's
+  // box over the output, 128-byte swizzle)
   CUtensorMap to = tq, tlo = tq;
   p.tma_out = p.seqlen ? 0 : 1;
   if (p.tma_out) {
-    const uint32_t obox_space[5] = {32, (uint32_t)p.G, (uint32_t)p.nTok, 1, 1};
-    const uint32_t obox_time[5] = {32, (uint32_t)p.G, 1, (uint32_t)p.nTok, 1};
-    const uint32_t* obox = is_time ? obox_time : obox_space;
-    if ((st = make_map(&to, o, bf, 2, B, T, S, Hq, D, obox, CU_TENSOR_MAP_SWIZZLE_64B, Hq)))
-      return st;
-    if (o_lo && (st = make_map(&tlo, o_lo, bf, 2, B, T, S, Hq, D, obox, CU_TENSOR_MAP_SWIZZLE_64B, Hq)))
-      return st;
+    if ((st = make_map(&to, o, bf, 2, B, T, S, Hq, D, qbox, sw, Hq))) return st;
+    if (o_lo && (st = make_map(&tlo, o_lo, bf, 2, B, T, S, Hq, D, qbox, sw, Hq))) return st;
   }
-  if (p.seqlen)
-    od::od_attn_fwd_kernel<true><<<(unsigned)grid, od::kFwdThreads, od::kFwdSmemBytes,
-                                   static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, tlo, p);
-  else
-    od::od_attn_fwd_kernel<false><<<(unsigned)grid, od::kFwdThreads, od::kFwdSmemBytes,
-                                    static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, tlo, p);
+
+  const dim3 g((unsigned)grid), blk(od::kFwdThreads);
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+#define OD_FWD_LAUNCH(V, M, R) \
+  od::od_attn_fwd_kernel<V, M, R><<<g, blk, od::kFwdSmemBytes, strm>>>(tq, tk, tv, to, tlo, p)
+  const bool res = p.resident != 0;
+  if (p.seqlen) {
+    if (res) OD_FWD_LAUNCH(true, od::kModeSpace, true); else OD_FWD_LAUNCH(true, od::kModeSpace, false);
+  } else if (p.mode == od::kModeSpace) {
+    if (res) OD_FWD_LAUNCH(false, od::kModeSpace, true); else OD_FWD_LAUNCH(false, od::kModeSpace, false);
+  } else if (p.mode == od::kModeTime) {
+    if (res) OD_FWD_LAUNCH(false, od::kModeTime, true); else OD_FWD_LAUNCH(false, od::kModeTime, false);
+  } else {
+    OD_FWD_LAUNCH(false, od::kModeTimePacked, true);  // packed units always fit (2 blocks)
+  }
+#undef OD_FWD_LAUNCH
   return cudaGetLastError() == cudaSuccess ? OD_OK : OD_ERR_CUDA;
 }
 
@@ -665,5 +700,20 @@ const char* od_status_string(od_status s) {
 }
 
 const char* od_version(void) { return "od_attn 0.1 (sm_103a)"; }
+
+#ifdef OD_TRACE
+// Profiling builds only: copies the per-warp trace regions (see od_common.cuh) into host
+// memory -- dst holds OD_TRACE_WARPS * OD_TRACE_PER_WARP records, counts OD_TRACE_WARPS
+// record counts -- and clears the counts.  Returns 0, or -1 on a CUDA error.
+int od_trace_read(unsigned long long* dst, unsigned int* counts) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(counts, g_od_trace_n, OD_TRACE_WARPS * sizeof(unsigned int)) != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(dst, g_od_trace, sizeof(unsigned long long) * OD_TRACE_WARPS * OD_TRACE_PER_WARP) != cudaSuccess)
+    return -1;
+  unsigned int zero[OD_TRACE_WARPS] = {0};
+  if (cudaMemcpyToSymbol(g_od_trace_n, zero, sizeof(zero)) != cudaSuccess) return -1;
+  return 0;
+}
+#endif
 
 }  // extern "C"

@@ -93,27 +93,30 @@ __device__ __forceinline__ void record_timeout(unsigned int* status, int site, u
             (static_cast<uint32_t>(site) << 24) | ((parity & 1u) << 23) | (blockIdx.x & 0x7FFFFFu));
 }
 
+// Out-of-line record of an expired wait (cold).
+__device__ __noinline__ void wait_expired(Ctl* ctl, unsigned int* status, int site, uint32_t parity) {
+  ctl->abort = 1;
+  record_timeout(status, site, parity);
+}
+
 // Wait until the phase with the given parity of `bar` has completed.  Returns false (and
 // leaves the CTA in abort mode) if the CTA was aborted or the wait exceeded the limit.
 __device__ __forceinline__ bool wait_bar_slow(uint32_t a, uint32_t parity, Ctl* ctl,
                                            unsigned int* status, int site) {
   const uint64_t t0 = globaltimer();
-  for (uint32_t i = 0;; ++i) {
+  while (true) {
     if (mbar_try_wait_sleep(a, parity, 20000u)) return true;
-    if ((i & 3u) == 3u) {
-      if (ctl->abort) return false;
-      if (globaltimer() - t0 > OD_WAIT_LIMIT_NS) {
-        ctl->abort = 1;
-        record_timeout(status, site, parity);
-        return false;
-      }
+    if (ctl->abort) return false;
+    if (globaltimer() - t0 > OD_WAIT_LIMIT_NS) {
+      wait_expired(ctl, status, site, parity);
+      return false;
     }
   }
 }
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl* ctl,
                                          unsigned int* status, int site) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (__builtin_expect(mbar_try_wait(a, parity), 1)) return true;
   return wait_bar_slow(a, parity, ctl, status, site);
 }
 
@@ -224,6 +227,68 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint6
       "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Groups of MMAs issued from one asm block with one elect: the operand offsets are formed
+// inside the block from one base each, so the issuing code stays short (a group costs about
+// what its MMAs cost on the tensor core).
+// D[tmem] (+)= A[smem] B[smem] over K = 64: four k-steps of 16, descriptors advanced by 32 bytes.
+__device__ __forceinline__ void mma_ss_k64_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e, t, f;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "setp.eq.u32 t, %3, %3;\n\tsetp.ne.u32 f, %3, %3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] B[smem] over K = 128: eight k-steps of 16 (A advanced by 8 columns,
+// B by 2048 bytes); the first accumulates only if `accumulate`.
+__device__ __forceinline__ void mma_ts_k128_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+      ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.u32 a4, %1, 32;\n\tadd.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\t"
+      "add.u32 a7, %1, 56;\n\t"
+      "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\t"
+      "add.s64 b4, %2, 512;\n\tadd.s64 b5, %2, 640;\n\tadd.s64 b6, %2, 768;\n\t"
+      "add.s64 b7, %2, 896;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, %3, %3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] B[smem] over K = 64: four k-steps of 16 (A advanced by 8 columns, B by
+// 2048 bytes); the first accumulates only if `accumulate`.
+__device__ __forceinline__ void mma_ts_k64_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, %3, %3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
