@@ -470,6 +470,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t tS = tmem + 256u * x, tP = tS + 128u, tO = tS + 192u;
         uint32_t nqk = 0, npv = 0, qn = 0, unit_loads = 0, stream_cnt = 0;
         int prev_unit = -1;
+        bool k_released = false;  // resident: this unit's K stages already released
         // the pending P V: on, stage, V phase parity, k-steps, accumulate
         int pon = 0, pst = 0, pks = 0;
         uint32_t pvp = 0, pacc = 0;
@@ -478,6 +479,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!__all_sync(0xffffffffu, wait_bar(&sm.p_full[x], npv & 1u, ctl, status, 10) &&
                                        wait_bar(&sm.v16_ready[pst], pvp, ctl, status, 11)))
             return false;
+          OD_TP(44 + x, 0, 0);
           tc_fence_after();
           const uint64_t bv = dv0 + static_cast<uint64_t>(pst * (kFwdKVTile >> 4));
           if (pks == 8) {
@@ -498,15 +500,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (kVarlen && !it.valid[0]) continue;  // past the unit's length: no role touches it
           if (kRes && static_cast<int>(it.unit) != prev_unit) {
             if (prev_unit >= 0) {
-              // every QK^T of the old unit is issued: its K stages go once those complete,
-              // its V stages once the last P V (still pending) does
-              for (int s2 = 0; s2 < p.nkb; ++s2) mma_commit_w(&sm.k_empty[s2]);
+              // every QK^T of the old unit is issued: its K stages go once those complete
+              // (unless already released after the unit's last QK^T), its V stages once the
+              // last P V (still pending) does
+              if (!k_released)
+                for (int s2 = 0; s2 < p.nkb; ++s2) mma_commit_w(&sm.k_empty[s2]);
               if (pon) ok = issue_pv();
               if (!ok) break;
               for (int s2 = 0; s2 < p.nkb; ++s2) mma_commit_w(&sm.v_empty[s2]);
             }
             ++unit_loads;
             prev_unit = static_cast<int>(it.unit);
+            k_released = false;
             // observe the new fills before this issuer can ever release them
             for (int s2 = 0; s2 < p.nkb && ok; ++s2)
               ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[s2], (unit_loads - 1) & 1u, ctl, status, 15) &&
@@ -546,7 +551,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mma_commit_w(&sm.s_full[x]);
             OD_TP(10 + x, i, s);
             ++nqk;
-            if (s == nb - 1) mma_commit_w(&sm.q_empty[x][qs]);
+            if (s == nb - 1) {
+              mma_commit_w(&sm.q_empty[x][qs]);
+              // resident: after the unit's last QK^T its K stages may take the next unit's
+              // keys while the last blocks' softmax and P V still run
+              // (fixed-length space calls only: there every item is processed, so the next
+              // item of this CTA tells whether the unit ends here; for time attention releasing
+              // at the unit change measured faster)
+              if (kRes && !kVarlen && kMode == kModeSpace && (i + istep >= i1 || fwd_item<kVarlen, kMode>(p, i + istep).unit != it.unit)) {
+                for (int s2 = 0; s2 < p.nkb; ++s2) mma_commit_w(&sm.k_empty[s2]);
+                k_released = true;
+              }
+            }
             // streaming: this fill's K may be reloaded once both tiles' QK^T complete
             if (!kRes) mma_commit_w(&sm.k_empty[f.stage]);
             if (pon) {
@@ -736,6 +752,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         reg_dep32(v + 32);
         reg_dep32(v + 64);
         reg_dep32(v + 96);
+        OD_TP(7, i, s);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.s_taken[x]);
@@ -771,6 +788,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           l *= alpha;
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+        OD_TP(8, i, s);
         // the V stage's scale exponent (its keys hold fp16(v * 2^e)); O is kept in the
         // scale of the item's latest block and rescaled when that changes
         const FwdSlot fs = fwd_slot<kRes>(blk, s, unit_loads, stream_cnt);
@@ -786,6 +804,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           waited = jP;
           tc_fence_after();
         }
+        OD_TP(2, i, s);
         if (__any_sync(0xffffffffu, rescale || de != 0)) {
           const float f = (rescale ? alpha : 1.f) * __int_as_float((127 + de) << 23);
 #pragma unroll 1
@@ -822,6 +841,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const float2 a = __fadd2_rn(acc0, acc1);
           l += a.x + a.y;
         }
+        OD_TP(3, i, s);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -831,13 +851,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
-      if (jP > waited) {
+      // Space attention does what does not need O first (the item's last P V is still
+      // running); for time attention waiting first measured faster.
+      constexpr bool kLateWait = kMode == kModeSpace;
+      if (!kLateWait && jP > waited) {
         ok = __all_sync(0xffffffffu, wait_bar(&sm.o_done[x], (jP - 1) & 1u, ctl, status, 23));
         if (!ok) break;
         waited = jP;
       }
-      OD_TP(5, i, 0);
-      tc_fence_after();
       const FwdItem2 it2 = fwd_item<kVarlen, kMode>(p, i);
       const int tok0x = x ? it2.tok0[1] : it2.tok0[0];
       const int spos = packed ? tok0x + spr : 0;        // packed: token position
@@ -869,35 +890,64 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!ok) break;
         }
       }
+      if (jP > waited) {
+        ok = __all_sync(0xffffffffu, wait_bar(&sm.o_done[x], (jP - 1) & 1u, ctl, status, 23));
+        if (!ok) break;
+        waited = jP;
+      }
+      OD_TP(5, i, 0);
+      tc_fence_after();
       uint8_t* so = sOst + x * kTile + r * 128;
       uint8_t* sl = sLst + x * kTile + r * 128;
       uint4* gdst = reinterpret_cast<uint4*>(p.o + (row_ok ? row : 0) * 64);
       uint4* gdlo = want_lo ? reinterpret_cast<uint4*>(p.o_lo + (row_ok ? row : 0) * 64) : nullptr;
-#pragma unroll 1
-      for (int hq2 = 0; hq2 < 4; ++hq2) {
-        uint32_t o16[16];
-        tmem_ld16(tO + 16 * hq2, reinterpret_cast<float*>(o16));
-        tmem_wait_ld();
+      // (fixed-length space attention loads the whole row at once, the other modes in
+      // quarters: each measured faster for its mode)
+      if (kMode == kModeSpace && !kVarlen) {
+        float o[64];
+        tmem_ld32(tO, o);
+        tmem_ld32(tO + 32, o + 32);
+        tmem_wait_ld_dep32(o);
+        reg_dep32(o + 32);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int chunk = 2 * hq2 + cc;
-        const uint32_t* o = o16 + 8 * cc;
-        uint32_t w[4], wl[4];
+        for (int chunk = 0; chunk < 8; ++chunk) {  // 16-byte chunk (8 columns) of the row
+          uint32_t w[4], wl[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 y = __fmul2_rn(make_float2(__uint_as_float(o[2 * j]), __uint_as_float(o[2 * j + 1])),
-                                      make_float2(inv, inv));
-          w[j] = split_bf16x2(y.x, y.y, &wl[j]);
-        }
-        if (!kVarlen) {
+          for (int j = 0; j < 4; ++j) {
+            const float2 y = __fmul2_rn(make_float2(o[8 * chunk + 2 * j], o[8 * chunk + 2 * j + 1]),
+                                        make_float2(inv, inv));
+            w[j] = split_bf16x2(y.x, y.y, &wl[j]);
+          }
           const int sc = chunk ^ (r & 7);
           *reinterpret_cast<uint4*>(so + sc * 16) = make_uint4(w[0], w[1], w[2], w[3]);
           if (want_lo) *reinterpret_cast<uint4*>(sl + sc * 16) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        } else if (row_ok) {
-          gdst[chunk] = make_uint4(w[0], w[1], w[2], w[3]);
-          if (want_lo) gdlo[chunk] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
-      }
+      } else
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t o16[16];
+        tmem_ld16(tO + 16 * q4, reinterpret_cast<float*>(o16));
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int chunk = 2 * q4 + cc;  // 16-byte chunk (8 columns) of the row
+          const uint32_t* o = o16 + 8 * cc;
+          uint32_t w[4], wl[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 y = __fmul2_rn(make_float2(__uint_as_float(o[2 * j]), __uint_as_float(o[2 * j + 1])),
+                                        make_float2(inv, inv));
+            w[j] = split_bf16x2(y.x, y.y, &wl[j]);
+          }
+          if (!kVarlen) {
+            const int sc = chunk ^ (r & 7);
+            *reinterpret_cast<uint4*>(so + sc * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (want_lo) *reinterpret_cast<uint4*>(sl + sc * 16) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          } else if (row_ok) {
+            gdst[chunk] = make_uint4(w[0], w[1], w[2], w[3]);
+            if (want_lo) gdlo[chunk] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          }
+        }
       }
       if (!kVarlen) {
         fence_proxy_async_smem();  // the staged rows, visible to the TMA stores
@@ -924,6 +974,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   }
 
+  OD_TRACE_END();
   // output stores issued by this thread: complete before the CTA's shared memory goes
   if (!kVarlen && warp < 8 && (warp & 3) == 0 && lane == 0) bulk_wait0();
   __syncwarp();
