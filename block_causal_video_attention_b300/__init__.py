@@ -16,6 +16,7 @@ _API = (
     "space_attn_fwd_packed", "time_attn_fwd_packed", "space_attn_bwd_packed", "time_attn_bwd_packed",
     "space_attn_fwd_varlen", "space_attn_bwd_varlen", "selftest_expired_wait",
     "bwd_workspace_bytes", "get_device_status", "get_device_status_detail", "library", "library_path",
+    "debug_build", "debug_library",
     "ODError", "EXPORTED_SYMBOLS",
 )
 

@@ -12,9 +12,11 @@ happens in the CUDA library; there is no other implementation to fall back to.
     time_attn_decode                          one rollout step over a ring-buffer KV cache
     get_device_status[_detail]                device-side timeouts since the last read
     selftest_expired_wait                     exercises the timeout path (no fault)
+    debug_build / debug_library               route calls to the range-checked build
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -26,15 +28,18 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_PKG)
 _LIB_PATH = os.path.join(_PKG, "libod_attn.so")
+_DEBUG_LIB_PATH = os.path.join(_PKG, "libod_attn_debug.so")
 _HEADER = os.path.join(_ROOT, "include", "od_attn.h")
 _lock = threading.Lock()
 _lib = None
+_debug_lib = None
+_override = None   # set inside debug_build(): the binding's calls go to that library
 
 # kernels one backward call launches (row statistics, main kernel, dQ conversion)
 BWD_LAUNCHES = 3
 
 STATUS = {0: "OD_OK", 1: "OD_ERR_INVALID_ARG", 2: "OD_ERR_UNSUPPORTED", 3: "OD_ERR_CUDA",
-          4: "OD_ERR_TIMEOUT", 5: "OD_ERR_WORKSPACE"}
+          4: "OD_ERR_TIMEOUT", 5: "OD_ERR_WORKSPACE", 6: "OD_ERR_RANGE"}
 
 
 class ODError(RuntimeError):
@@ -58,50 +63,84 @@ def library_path() -> str:
 
 
 def library():
-    """Load libod_attn.so (raises if it has not been built)."""
+    """Load libod_attn.so (raises if it has not been built); inside debug_build(), the
+    range-checked build instead."""
     global _lib
+    if _override is not None:
+        return _override
     with _lock:
         if _lib is None:
-            if not os.path.exists(_LIB_PATH):
-                raise ODError(3, "libod_attn.so is not built (run __graft_entry__.build())")
-            lib = ctypes.CDLL(_LIB_PATH)
-            P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-            fwd = [P] * 6 + [I] * 7 + [F, P]
-            bwd = [P] * 13 + [I] * 7 + [F, P, Z, P]
-            for name, args in (("od_space_attn_fwd", fwd), ("od_time_attn_fwd", fwd),
-                               ("od_space_attn_bwd", bwd), ("od_time_attn_bwd", bwd)):
-                fn = getattr(lib, name)
-                fn.argtypes = args
-                fn.restype = I
-            fwdp = [P] * 4 + [I] * 7 + [F, P]
-            bwdp = [P] * 9 + [I] * 7 + [F, P, Z, P]
-            for name, args in (("od_space_attn_fwd_packed", fwdp), ("od_time_attn_fwd_packed", fwdp),
-                               ("od_space_attn_bwd_packed", bwdp), ("od_time_attn_bwd_packed", bwdp)):
-                fn = getattr(lib, name)
-                fn.argtypes = args
-                fn.restype = I
-            lib.od_space_attn_fwd_varlen.argtypes = [P] * 7 + [I] * 7 + [F, P]
-            lib.od_space_attn_fwd_varlen.restype = I
-            lib.od_space_attn_bwd_varlen.argtypes = [P] * 14 + [I] * 7 + [F, P, Z, P]
-            lib.od_space_attn_bwd_varlen.restype = I
-            lib.od_time_attn_decode.argtypes = [P] * 7 + [I] * 6 + [ctypes.c_longlong, F, P]
-            lib.od_time_attn_decode.restype = I
-            lib.od_space_attn_bwd_static_ws.argtypes = [P] * 13 + [I] * 7 + [F, P]
-            lib.od_space_attn_bwd_static_ws.restype = I
-            lib.od_attn_bwd_workspace_bytes.argtypes = [I] * 7
-            lib.od_attn_bwd_workspace_bytes.restype = Z
-            lib.od_selftest_expired_wait.argtypes = [P]
-            lib.od_selftest_expired_wait.restype = I
-            lib.od_get_device_status.argtypes = [P]
-            lib.od_get_device_status.restype = I
-            lib.od_get_device_status_detail.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
-            lib.od_get_device_status_detail.restype = I
-            lib.od_status_string.argtypes = [I]
-            lib.od_status_string.restype = ctypes.c_char_p
-            lib.od_version.argtypes = []
-            lib.od_version.restype = ctypes.c_char_p
-            _lib = lib
+            _lib = _load(_LIB_PATH)
     return _lib
+
+
+def debug_library():
+    """Load libod_attn_debug.so, the build with device-side range checks (raises if it has
+    not been built).  Same calls as library(); the binding's functions use library()."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            _debug_lib = _load(_DEBUG_LIB_PATH)
+    return _debug_lib
+
+
+@contextlib.contextmanager
+def debug_build():
+    """Within the block every call of this binding goes to libod_attn_debug.so (same
+    results; device-side range checks reported as OD_ERR_RANGE by get_device_status)."""
+    global _override
+    prev = _override
+    _override = debug_library()
+    try:
+        yield _override
+    finally:
+        _override = prev
+
+
+def _load(path):
+    if not os.path.exists(path):
+        raise ODError(3, "%s is not built (run __graft_entry__.build())" % os.path.basename(path))
+    lib = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fwd = [P] * 5 + [I] * 7 + [F, P]
+    bwd = [P] * 9 + [I] * 7 + [F, P, Z, P]
+    fwd_ex = [P] * 6 + [I] * 7 + [F, P]
+    bwd_ex = [P] * 13 + [I] * 7 + [F, P, Z, P]
+    for name, args in (("od_space_attn_fwd", fwd), ("od_time_attn_fwd", fwd),
+                       ("od_space_attn_bwd", bwd), ("od_time_attn_bwd", bwd),
+                       ("od_space_attn_fwd_ex", fwd_ex), ("od_time_attn_fwd_ex", fwd_ex),
+                       ("od_space_attn_bwd_ex", bwd_ex), ("od_time_attn_bwd_ex", bwd_ex)):
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = I
+    fwdp = [P] * 4 + [I] * 7 + [F, P]
+    bwdp = [P] * 9 + [I] * 7 + [F, P, Z, P]
+    for name, args in (("od_space_attn_fwd_packed", fwdp), ("od_time_attn_fwd_packed", fwdp),
+                       ("od_space_attn_bwd_packed", bwdp), ("od_time_attn_bwd_packed", bwdp)):
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = I
+    lib.od_space_attn_fwd_varlen.argtypes = [P] * 7 + [I] * 7 + [F, P]
+    lib.od_space_attn_fwd_varlen.restype = I
+    lib.od_space_attn_bwd_varlen.argtypes = [P] * 14 + [I] * 7 + [F, P, Z, P]
+    lib.od_space_attn_bwd_varlen.restype = I
+    lib.od_time_attn_decode.argtypes = [P] * 7 + [I] * 6 + [ctypes.c_longlong, F, P]
+    lib.od_time_attn_decode.restype = I
+    lib.od_space_attn_bwd_static_ws.argtypes = [P] * 13 + [I] * 7 + [F, P]
+    lib.od_space_attn_bwd_static_ws.restype = I
+    lib.od_attn_bwd_workspace_bytes.argtypes = [I] * 7
+    lib.od_attn_bwd_workspace_bytes.restype = Z
+    lib.od_selftest_expired_wait.argtypes = [P]
+    lib.od_selftest_expired_wait.restype = I
+    lib.od_get_device_status.argtypes = [P]
+    lib.od_get_device_status.restype = I
+    lib.od_get_device_status_detail.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+    lib.od_get_device_status_detail.restype = I
+    lib.od_status_string.argtypes = [I]
+    lib.od_status_string.restype = ctypes.c_char_p
+    lib.od_version.argtypes = []
+    lib.od_version.restype = ctypes.c_char_p
+    return lib
 
 
 def _stream(stream):
@@ -153,8 +192,13 @@ def _fwd(name, q, k, v, extra, scale, out, lse, o_lo, stream):
     if l.shape != (B, T, S, Hq) or l.dtype != torch.float32 or not l.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor [B,T,S,Hq]")
     r = _residual_out(o_lo, tuple(q.shape), q.device)
-    st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(r), B, T, S,
-                                  Hq, Hkv, D, int(extra), float(scale), _stream(stream))
+    if r is None:   # the plain call; the extended one only when the residual is wanted
+        st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, T, S, Hq,
+                                      Hkv, D, int(extra), float(scale), _stream(stream))
+    else:
+        name += "_ex"
+        st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(r), B, T,
+                                      S, Hq, Hkv, D, int(extra), float(scale), _stream(stream))
     if st:
         raise ODError(st, name)
     return (o, l) if r is None else (o, l, r)
@@ -202,11 +246,18 @@ def _bwd(name, which, q, k, v, o, lse, dout, extra, scale, fp32_grads, workspace
     if o_lo is not None and (o_lo.shape != q.shape or o_lo.dtype != torch.bfloat16
                              or not o_lo.is_contiguous()):
         raise ValueError("o_lo must be a contiguous bf16 tensor shaped like q")
-    st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_lo), _ptr(lse), _ptr(dout),
-                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(f32[0]), _ptr(f32[1]),
-                                  _ptr(f32[2]), B, T, S, Hq, Hkv, D, int(extra), float(scale),
-                                  _ptr(workspace), ctypes.c_size_t(workspace.numel()),
-                                  _stream(stream))
+    if o_lo is None and not fp32_grads:   # the plain call
+        st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                      _ptr(dq), _ptr(dk), _ptr(dv), B, T, S, Hq, Hkv, D,
+                                      int(extra), float(scale), _ptr(workspace),
+                                      ctypes.c_size_t(workspace.numel()), _stream(stream))
+    else:
+        name += "_ex"
+        st = getattr(library(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_lo), _ptr(lse),
+                                      _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(f32[0]),
+                                      _ptr(f32[1]), _ptr(f32[2]), B, T, S, Hq, Hkv, D, int(extra),
+                                      float(scale), _ptr(workspace),
+                                      ctypes.c_size_t(workspace.numel()), _stream(stream))
     if st:
         raise ODError(st, name)
     if fp32_grads:

@@ -116,11 +116,13 @@ od_status check_shape(int B, int T, int S, int Hq, int Hkv, int D, float scale) 
   if (!std::isfinite(scale) || !(scale > 0.f)) return OD_ERR_INVALID_ARG;
   if (D != 64) return OD_ERR_UNSUPPORTED;
   if (Hq / Hkv > 128) return OD_ERR_UNSUPPORTED;
-  const long long rows = 1LL * B * T * S;
-  // tensor-map coordinates are 32-bit and the element count of one tensor must stay
-  // addressable with 64-bit strides below 2^40 bytes
-  if (rows * Hq * D * 2 >= (1LL << 40)) return OD_ERR_UNSUPPORTED;
+  // each dimension first (so that the product below cannot wrap), then the bytes of one Q-like
+  // tensor: tensor-map coordinates are 32-bit and the tensor must stay below 2^40 bytes
   if (B > 65535 || T > (1 << 24) || S > (1 << 24) || Hq > 65535) return OD_ERR_UNSUPPORTED;
+  const unsigned __int128 bytes = static_cast<unsigned __int128>(B) * static_cast<unsigned>(T) *
+                                  static_cast<unsigned>(S) * static_cast<unsigned>(Hq) *
+                                  static_cast<unsigned>(D) * 2u;
+  if (bytes >= (static_cast<unsigned __int128>(1) << 40)) return OD_ERR_UNSUPPORTED;
   return OD_OK;
 }
 
@@ -321,7 +323,7 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   float* amax = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                          od::bwd_delta_bytes(B, T, S, Hq));
   const int num_ctas = dev->num_sms < od::kAmaxSlots ? dev->num_sms : od::kAmaxSlots;
-  int amax_slots = 0;
+  int amax_slots = 0, dq_slots = 0;
   const uint32_t qbox_space[5] = {64, (uint32_t)f.G, (uint32_t)f.nTok, 1, 1};
   const uint32_t qbox_time[5] = {64, (uint32_t)f.G, 1, (uint32_t)f.nTok, 1};
   const uint32_t* qbox = is_time ? qbox_time : qbox_space;
@@ -350,6 +352,7 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     dp.amax = amax;
     const long long grid = f.nitems < num_ctas ? f.nitems : num_ctas;
     amax_slots = static_cast<int>(grid);
+    dq_slots = static_cast<int>(grid);
     dp.amax_slots = amax_slots;
     // 1. Delta (from O and its residual when the forward wrote it, else the Delta pass),
     // 2. dQ
@@ -358,13 +361,13 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
       d.o = static_cast<const __nv_bfloat16*>(o);
       d.o_lo = static_cast<const __nv_bfloat16*>(o_lo);
       d.dout = static_cast<const __nv_bfloat16*>(dout);
-      d.q = static_cast<const __nv_bfloat16*>(q);
       d.k = static_cast<const __nv_bfloat16*>(k);
       d.v = static_cast<const __nv_bfloat16*>(v);
       d.ntok = 1LL * B * T * S;
-      d.Hq = Hq; d.Hkv = Hkv; d.q_rows = q_rows; d.kv_rows = kv_rows;
+      d.Hq = Hq; d.Hkv = Hkv; d.kv_rows = kv_rows;
       d.delta = delta;
       d.amax = amax;
+      d.status = f.status;
       // one wave of resident CTAs: every CTA streams an equal share
       const long long dgrid = dev->delta_o_ctas;
       amax_slots = static_cast<int>(dgrid);
@@ -405,6 +408,7 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     kp.dv_f32 = dv_f32;
     kp.amax = amax;
     kp.amax_slots = amax_slots;
+    kp.dq_slots = dq_slots;
     const long long grid = kp.nitems < num_ctas ? kp.nitems : num_ctas;
     if (f.seqlen)
       od::od_bwd_dkdv_kernel<true><<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
@@ -427,7 +431,10 @@ od_status launch_decode(const void* q, const void* k_new, const void* v_new, voi
   if (st != OD_OK) return st;
   if (Hq / Hkv > 16) return OD_ERR_UNSUPPORTED;
   // cache coordinates (frames x positions x heads) and the unit count stay 32-bit
-  if (1LL * B * window * S * Hkv * D * 2 >= (1LL << 40) || window > (1 << 24) ||
+  if (window > (1 << 24)) return OD_ERR_UNSUPPORTED;
+  if (static_cast<unsigned __int128>(B) * static_cast<unsigned>(window) * static_cast<unsigned>(S) *
+              static_cast<unsigned>(Hkv) * static_cast<unsigned>(D) * 2u >=
+          (static_cast<unsigned __int128>(1) << 40) ||
       1LL * B * S * Hkv >= (1LL << 31))
     return OD_ERR_UNSUPPORTED;
   DeviceState* dev = nullptr;
@@ -521,16 +528,28 @@ od_status od_space_attn_bwd_static_ws(const void* q, const void* k, const void* 
 }
 
 
-od_status od_space_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                            void* o_lo, int B, int T, int S, int Hq, int Hkv, int D,
-                            int agent_idx, float scale, void* stream) {
+od_status od_space_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                               void* o_lo, int B, int T, int S, int Hq, int Hkv, int D,
+                               int agent_idx, float scale, void* stream) {
   return launch_fwd(0, q, k, v, o, lse, o_lo, B, T, S, Hq, Hkv, D, agent_idx, 1, scale, stream);
 }
 
-od_status od_time_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                           void* o_lo, int B, int T, int S, int Hq, int Hkv, int D, int window,
-                           float scale, void* stream) {
+od_status od_time_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                              void* o_lo, int B, int T, int S, int Hq, int Hkv, int D, int window,
+                              float scale, void* stream) {
   return launch_fwd(1, q, k, v, o, lse, o_lo, B, T, S, Hq, Hkv, D, -1, window, scale, stream);
+}
+
+od_status od_space_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                            float scale, void* stream) {
+  return launch_fwd(0, q, k, v, o, lse, nullptr, B, T, S, Hq, Hkv, D, agent_idx, 1, scale, stream);
+}
+
+od_status od_time_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
+                           void* stream) {
+  return launch_fwd(1, q, k, v, o, lse, nullptr, B, T, S, Hq, Hkv, D, -1, window, scale, stream);
 }
 
 size_t od_attn_bwd_workspace_bytes(int which, int B, int T, int S, int Hq, int Hkv, int D) {
@@ -538,22 +557,38 @@ size_t od_attn_bwd_workspace_bytes(int which, int B, int T, int S, int Hq, int H
   return od::bwd_workspace_bytes(B, T, S, Hq, D);
 }
 
-od_status od_space_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                            const void* o_lo, const float* lse, const void* dout, void* dq,
-                            void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
-                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
-                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
+od_status od_space_attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                               const void* o_lo, const float* lse, const void* dout, void* dq,
+                               void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                               int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                               float scale, void* workspace, size_t workspace_bytes, void* stream) {
   return launch_bwd(0, q, k, v, o, o_lo, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
                     Hkv, D, agent_idx, 1, scale, workspace, workspace_bytes, stream);
 }
 
-od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                           const void* o_lo, const float* lse, const void* dout, void* dq,
-                           void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
-                           int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
-                           void* workspace, size_t workspace_bytes, void* stream) {
+od_status od_time_attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                              const void* o_lo, const float* lse, const void* dout, void* dq,
+                              void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                              int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
+                              void* workspace, size_t workspace_bytes, void* stream) {
   return launch_bwd(1, q, k, v, o, o_lo, lse, dout, dq, dk, dv, dq_f32, dk_f32, dv_f32, B, T, S, Hq,
                     Hkv, D, -1, window, scale, workspace, workspace_bytes, stream);
+}
+
+od_status od_space_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return launch_bwd(0, q, k, v, o, nullptr, lse, dout, dq, dk, dv, nullptr, nullptr, nullptr, B, T,
+                    S, Hq, Hkv, D, agent_idx, 1, scale, workspace, workspace_bytes, stream);
+}
+
+od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                           int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  return launch_bwd(1, q, k, v, o, nullptr, lse, dout, dq, dk, dv, nullptr, nullptr, nullptr, B, T,
+                    S, Hq, Hkv, D, -1, window, scale, workspace, workspace_bytes, stream);
 }
 
 od_status od_time_attn_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,
@@ -570,8 +605,13 @@ static od_status packed_views(const void* qkv, int B, int T, int S, int Hq, int 
   if (!qkv || B <= 0 || T <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0)
     return OD_ERR_INVALID_ARG;
   if (D != 64) return OD_ERR_UNSUPPORTED;
+  if (B > 65535 || T > (1 << 24) || S > (1 << 24) || Hq > 65535 || Hkv > 65535)
+    return OD_ERR_UNSUPPORTED;
   *rows = Hq + 2 * Hkv;
-  if (1LL * B * T * S * (*rows) * D * 2 >= (1LL << 40)) return OD_ERR_UNSUPPORTED;
+  if (static_cast<unsigned __int128>(B) * static_cast<unsigned>(T) * static_cast<unsigned>(S) *
+          static_cast<unsigned>(*rows) * static_cast<unsigned>(D) * 2u >=
+      (static_cast<unsigned __int128>(1) << 40))
+    return OD_ERR_UNSUPPORTED;
   const uint8_t* base = static_cast<const uint8_t*>(qkv);
   *q = base;
   *k = base + static_cast<size_t>(Hq) * D * 2;
@@ -682,6 +722,7 @@ od_status od_get_device_status_detail(void* stream, unsigned int* site_word) {
     if (cudaMemcpyToSymbol(g_od_status, zero, sizeof(zero)) != cudaSuccess) return OD_ERR_CUDA;
   }
   if (site_word) *site_word = v[1];
+  if (v[0] & OD_DEV_RANGE) return OD_ERR_RANGE;
   return (v[0] & OD_DEV_TIMEOUT) ? OD_ERR_TIMEOUT : OD_OK;
 }
 
@@ -695,11 +736,16 @@ const char* od_status_string(od_status s) {
     case OD_ERR_CUDA: return "CUDA error";
     case OD_ERR_TIMEOUT: return "device-side wait timed out";
     case OD_ERR_WORKSPACE: return "workspace too small";
+    case OD_ERR_RANGE: return "device-side range check failed (debug build)";
   }
   return "unknown status";
 }
 
+#ifdef OD_DEBUG
+const char* od_version(void) { return "od_attn 0.1 (sm_103a, debug: device-side range checks)"; }
+#else
 const char* od_version(void) { return "od_attn 0.1 (sm_103a)"; }
+#endif
 
 #ifdef OD_TRACE
 // Profiling builds only: copies the per-warp trace regions (see od_common.cuh) into host

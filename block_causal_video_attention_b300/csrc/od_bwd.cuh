@@ -36,13 +36,23 @@ constexpr int kBN = 96;
 constexpr int kKVTile = kBN * 128;  // bytes of one K or V stage
 
 // ---------------------------------------------------------------- fp16 operand scaling
-// The dK/dV products run on fp16 operands scaled by powers of two: every bf16 input value
-// is exactly representable in fp16 once the tensor's largest magnitude is brought just
-// below 2^15 (only values 2^25 times smaller than that largest one lose bits as fp16
-// subnormals), and power-of-two scales cancel exactly after accumulation.  The first kernel
-// records max|Q|, max|K|, max|V|, max|dO| per CTA (kAmaxSlots slots of 4 floats after the
-// Delta array in the workspace); the dK/dV kernel reduces the slots and derives the scales.
+// The dQ and dK/dV products run on fp16 operands scaled by powers of two: every bf16 input
+// value is exactly representable in fp16 once the tensor's (or Q tile's) largest magnitude is
+// brought just below 2^15 (only values 2^25 times smaller than that largest one lose bits as
+// fp16 subnormals), and power-of-two scales cancel exactly after accumulation.
+// dS = P (dP - Delta) is a product whose range is not bounded by any one input's, so its
+// scale is chosen per query row in the dQ pass and per key in the dK/dV kernel, from
+//   |dS_ij| <= P_ij (|<dO_i, v_j>| + |Delta_i|) <= ||dO_i|| ||v_j|| + |Delta_i|
+// with the row's own ||dO_i|| and Delta_i (dQ: ||v_j|| <= 8 max|V|) or the key's own ||v_j||
+// (dK: ||dO_i|| <= 8 max|dO|, |Delta_i| <= max|Delta|).  A single large element of V or dO
+// then lowers the scale only of the rows or keys it can reach.
+// Operand ranges live in kAmaxSlots slots of kAmaxStride floats after the Delta array in the
+// workspace, one slot per CTA of the launch that wrote it: the Delta launch (Delta pass or
+// Delta from O) writes max|K|, max|V|, max|dO|, max|Delta|; the dQ pass writes max|Q| (it
+// scales each Q tile by the tile's own range and records the maximum for the dK/dV kernel).
 constexpr int kAmaxSlots = 1024;
+constexpr int kAmaxStride = 8;
+constexpr int kAmK = 0, kAmV = 1, kAmDo = 2, kAmDelta = 3, kAmQ = 4;
 
 // Running max of |x| over packed bf16 pairs, kept per 16-bit half as bf16 bit patterns
 // (non-negative bf16 patterns order like their values; NaN sorts above infinity).
@@ -79,6 +89,42 @@ __device__ __forceinline__ int fp16_shift(float a) {
   return ok ? min(max(15 - E, -60), 60) : 0;
 }
 
+// Max over `nslots` operand-range slots of field `f` (whole warp; every lane gets the
+// result).  NaN propagates (fmaxf alone would drop it), so that no scaling is applied.
+__device__ __forceinline__ float slots_max(const float* amax, int nslots, int f, int lane) {
+  float a = 0.f;
+  bool bad = false;
+  for (int sl = lane; sl < nslots; sl += 32) {
+    const float v = amax[kAmaxStride * sl + f];
+    a = fmaxf(a, v);
+    bad |= !(v == v);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  }
+  return bad ? __int_as_float(0x7fc00000) : a;
+}
+// Squared Euclidean norm of 64-element bf16 row `row` of a 128-byte-swizzled tile.  Chunk c
+// is read at position c ^ (row & 7), so that lanes on 8 consecutive rows hit 8 different
+// bank groups (the sum does not depend on the order).
+__device__ __forceinline__ float row_norm2(const uint8_t* tile, int row) {
+  const uint4* src = reinterpret_cast<const uint4*>(tile + row * 128);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 d = src[c ^ (row & 7)];
+    const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float2 f = make_float2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
+      acc = __ffma2_rn(f, f, acc);
+    }
+  }
+  return acc.x + acc.y;
+}
+
 // Rewrite `bytes` of packed bf16 pairs as fp16 pairs times 2^e, in place (one warp).
 __device__ __forceinline__ void to_fp16_scaled(uint8_t* buf, int bytes, float s, int lane) {
   uint4* p = reinterpret_cast<uint4*>(buf);
@@ -109,8 +155,9 @@ struct DqParams {
   FwdParams f;            // shapes and item schedule (f.o unused)
   const float* lse;       // forward logsumexp (natural log)
   float* delta;           // Delta per query row (written by the Delta pass, read otherwise)
-  float* amax;            // Delta pass: this CTA's max|Q|, max|K|, max|V|, max|dO| at 4*blockIdx.x
-  int amax_slots;         // dQ pass: slots the Delta pass wrote (scales for the fp16 products)
+  float* amax;            // operand-range slots: the Delta pass writes its CTA's max|K|, max|V|,
+                          // max|dO|, max|Delta|; the dQ pass its CTA's max|Q|
+  int amax_slots;         // dQ pass: slots the Delta launch wrote (scales for the fp16 products)
   float scale;
   __nv_bfloat16* dq;
   int dq_rows;            // 64-element rows per token of dq (Hq, or Hq + 2 Hkv when packed)
@@ -125,7 +172,11 @@ struct DqSmem {
   uint64_t drain[2];
   uint32_t tmem_base;
   Ctl ctl;
-  int eq, ek, eds;  // dQ pass: fp16 scale exponents
+  int ek;                     // dQ pass: K's fp16 scale exponent
+  float vn8;                  // dQ pass: 8 max|V| >= every ||v_j||
+  unsigned int dmax_bits;     // Delta pass: max |Delta| of the CTA's rows (float bits)
+  int eqt[2];                 // dQ pass: scale exponent of Q tile x
+  float dn2[2][128];          // dQ pass: ||dO_i||^2 of tile x's rows
 };
 // smem: [Q0 Q1 dO0 dO1][K stages][V stages][dQ staging 8 x 4 KB][DqSmem]
 constexpr size_t kDqTileBytes = size_t(4) * kTile + size_t(2 * kDqStages) * kKVTile + 8 * 4096;
@@ -175,7 +226,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (tid == 0) {
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.q_full[x], 1);
-      mbar_init(&sm.q_empty[x], kDelta ? 2 : 1);  // + the range scanner in the Delta pass
+      // Delta pass: MMA commit + the range scanner; dQ pass: MMA commit + the 4 dS warps of
+      // the tile, which read the fill's eq and row norms (so the slot is not refilled first)
+      mbar_init(&sm.q_empty[x], kDelta ? 2 : 5);
       mbar_init(&sm.q16[x], 1);
       mbar_init(&sm.s_full[x], 1);
       mbar_init(&sm.ds_full[x], 4);
@@ -189,35 +242,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(&sm.k16[s], 1);
     }
     sm.ctl.abort = 0;
+    sm.dmax_bits = 0u;
     fence_mbar_init();
   }
   if (!kDelta && warp == kQsProducerWarp) {
-    // operand ranges recorded by the Delta pass -> scale exponents
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
-    bool bad[4] = {false, false, false, false};
-    for (int sl = lane; sl < dp.amax_slots; sl += 32) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float v = dp.amax[4 * sl + c];
-        a[c] = fmaxf(a[c], v);
-        bad[c] |= !(v == v);
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        a[c] = fmaxf(a[c], __shfl_xor_sync(0xffffffffu, a[c], o));
-        bad[c] |= __shfl_xor_sync(0xffffffffu, bad[c], o);
-      }
-      if (bad[c]) a[c] = __int_as_float(0x7fc00000);
-    }
+    // operand ranges recorded by the Delta launch -> K's scale and the bound on ||v_j||
+    const float ak = slots_max(dp.amax, dp.amax_slots, kAmK, lane);
+    const float av = slots_max(dp.amax, dp.amax_slots, kAmV, lane);
     if (lane == 0) {
-      sm.eq = fp16_shift(a[0]);
-      sm.ek = fp16_shift(a[1]);
-      bool ok_do, ok_v;
-      const int Edo = amax_exp(a[3], &ok_do), Ev = amax_exp(a[2], &ok_v);
-      sm.eds = (ok_do && ok_v) ? min(max(15 - (Edo + Ev + 7), -60), 60) : 0;
+      sm.ek = fp16_shift(ak);
+      sm.vn8 = 8.f * av;
     }
   }
   if (warp == kQsMmaWarp) {
@@ -230,17 +264,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   Ctl* ctl = &sm.ctl;
   unsigned int* status = p.status;
-  const int eq = kDelta ? 0 : sm.eq, ek = kDelta ? 0 : sm.ek, eds = kDelta ? 0 : sm.eds;
+  const int ek = kDelta ? 0 : sm.ek;
+  const float vn8 = kDelta ? 0.f : sm.vn8;
 
   if (warp >= 8) {
     regs_dec<kQsCtrlRegs>();
     if (!kDelta && warp == 11) {
       // ---------------------------------------------------------- operand conversion
-      // dQ pass: every Q tile and K block is rewritten in place as fp16 times 2^eq / 2^ek (S
-      // then runs on fp16 operands -- exact, the scales fold into the exponent -- and
-      // dQ += dS K on fp16 dS) and released to the MMA issuers through q16 / k16.  Walks the
-      // producer's fills in its order.
-      const float sq = ldexpf(1.f, eq), sk = ldexpf(1.f, ek);
+      // dQ pass: every Q tile is rewritten in place as fp16 times 2^eq (eq from the tile's own
+      // largest magnitude) and every K block as fp16 times 2^ek (S then runs on fp16 operands
+      // -- exact, the scales fold into the exponent -- and dQ += dS K on fp16 dS); the rows'
+      // ||dO_i||^2 and the tile's eq go to the dS warpgroups.  Released to the MMA issuers
+      // and the dS warpgroups through q16 / k16.  Walks the producer's fills in its order.
+      const float sk = ldexpf(1.f, ek);
+      uint32_t mq = 0;  // running max|Q| over the CTA's tiles (bf16 bit pairs)
       long long prev_unit = -1;
       uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
       bool ok = true;
@@ -261,7 +298,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           ok = __all_sync(0xffffffffu, wait_bar(&sm.q_full[x], qn[x] & 1u, ctl, status, 17));
           if (!ok) break;
           ++qn[x];
-          to_fp16_scaled(sQ[x], p.rows * 128, sq, lane);
+          const uint32_t mt = scan_amax(sQ[x], p.rows * 128, lane, 0u);
+          mq = __vmaxu2(mq, mt);
+          const int eqt = fp16_shift(amax_reduce(mt));
+          to_fp16_scaled(sQ[x], p.rows * 128, ldexpf(1.f, eqt), lane);
+          for (int rr = lane; rr < p.rows; rr += 32) sm.dn2[x][rr] = row_norm2(sdO[x], rr);
+          if (lane == 0) sm.eqt[x] = eqt;
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.q16[x]);
@@ -281,11 +323,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         sbase += nb;
       }
+      const float aq = amax_reduce(mq);
+      if (lane == 0) dp.amax[kAmaxStride * blockIdx.x + kAmQ] = aq;
     } else if (kDelta && warp == 11) {
       // ---------------------------------------------------------- operand range scan
       // Walks the producer's fills in its order; every fill is scanned and then released
-      // (one more arrival on q_empty / kv_empty), so no buffer is refilled unscanned.
-      uint32_t mq = 0, mk = 0, mv = 0, mdo = 0;
+      // (one more arrival on q_empty / kv_empty), so no buffer is refilled unscanned.  (Q's
+      // range is taken per tile by the dQ pass.)
+      uint32_t mk = 0, mv = 0, mdo = 0;
       long long prev_unit = -1;
       uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
       bool ok = true;
@@ -298,7 +343,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           ok = __all_sync(0xffffffffu, wait_bar(&sm.q_full[x], qn[x] & 1u, ctl, status, 17));
           if (!ok) break;
           ++qn[x];
-          mq = scan_amax(sQ[x], p.rows * 128, lane, mq);
           mdo = scan_amax(sdO[x], p.rows * 128, lane, mdo);
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.q_empty[x]);
@@ -328,14 +372,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         sbase += nb;
       }
-      const float aq = amax_reduce(mq), ak = amax_reduce(mk), av = amax_reduce(mv),
-                  ad = amax_reduce(mdo);
+      const float ak = amax_reduce(mk), av = amax_reduce(mv), ad = amax_reduce(mdo);
       if (lane == 0) {
-        float* slot = dp.amax + 4 * blockIdx.x;
-        slot[0] = aq;
-        slot[1] = ak;
-        slot[2] = av;
-        slot[3] = ad;
+        float* slot = dp.amax + kAmaxStride * blockIdx.x;
+        slot[kAmK] = ak;
+        slot[kAmV] = av;
+        slot[kAmDo] = ad;
       }
     } else if (warp == kQsProducerWarp) {
       // ---------------------------------------------------------- TMA producer
@@ -353,6 +395,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const int nb = it.kb_hi - it.kb_lo + 1;
           auto load_kv = [&](int stage, int kb) {
             const int kp = kb * kBN;
+            (void)OD_TMA_OK(it.kvh, p.is_time ? it.fixed : kp, p.is_time ? kp : it.fixed, it.b, p.Hkv,
+                            p.S, p.T, p.B, status, 210);
             mbar_arrive_expect_tx(&sm.k_full[stage], kKVTile);
             mbar_arrive_expect_tx(&sm.v_full[stage], kKVTile);
             if (p.is_time) {
@@ -368,6 +412,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (qn[x] > 0) ok = wait_bar(&sm.q_empty[x], (qn[x] - 1) & 1u, ctl, status, 1);
             if (!ok) break;
             const int t0 = x ? it.tok0[1] : it.tok0[0];
+            (void)OD_TMA_OK(it.kvh * p.G, p.is_time ? it.fixed : t0, p.is_time ? t0 : it.fixed, it.b,
+                            p.Hq, p.S, p.T, p.B, status, 211);
             mbar_arrive_expect_tx(&sm.q_full[x], 2 * p.rows * 128);
             if (p.is_time) {
               tma_load_5d(sQ[x], &tm_q, &sm.q_full[x], 0, it.kvh * p.G, it.fixed, t0, it.b);
@@ -529,7 +575,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int tok = r / G;
     const int g = r - tok * G;
     const float lg2e = 1.4426950408889634f;
-    uint32_t jS = 0, jD = 0;
+    uint32_t jS = 0, jD = 0, jq = 0;
+    uint32_t dmax = 0u;  // Delta pass: max |Delta| of this thread's rows (float bits; NaN on top)
     bool ok = true;
     for (long long i = i0; i < i1 && ok; i += istep) {
       const FwdItem it = fwd_decode<kVarlen>(p, i);
@@ -538,20 +585,37 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int nb = it.kb_hi - it.kb_lo + 1;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
       const int pos = mytok0 + tok;
-      const bool row_ok = (r < p.rows) && (pos < (kVarlen ? it.L : p.L));
       long long row = 0;
-      float lse2 = INFINITY, ndl = 0.f;
+      float lse2 = INFINITY, dl = 0.f;
       float dacc[4] = {0.f, 0.f, 0.f, 0.f};
+      bool row_ok = (r < p.rows) && (pos < (kVarlen ? it.L : p.L));
       if (row_ok) {
         const long long t_idx = p.is_time ? pos : it.fixed;
         const long long s_idx = p.is_time ? it.fixed : pos;
         row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + g;
-        lse2 = dp.lse[row] * lg2e;
-        if (!kDelta) ndl = -dp.delta[row] * ldexpf(1.f, eds);
+        row_ok = OD_IN_RANGE(row, static_cast<long long>(p.B) * p.T * p.S * p.Hq, status, 212);
       }
-      // the dQ pass's S carries 2^(eq + ek); its dS is written times 2^eds
-      const float slx = kDelta ? p.sl : p.sl * ldexpf(1.f, -(eq + ek));
-      const float c1 = ldexpf(1.f, eds);
+      if (row_ok) {
+        lse2 = dp.lse[row] * lg2e;
+        if (!kDelta) dl = dp.delta[row];
+      }
+      // dQ pass: S carries 2^(eq + ek) (eq: this Q tile's); dS is written times 2^eds with eds
+      // from the row's bound ||dO_i|| 8 max|V| + |Delta_i| on |dS|, and dQ undoes 2^(eds + ek)
+      float slx = p.sl, c1 = 1.f, fq = dp.scale;
+      if (!kDelta) {
+        ok = __all_sync(0xffffffffu, wait_bar(&sm.q16[x], jq & 1u, ctl, status, 9));
+        if (!ok) break;
+        ++jq;
+        const int eqt = sm.eqt[x];
+        const float dn = row_ok ? sqrtf(sm.dn2[x][r]) : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.q_empty[x]);  // this warp is done with the fill's values
+        const int eds = fp16_shift(fmaf(dn, vn8, fabsf(dl)));
+        slx = p.sl * ldexpf(1.f, -(eqt + ek));
+        c1 = ldexpf(1.f, eds);
+        fq = dp.scale * ldexpf(1.f, -(eds + ek));
+      }
+      const float ndl = -dl * c1;
       const float2 sl2 = make_float2(slx, slx), c12 = make_float2(c1, c1), nd2 = make_float2(ndl, ndl);
       const float2 nl2 = make_float2(-lse2, -lse2);
       for (int bi = 0; bi < nb; ++bi) {
@@ -610,7 +674,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       if (!ok) break;
       if (kDelta) {
-        if (row_ok) dp.delta[row] = (dacc[0] + dacc[1]) + (dacc[2] + dacc[3]);
+        if (row_ok) {
+          const float d = (dacc[0] + dacc[1]) + (dacc[2] + dacc[3]);
+          dp.delta[row] = d;
+          dmax = max(dmax, __float_as_uint(fabsf(d)));
+        }
         continue;
       }
       // ---------------------------------------------------------------- epilogue
@@ -624,7 +692,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tmem_ld32(tQ + 32, o + 32);
       tmem_wait_ld_dep32(o);
       tmem_wait_ld_dep32(o + 32);
-      const float fq = dp.scale * ldexpf(1.f, -(eds + ek));  // undo the fp16 scales
       if (row_ok && dp.dq_f32) {
         float4* dst = reinterpret_cast<float4*>(dp.dq_f32 + row * 64);
 #pragma unroll
@@ -658,17 +725,24 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             const long long rw =
                 ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * dp.dq_rows + it.kvh * G + gg;
             const uint4 wv = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
-            reinterpret_cast<uint4*>(dp.dq + rw * 64)[ch] = wv;
+            if (OD_IN_RANGE(rw, static_cast<long long>(p.B) * p.T * p.S * dp.dq_rows, status, 213))
+              reinterpret_cast<uint4*>(dp.dq + rw * 64)[ch] = wv;
           }
         }
         __syncwarp();
       }
+    }
+    if (kDelta) {
+      __syncwarp();
+      const uint32_t m = __reduce_max_sync(0xffffffffu, dmax);
+      if (lane == 0) atomicMax(&sm.dmax_bits, m);
     }
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (kDelta && tid == 0) dp.amax[kAmaxStride * blockIdx.x + kAmDelta] = __uint_as_float(sm.dmax_bits);
   if (warp == kQsMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -706,8 +780,9 @@ struct KvParams {
   FwdParams f;            // shapes (item fields unused)
   const float* lse;
   const float* delta;
-  const float* amax;      // Delta-pass slots: 4 floats per CTA of that launch
-  int amax_slots;
+  const float* amax;      // operand-range slots (see "fp16 operand scaling")
+  int amax_slots;         // slots the Delta launch wrote
+  int dq_slots;           // slots the dQ pass wrote (max|Q|)
   float scale;
   long long nitems;       // units x key blocks
   int nkb;                // 128-key blocks per unit
@@ -725,9 +800,10 @@ struct KvSmem {
   uint64_t drain;
   uint32_t tmem_base;
   Ctl ctl;
-  int eq, ek, ev, edo, eds;          // fp16 scale exponents
+  int eq, ek, ev, edo;               // fp16 scale exponents
+  float don8, dmax;                  // 8 max|dO| >= every ||dO_i||; max|Delta|
   alignas(16) float nlse2[kKvQSlots][128];  // -log2(e) LSE per tile row (-inf: no row)
-  alignas(16) float ndel[kKvQSlots][128];   // -Delta * 2^eds per tile row
+  alignas(16) float ndel[kKvQSlots][128];   // -Delta per tile row
 };
 static_assert(offsetof(KvSmem, nlse2) % 16 == 0 && offsetof(KvSmem, ndel) % 16 == 0,
               "row arrays are read with 16-byte loads");
@@ -794,11 +870,12 @@ struct KvSeq {
 };
 
 // One 32-column chunk of a key lane's elementwise step: P = exp2(S sl + nlse2) (zero
-// outside the lane's rows when kMasked), dS = P (dP c1 + ndel); both packed as fp16 pairs.
+// outside the lane's rows when kMasked), dS = (P sj) (dP c1 + ndel); both packed as fp16
+// pairs.
 template <bool kMasked>
 __device__ __forceinline__ void dkdv_chunk(const float* sv, const float* dv, const float* NL,
-                                           const float* ND, float2 sl2, float2 c12, uint32_t keep,
-                                           uint32_t* pk, uint32_t* dk) {
+                                           const float* ND, float2 sl2, float2 c12, float2 sj2,
+                                           uint32_t keep, uint32_t* pk, uint32_t* dk) {
 #pragma unroll
   for (int j4 = 0; j4 < 8; ++j4) {
     const float4 l4 = *reinterpret_cast<const float4*>(NL + 4 * j4);
@@ -816,8 +893,8 @@ __device__ __forceinline__ void dkdv_chunk(const float* sv, const float* dv, con
     }
     const float2 t0 = __ffma2_rn(make_float2(dv[4 * j4], dv[4 * j4 + 1]), c12, make_float2(d4.x, d4.y));
     const float2 t1 = __ffma2_rn(make_float2(dv[4 * j4 + 2], dv[4 * j4 + 3]), c12, make_float2(d4.z, d4.w));
-    const float2 s0 = __fmul2_rn(p0, t0);
-    const float2 s1 = __fmul2_rn(p1, t1);
+    const float2 s0 = __fmul2_rn(__fmul2_rn(p0, sj2), t0);
+    const float2 s1 = __fmul2_rn(__fmul2_rn(p1, sj2), t1);
     pk[2 * j4] = pack_f16x2(p0.x, p0.y);
     pk[2 * j4 + 1] = pack_f16x2(p1.x, p1.y);
     dk[2 * j4] = pack_f16x2(s0.x, s0.y);
@@ -874,33 +951,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     fence_mbar_init();
   }
   if (warp == kKvProducerWarp) {
-    // operand ranges recorded by the Delta pass -> scale exponents
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int sl = lane; sl < kp.amax_slots; sl += 32) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) a[c] = fmaxf(a[c], kp.amax[4 * sl + c]);
-    }
-    // NaN compares false in fmaxf: propagate it explicitly so that no scaling is applied
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      bool bad = false;
-      for (int sl = lane; sl < kp.amax_slots; sl += 32) bad |= !(kp.amax[4 * sl + c] == kp.amax[4 * sl + c]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        a[c] = fmaxf(a[c], __shfl_xor_sync(0xffffffffu, a[c], o));
-        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-      }
-      if (bad) a[c] = __int_as_float(0x7fc00000);
-    }
+    // operand ranges recorded by the Delta launch and the dQ pass -> scale exponents
+    const float aq = slots_max(kp.amax, kp.dq_slots, kAmQ, lane);
+    const float ak = slots_max(kp.amax, kp.amax_slots, kAmK, lane);
+    const float av = slots_max(kp.amax, kp.amax_slots, kAmV, lane);
+    const float ado = slots_max(kp.amax, kp.amax_slots, kAmDo, lane);
+    const float adl = slots_max(kp.amax, kp.amax_slots, kAmDelta, lane);
     if (lane == 0) {
-      sm.eq = fp16_shift(a[0]);
-      sm.ek = fp16_shift(a[1]);
-      sm.ev = fp16_shift(a[2]);
-      sm.edo = fp16_shift(a[3]);
-      // |dS| <= |dP| + |Delta| <= 2 * 64 * max|dO| * max|V| < 2^(Edo + Ev + 7)
-      bool ok_do, ok_v;
-      const int Edo = amax_exp(a[3], &ok_do), Ev = amax_exp(a[2], &ok_v);
-      sm.eds = (ok_do && ok_v) ? min(max(15 - (Edo + Ev + 7), -60), 60) : 0;
+      sm.eq = fp16_shift(aq);
+      sm.ek = fp16_shift(ak);
+      sm.ev = fp16_shift(av);
+      sm.edo = fp16_shift(ado);
+      sm.don8 = 8.f * ado;
+      sm.dmax = adl;
     }
   }
   if (warp == kKvMmaWarp) {
@@ -913,7 +976,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   Ctl* ctl = &sm.ctl;
   unsigned int* status = p.status;
-  const int eq = sm.eq, ek = sm.ek, ev = sm.ev, edo = sm.edo, eds = sm.eds;
+  const int eq = sm.eq, ek = sm.ek, ev = sm.ev, edo = sm.edo;
 
   if (warp >= 8) {
     regs_dec<kKvCtrlRegs>();
@@ -932,6 +995,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(&sm.kv_full[slot], 2 * kKvBN * 128);
           const int k0 = it.kb * kKvBN;
+          (void)OD_TMA_OK(it.kvh, p.is_time ? it.fixed : k0, p.is_time ? k0 : it.fixed, it.b, p.Hkv,
+                          p.S, p.T, p.B, status, 220);
           uint8_t* dK = sKV + (2 * slot) * kTile;
           uint8_t* dV = sKV + (2 * slot + 1) * kTile;
           if (p.is_time) {
@@ -953,6 +1018,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           }
           const int t0 = tq * p.nTok;
           if (lane == 0) {
+            (void)OD_TMA_OK(it.kvh * p.G, p.is_time ? it.fixed : t0, p.is_time ? t0 : it.fixed, it.b,
+                            p.Hq, p.S, p.T, p.B, status, 221);
             uint8_t* dQ = sQD + (2 * q) * kTile;
             uint8_t* dO = sQD + (2 * q + 1) * kTile;
             mbar_arrive_expect_tx(&sm.q_full[q], 2 * p.rows * 128);
@@ -1095,7 +1162,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       // ---------------------------------------------------------- converters (10: Q, 11: dO)
       const int which = warp - kKvConvWarp;  // 0: Q, 1: dO
       const float sqd = ldexpf(1.f, which ? edo : eq);
-      const float rowf = which ? -ldexpf(1.f, eds) : -1.4426950408889634f;
+      const float rowf = which ? -1.f : -1.4426950408889634f;
       KvSeq<kVarlen> seq;
       KvItem it;
       uint32_t n = 0, tau = 0;
@@ -1109,7 +1176,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (!ok) break;
           OD_TP(71, (int)tau, 0);
           to_fp16_scaled(sQD + (2 * q + which) * kTile, p.rows * 128, sqd, lane);
-          {  // rows of the tile: -log2(e) LSE (warp 10) or -Delta 2^eds (warp 11); 0 elsewhere
+          {  // rows of the tile: -log2(e) LSE (warp 10) or -Delta (warp 11); 0 elsewhere
             float* rowv = which ? sm.ndel[q] : sm.nlse2[q];
             const int t0 = tq * p.nTok;
             for (int rr = lane; rr < 128; rr += 32) {
@@ -1130,10 +1197,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int j = tid & 127;               // key lane within the block
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + 128u * h + lane_off, tD = tS + 64u;
-    // logits: S^T carries 2^(eq+ek), dP^T carries 2^(edo+ev); dS^T is written times 2^eds
+    // logits: S^T carries 2^(eq+ek), dP^T carries 2^(edo+ev); dS^T is written times 2^eds,
+    // eds from this key's bound ||v_j|| 8 max|dO| + max|Delta| on |dS|
     const float slx = p.sl * ldexpf(1.f, -(eq + ek));
-    const float c1 = ldexpf(1.f, eds - edo - ev);
+    const float c1 = ldexpf(1.f, -(edo + ev));
     const float2 sl2 = make_float2(slx, slx), c12 = make_float2(c1, c1);
+    const float don8 = sm.don8, dmax = sm.dmax;
+    int eds = 0;
+    float2 sj2 = make_float2(1.f, 1.f);
     const int Weff = min(p.window, p.L);
     const float skv = ldexpf(1.f, h ? ev : ek);
     KvSeq<kVarlen> seq;
@@ -1149,6 +1220,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (!ok) break;
         const uint8_t* row = sKV + (2 * slot + h) * kTile + j * 128;
         const float2 s2 = make_float2(skv, skv);
+        eds = fp16_shift(fmaf(sqrtf(row_norm2(sKV + (2 * slot + 1) * kTile, j)), don8, dmax));
+        sj2 = make_float2(ldexpf(1.f, eds), ldexpf(1.f, eds));
         uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row sits at chunk c ^ (j & 7)
@@ -1208,9 +1281,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const uint32_t keep = keep_bits32(64 * h + 32 * c, r_lo, r_hi, -1);
           uint32_t pk[16], dk[16];
           if (__any_sync(0xffffffffu, keep != 0xFFFFFFFFu))
-            dkdv_chunk<true>(sv + 32 * c, dv + 32 * c, NL, ND, sl2, c12, keep, pk, dk);
+            dkdv_chunk<true>(sv + 32 * c, dv + 32 * c, NL, ND, sl2, c12, sj2, keep, pk, dk);
           else
-            dkdv_chunk<false>(sv + 32 * c, dv + 32 * c, NL, ND, sl2, c12, keep, pk, dk);
+            dkdv_chunk<false>(sv + 32 * c, dv + 32 * c, NL, ND, sl2, c12, sj2, keep, pk, dk);
           tmem_st16(tS + 16 * c, pk);   // P^T (fp16 pairs) over the scores already read
           tmem_st16(tD + 16 * c, dk);   // dS^T (fp16 pairs, times 2^eds) over dP^T
         }
@@ -1244,6 +1317,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const long long t_idx = p.is_time ? kpos : it.fixed;
         const long long s_idx = p.is_time ? it.fixed : kpos;
         const long long tok = (static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx;
+        if (!OD_IN_RANGE(tok, static_cast<long long>(p.B) * p.T * p.S, status, 222)) continue;
         const long long row = tok * p.Hkv + it.kvh;
         uint4* out = reinterpret_cast<uint4*>((h ? kp.dv : kp.dk) + (tok * kp.kv_rows + it.kvh) * 64);
 #pragma unroll
@@ -1312,22 +1386,23 @@ inline cudaError_t bwd_setup() {
 // When the forward also wrote O's rounding residual O_lo (O ~ o + o_lo to about 16 significant
 // bits), Delta = <dO, O> is a row-wise dot product of tensors in HBM and needs no recompute of
 // P and dP: this streaming kernel replaces the Delta pass.  It also records the operand
-// ranges max|Q|, max|K|, max|V|, max|dO| per CTA, in the slots the Delta pass would fill.
+// ranges max|K|, max|V|, max|dO|, max|Delta| per CTA, in the slots the Delta pass would fill
+// (Q's range is taken per tile by the dQ pass, so Q is not read here).
 // One warp takes 4 query rows at a time (8 lanes x 16 bytes per 128-byte row); every byte of
-// dO, O, O_lo, Q, K and V is read once.
+// dO, O, O_lo, K and V is read once.
 constexpr int kDeltaOThreads = 256;
 
 struct DeltaOParams {
   const __nv_bfloat16* o;       // [rows, 64] contiguous
   const __nv_bfloat16* o_lo;    // [rows, 64] contiguous
   const __nv_bfloat16* dout;    // [rows, 64] contiguous
-  const __nv_bfloat16* q;       // views: token i starts at row i * q_rows (or kv_rows)
-  const __nv_bfloat16* k;
+  const __nv_bfloat16* k;       // views: token i starts at row i * kv_rows
   const __nv_bfloat16* v;
   long long ntok;               // B * T * S
-  int Hq, Hkv, q_rows, kv_rows;
+  int Hq, Hkv, kv_rows;
   float* delta;                 // [rows]
-  float* amax;                  // 4 floats per CTA
+  float* amax;                  // one slot of kAmaxStride floats per CTA
+  unsigned int* status;         // device status word (range checks of debug builds)
 };
 
 __device__ __forceinline__ float bf16x2_dot3(uint32_t d, uint32_t o, uint32_t l, float acc) {
@@ -1339,12 +1414,13 @@ __device__ __forceinline__ float bf16x2_dot3(uint32_t d, uint32_t o, uint32_t l,
 
 __global__ void __launch_bounds__(kDeltaOThreads)
     od_bwd_delta_o_kernel(const DeltaOParams p) {
-  __shared__ float red[kDeltaOThreads / 32][4];
+  __shared__ float red[kDeltaOThreads / 32][4];  // per warp: K, V, dO, Delta
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long gw = static_cast<long long>(blockIdx.x) * (kDeltaOThreads / 32) + warp;
   const long long nw = static_cast<long long>(gridDim.x) * (kDeltaOThreads / 32);
   const int sub = lane >> 3, ch = lane & 7;
-  uint32_t mq = 0, mk = 0, mv = 0, md = 0;
+  uint32_t mk = 0, mv = 0, md = 0;
+  uint32_t mdl = 0u;  // max |Delta| (float bits; NaN on top)
 
   // Delta: groups of 4 rows, four groups in flight per warp
   const long long nrows = p.ntok * p.Hq;
@@ -1380,11 +1456,14 @@ __global__ void __launch_bounds__(kDeltaOThreads)
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
       acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      if (ch == 0 && r[u] >= 0) p.delta[r[u]] = acc;
+      if (ch == 0 && r[u] >= 0 && OD_IN_RANGE(r[u], nrows, p.status, 230)) {
+        p.delta[r[u]] = acc;
+        mdl = max(mdl, __float_as_uint(fabsf(acc)));
+      }
     }
   }
 
-  // operand ranges of Q, K, V.  A contiguous tensor is one flat array (four 16-byte loads in
+  // operand ranges of K and V.  A contiguous tensor is one flat array (four 16-byte loads in
   // flight per thread); a packed view is walked token by token (the token's head rows are
   // contiguous), again four loads in flight per lane.
   auto vmax4 = [](uint32_t m, const uint4& x) {
@@ -1423,11 +1502,11 @@ __global__ void __launch_bounds__(kDeltaOThreads)
     }
     return m;
   };
-  mq = scan(p.q, p.q_rows, p.Hq, mq);
   mk = scan(p.k, p.kv_rows, p.Hkv, mk);
   mv = scan(p.v, p.kv_rows, p.Hkv, mv);
 
-  const float a[4] = {amax_reduce(mq), amax_reduce(mk), amax_reduce(mv), amax_reduce(md)};
+  const float a[4] = {amax_reduce(mk), amax_reduce(mv), amax_reduce(md),
+                      __uint_as_float(__reduce_max_sync(0xffffffffu, mdl))};
   if (lane == 0)
     for (int c = 0; c < 4; ++c) red[warp][c] = a[c];
   __syncthreads();
@@ -1439,16 +1518,17 @@ __global__ void __launch_bounds__(kDeltaOThreads)
       nan |= !(x == x);
       m = fmaxf(m, x);
     }
-    p.amax[4 * blockIdx.x + threadIdx.x] = nan ? __int_as_float(0x7fc00000) : m;
+    static_assert(kAmK == 0 && kAmV == 1 && kAmDo == 2 && kAmDelta == 3, "slot fields in order");
+    p.amax[kAmaxStride * blockIdx.x + threadIdx.x] = nan ? __int_as_float(0x7fc00000) : m;
   }
 }
 
-// workspace: Delta (fp32, one per query row), then kAmaxSlots x 4 fp32 operand ranges
+// workspace: Delta (fp32, one per query row), then kAmaxSlots x kAmaxStride fp32 operand ranges
 inline size_t bwd_delta_bytes(int B, int T, int S, int Hq) {
   return (size_t(B) * T * S * Hq * sizeof(float) + 255) & ~size_t(255);
 }
 inline size_t bwd_workspace_bytes(int B, int T, int S, int Hq, int /*D*/) {
-  return bwd_delta_bytes(B, T, S, Hq) + size_t(kAmaxSlots) * 4 * sizeof(float);
+  return bwd_delta_bytes(B, T, S, Hq) + size_t(kAmaxSlots) * kAmaxStride * sizeof(float);
 }
 
 struct BwdArgs {

@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (blk == 0) bytes += G * kDecRowBytes;
     if (blk == slot_blk) bytes += 2 * kDecRowBytes;
     mbar_arrive_expect_tx(bar, bytes);
+    (void)OD_TMA_OK(d.h, d.s, blk * kDecBN, d.b, p.Hkv, p.S, p.W, p.B, p.status, 240);
     tma_load_5d(sK, &tk, bar, 0, d.h, d.s, blk * kDecBN, d.b);
     tma_load_5d(sV, &tv, bar, 0, d.h, d.s, blk * kDecBN, d.b);
     if (blk == 0) {
@@ -188,8 +189,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       *reinterpret_cast<uint32_t*>(sK + off) = kn;
       *reinterpret_cast<uint32_t*>(sV + off) = vn;
       const size_t crow = ((static_cast<size_t>(d.b) * p.W + p.slot) * p.S + d.s) * p.Hkv + d.h;
-      reinterpret_cast<uint32_t*>(p.k_cache + crow * 64)[lane] = kn;
-      reinterpret_cast<uint32_t*>(p.v_cache + crow * 64)[lane] = vn;
+      if (OD_IN_RANGE(static_cast<long long>(crow), static_cast<long long>(p.B) * p.W * p.S * p.Hkv,
+                      p.status, 241)) {
+        reinterpret_cast<uint32_t*>(p.k_cache + crow * 64)[lane] = kn;
+        reinterpret_cast<uint32_t*>(p.v_cache + crow * 64)[lane] = vn;
+      }
       __syncwarp();
     }
 
@@ -289,13 +293,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
       const float inv0 = 1.f / s0, inv1 = 1.f / s1;
       const size_t qrow = (static_cast<size_t>(d.b) * p.S + d.s) * p.Hq + static_cast<size_t>(d.h) * G;
-      if (g < G) {
+      const long long nq = static_cast<long long>(p.B) * p.S * p.Hq;  // query rows (range checks)
+      (void)nq;
+      if (g < G && OD_IN_RANGE(static_cast<long long>(qrow + g), nq, p.status, 242)) {
         uint32_t* orow = reinterpret_cast<uint32_t*>(p.o + (qrow + g) * 64);
 #pragma unroll
         for (int n = 0; n < 8; ++n) orow[4 * n + qd] = pack_bf16x2(oacc[n][0] * inv0, oacc[n][1] * inv0);
         if (qd == 0) p.lse[qrow + g] = (m0 + __log2f(s0)) * 0.6931471805599453f;
       }
-      if (g + 8 < G) {
+      if (g + 8 < G && OD_IN_RANGE(static_cast<long long>(qrow + g + 8), nq, p.status, 242)) {
         uint32_t* orow = reinterpret_cast<uint32_t*>(p.o + (qrow + g + 8) * 64);
 #pragma unroll
         for (int n = 0; n < 8; ++n) orow[4 * n + qd] = pack_bf16x2(oacc[n][2] * inv1, oacc[n][3] * inv1);

@@ -357,6 +357,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           auto load_k = [&](int stage, int kb) {
             int c[2];
             kv_coords(kb, c);
+            // (a packed unit without a tile B loads its second block from past the end on
+            // purpose: TMA fills it with zeros)
+            if (kMode != kModeTimePacked || kb == 0 || it.valid[1])
+              (void)OD_TMA_OK(it.kvh, c[0], c[1], it.b, p.Hkv, p.S, p.T, p.B, status, 201);
             mbar_arrive_expect_tx(&sm.k_full[stage], p.kvb * 128);
             tma_load_5d(sK + stage * kFwdKVTile, &tm_k, &sm.k_full[stage], 0, it.kvh, c[0], c[1], it.b);
           };
@@ -376,6 +380,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             uint8_t* dst = sQ + (2 * x + q) * kTile;
             mbar_arrive_expect_tx(&sm.q_full[x][q], p.rows * 128);
             const int c1 = it.kvh * p.G;
+            (void)OD_TMA_OK(c1, kMode == kModeTime ? it.fixed : it.tok0[x],
+                            kMode == kModeSpace ? it.fixed : (kMode == kModeTime ? it.tok0[x] : 0),
+                            it.b, p.Hq, p.S, p.T, p.B, status, 200);
             if (kMode == kModeSpace)
               tma_load_5d(dst, &tm_q, &sm.q_full[x][q], 0, c1, it.tok0[x], it.fixed, it.b);
             else if (kMode == kModeTime)
@@ -873,7 +880,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         row = ((static_cast<long long>(it2.b) * p.T + pos) * p.S + it2.fixed) * p.Hq + hq;
       else
         row = ((static_cast<long long>(it2.b) * p.T + pos) * p.S + spos) * p.Hq + hq;
-      if (row_ok) p.lse[row] = (m_used + log2f(l)) * 0.69314718055994531f;
+      // (row_w: row_ok, and in debug builds also the row inside the output)
+      const bool row_w =
+          row_ok && OD_IN_RANGE(row, static_cast<long long>(p.B) * p.T * p.S * p.Hq, status, 202);
+      if (row_w) p.lse[row] = (m_used + log2f(l)) * 0.69314718055994531f;
       const bool want_lo = p.o_lo != nullptr;
       if (!kVarlen) {
         // stage the tile's rows (128 bytes each, 16-byte chunk c of row r at c ^ (r & 7): the
@@ -899,8 +909,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       uint8_t* so = sOst + x * kTile + r * 128;
       uint8_t* sl = sLst + x * kTile + r * 128;
-      uint4* gdst = reinterpret_cast<uint4*>(p.o + (row_ok ? row : 0) * 64);
-      uint4* gdlo = want_lo ? reinterpret_cast<uint4*>(p.o_lo + (row_ok ? row : 0) * 64) : nullptr;
+      uint4* gdst = reinterpret_cast<uint4*>(p.o + (row_w ? row : 0) * 64);
+      uint4* gdlo = want_lo ? reinterpret_cast<uint4*>(p.o_lo + (row_w ? row : 0) * 64) : nullptr;
       // (fixed-length space attention loads the whole row at once, the other modes in
       // quarters: each measured faster for its mode)
       if (kMode == kModeSpace && !kVarlen) {
@@ -943,7 +953,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int sc = chunk ^ (r & 7);
             *reinterpret_cast<uint4*>(so + sc * 16) = make_uint4(w[0], w[1], w[2], w[3]);
             if (want_lo) *reinterpret_cast<uint4*>(sl + sc * 16) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-          } else if (row_ok) {
+          } else if (row_w) {
             gdst[chunk] = make_uint4(w[0], w[1], w[2], w[3]);
             if (want_lo) gdlo[chunk] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
           }
@@ -962,8 +972,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (kMode == kModeSpace) { c2 = tok0x; c3 = it2.fixed; }
             else if (kMode == kModeTime) { c2 = it2.fixed; c3 = tok0x; }
             else { c2 = tok0x; c3 = 0; }
-            tma_store_5d(&tm_o, sOst + x * kTile, 0, c1, c2, c3, it2.b);
-            if (want_lo) tma_store_5d(&tm_lo, sLst + x * kTile, 0, c1, c2, c3, it2.b);
+            if (OD_TMA_OK(c1, c2, c3, it2.b, p.Hq, p.S, p.T, p.B, status, 203)) {
+              tma_store_5d(&tm_o, sOst + x * kTile, 0, c1, c2, c3, it2.b);
+              if (want_lo) tma_store_5d(&tm_lo, sLst + x * kTile, 0, c1, c2, c3, it2.b);
+            }
             bulk_commit();
           }
           __syncwarp();

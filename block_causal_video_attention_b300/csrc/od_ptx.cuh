@@ -15,6 +15,7 @@
 
 // Device status bits (read and cleared by od_get_device_status).
 #define OD_DEV_TIMEOUT 1u
+#define OD_DEV_RANGE 2u   // a range check of a debug build (OD_DEBUG) failed
 
 namespace od {
 
@@ -92,6 +93,36 @@ __device__ __forceinline__ void record_timeout(unsigned int* status, int site, u
   atomicCAS(status + 1, 0u,
             (static_cast<uint32_t>(site) << 24) | ((parity & 1u) << 23) | (blockIdx.x & 0x7FFFFFu));
 }
+
+// Range checks of debug builds.  Compiled with -DOD_DEBUG, every TMA coordinate and every
+// row index a thread writes through is checked against the tensor's extent before the
+// access; a violation sets OD_DEV_RANGE in status[0], keeps the first one in status[1] as
+// (site << 24) | block index, and the access is skipped (a TMA load, which the hardware
+// clips to the tensor anyway, is still issued so that its barrier completes).  Nothing
+// traps.  Without OD_DEBUG the checks compile to nothing.
+#ifdef OD_DEBUG
+__device__ __noinline__ void record_range(unsigned int* status, int site) {
+  atomicOr(status, OD_DEV_RANGE);
+  atomicCAS(status + 1, 0u, (static_cast<uint32_t>(site) << 24) | (blockIdx.x & 0xFFFFFFu));
+}
+__device__ __forceinline__ bool in_range(long long v, long long hi, unsigned int* status, int site) {
+  if (v >= 0 && v < hi) return true;
+  record_range(status, site);
+  return false;
+}
+// Start coordinates (h, s, t, b) of a box of a [D, H, S, T, B] tensor map (x is always 0).
+__device__ __forceinline__ bool tma_coords_ok(int h, int s, int t, int b, int H, int S, int T,
+                                              int B, unsigned int* status, int site) {
+  return in_range(h, H, status, site) && in_range(s, S, status, site) &&
+         in_range(t, T, status, site) && in_range(b, B, status, site);
+}
+#define OD_IN_RANGE(v, hi, status, site) ::od::in_range((v), (hi), (status), (site))
+#define OD_TMA_OK(h, s, t, b, H, S, T, B, status, site) \
+  ::od::tma_coords_ok((h), (s), (t), (b), (H), (S), (T), (B), (status), (site))
+#else
+#define OD_IN_RANGE(v, hi, status, site) true
+#define OD_TMA_OK(h, s, t, b, H, S, T, B, status, site) true
+#endif
 
 // Out-of-line record of an expired wait (cold).
 __device__ __noinline__ void wait_expired(Ctl* ctl, unsigned int* status, int site, uint32_t parity) {

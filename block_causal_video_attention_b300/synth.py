@@ -1,7 +1,9 @@
 """Seeded synthetic inputs and workload shapes.
 
-This module is shared by the CUDA path, the oracle, the tests and the bench.
-It holds no attention arithmetic: only shapes and a counter-based normal
+Test and benchmark infrastructure: the tests, the bench and the smoke check
+call it to make the inputs that they then hand both to the CUDA kernels (through
+the C ABI) and to the oracle.  Neither the kernels nor the oracle import it, and
+it holds no attention arithmetic: only shapes and a counter-based normal
 generator, so both sides of every parity check consume identical bf16 bytes.
 
 Generator (stated so that it can be re-implemented anywhere):

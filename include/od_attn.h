@@ -61,47 +61,68 @@ typedef enum {
   OD_ERR_UNSUPPORTED = 2,
   OD_ERR_CUDA = 3,
   OD_ERR_TIMEOUT = 4,
-  OD_ERR_WORKSPACE = 5
+  OD_ERR_WORKSPACE = 5,
+  OD_ERR_RANGE = 6   /* debug builds (OD_DEBUG) only: a device-side range check failed */
 } od_status;
 
-/* Space attention forward.  Writes O [B,T,S,Hq,D] (bf16) and LSE [B,T,S,Hq] (fp32).
- * o_lo (optional, may be NULL): if given, also receives O's rounding residual, [B,T,S,Hq,D]
- * bf16: o_lo = bf16(O - o) with O the fp32 result, so o + o_lo holds O to about 16
- * significant bits.  Passing it on to the backward lets the backward take Delta = <dO, O>
- * from memory instead of recomputing P and dP for it (a faster backward). */
+/* Space attention forward.  Writes O [B,T,S,Hq,D] (bf16) and LSE [B,T,S,Hq] (fp32). */
 od_status od_space_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                            void* o_lo, int B, int T, int S, int Hq, int Hkv, int D,
-                            int agent_idx, float scale, void* stream);
+                            int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                            float scale, void* stream);
 
-/* Time attention forward (window >= 1; keys t-window+1 .. t).  Writes O and LSE (and o_lo,
- * as for the space forward). */
+/* Time attention forward (window >= 1; keys t-window+1 .. t).  Writes O and LSE. */
 od_status od_time_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                           void* o_lo, int B, int T, int S, int Hq, int Hkv, int D, int window,
-                           float scale, void* stream);
+                           int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
+                           void* stream);
 
-/* Space attention backward.  Inputs: Q, K, V, the forward's O, o_lo and LSE, and dO.  Outputs
- * dQ [B,T,S,Hq,D], dK and dV [B,T,S,Hkv,D] in bf16 (overwritten).
- * o_lo may be NULL: Delta = <dO, O> per query row is then recomputed from P and dP (an extra
- * pass over Q, K, V, dO with two matrix products), because bf16 O alone does not give Delta
- * to the accuracy the gradients need; O is not read in that case.  With o_lo (the residual
- * the forward wrote), Delta is the row-wise dot product of dO with o + o_lo, read from memory.  `workspace` is
- * caller-owned device scratch of at least od_attn_bwd_workspace_bytes(0, ...) bytes
- * (Delta per query row in fp32, rounded up to 256 bytes, then 16 KiB of per-CTA operand
- * ranges); its contents on entry do not matter.
- * If dq_f32/dk_f32/dv_f32 are non-NULL, the gradients are also written there in fp32
- * (same layouts), before rounding to bf16. */
+/* Space attention backward.  Inputs: Q, K, V, the forward's O and LSE, and dO.  Outputs
+ * dQ [B,T,S,Hq,D], dK and dV [B,T,S,Hkv,D] in bf16 (overwritten).  Delta = <dO, O> per
+ * query row is recomputed from P and dP (an extra pass over Q, K, V, dO with two matrix
+ * products), because bf16 O alone does not give Delta to the accuracy the gradients need;
+ * O is therefore not read (it must still be a valid, aligned pointer).  `workspace` is
+ * caller-owned device scratch of at least od_attn_bwd_workspace_bytes(0, ...) bytes (Delta
+ * per query row in fp32, rounded up to 256 bytes, then 32 KiB of per-CTA operand ranges);
+ * its contents on entry do not matter. */
 od_status od_space_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                            const void* o_lo, const float* lse, const void* dout, void* dq,
-                            void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
                             int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
                             float scale, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Time attention backward; as od_space_attn_bwd with `window` in place of agent_idx. */
+/* Time attention backward; as od_space_attn_bwd with `window` in place of agent_idx
+ * (workspace: od_attn_bwd_workspace_bytes(1, ...)). */
 od_status od_time_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                           const void* o_lo, const float* lse, const void* dout, void* dq,
-                           void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
                            int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Extended forms: the calls above plus optional outputs.  With every added pointer NULL
+ * each computes exactly what the corresponding call above computes (same kernels, same
+ * results bit for bit).
+ * Forward: o_lo (may be NULL), if given, also receives O's rounding residual [B,T,S,Hq,D]
+ * bf16: o_lo = bf16(O - o) with O the fp32 result, so o + o_lo holds O to about 16
+ * significant bits.  Passing it on to the backward lets the backward take Delta = <dO, O>
+ * from memory instead of recomputing P and dP for it (a faster backward).
+ * Backward: o_lo (may be NULL) is the residual the forward wrote; with it, Delta is the
+ * row-wise dot product of dO with o + o_lo, read from memory (o is read then).  If
+ * dq_f32/dk_f32/dv_f32 are non-NULL, the gradients are also written there in fp32 (same
+ * layouts, contiguous), before rounding to bf16.  Errors as for the calls above, and
+ * OD_ERR_INVALID_ARG for a misaligned optional pointer. */
+od_status od_space_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                               void* o_lo, int B, int T, int S, int Hq, int Hkv, int D,
+                               int agent_idx, float scale, void* stream);
+od_status od_time_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                              void* o_lo, int B, int T, int S, int Hq, int Hkv, int D, int window,
+                              float scale, void* stream);
+od_status od_space_attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                               const void* o_lo, const float* lse, const void* dout, void* dq,
+                               void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                               int B, int T, int S, int Hq, int Hkv, int D, int agent_idx,
+                               float scale, void* workspace, size_t workspace_bytes, void* stream);
+od_status od_time_attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                              const void* o_lo, const float* lse, const void* dout, void* dq,
+                              void* dk, void* dv, float* dq_f32, float* dk_f32, float* dv_f32,
+                              int B, int T, int S, int Hq, int Hkv, int D, int window, float scale,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Packed-QKV forms.  Each layer of the block-causal backbone alternates space and time
  * attention (7minutos.es page, section "Arquitectura: una columna vertebral, dos modelos"),
@@ -143,7 +164,7 @@ od_status od_time_attn_bwd_packed(const void* qkv, const void* o, const void* o_
  * scales with the lengths: tiles and key blocks past a block's length are never loaded or
  * computed.  Padding rows of Q, K, V and dO must hold finite values (zeros will do); the
  * outputs' padding rows (O, LSE, o_lo, dQ, dK, dV and the fp32 copies) are left unchanged.
- * The backward takes the forward's o_lo like od_space_attn_bwd. */
+ * The backward takes the forward's o_lo like od_space_attn_bwd_ex. */
 od_status od_space_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o,
                                    float* lse, void* o_lo, const int* seqlen, int B, int T, int S,
                                    int Hq, int Hkv, int D, int agent_idx, float scale,
@@ -182,11 +203,11 @@ od_status od_time_attn_decode(const void* q, const void* k_new, const void* v_ne
  * code running under an allocator-free runtime, or at a point where cudaMalloc is not
  * allowed or would synchronise the device.  (The Open Dreamer pages have no counterpart;
  * this is a property of this library's interface.)  Same arguments and results as
- * od_space_attn_bwd, minus the workspace: the scratch the backward needs (fp32 per query row
- * plus a fixed 16 KiB of operand ranges) lives in a fixed device array of
+ * od_space_attn_bwd_ex, minus the workspace: the scratch the backward needs (fp32 per query row
+ * plus a fixed 32 KiB of operand ranges) lives in a fixed device array of
  * OD_STATIC_WORKSPACE_BYTES bytes inside the library, which every device that loads the
  * library keeps until the process exits.  Calls for which od_attn_bwd_workspace_bytes(0, ...)
- * exceeds OD_STATIC_WORKSPACE_BYTES (B*T*S*Hq above 4,190,208) are rejected with
+ * exceeds OD_STATIC_WORKSPACE_BYTES (B*T*S*Hq above 4,186,112) are rejected with
  * OD_ERR_WORKSPACE before anything is enqueued.  This call never allocates or frees device
  * memory.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress)
@@ -207,7 +228,14 @@ size_t od_attn_bwd_workspace_bytes(int which, int B, int T, int S, int Hq, int H
 
 /* Synchronises `stream`, then reads and clears the device status word of the current
  * device.  Returns OD_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
- * call, OD_ERR_CUDA if the synchronisation failed, OD_OK otherwise. */
+ * call, OD_ERR_RANGE if a range check of the debug build failed (see below), OD_ERR_CUDA if
+ * the synchronisation failed, OD_OK otherwise.
+ * Debug build: libod_attn_debug.so, the same sources compiled with -DOD_DEBUG, exports the
+ * same calls.  Its kernels check every TMA box start coordinate and every output row index
+ * against the tensor's extent before the access; a failed check skips the access (a TMA
+ * load is still issued -- the hardware clips it -- so that no wait is left without its
+ * bytes), never traps, and is reported as OD_ERR_RANGE with the first check's site word
+ * (bits 31-24: the check site, 200-249; bits 23-0: the CTA index).  Slower; for diagnosis. */
 od_status od_get_device_status(void* stream);
 
 /* As od_get_device_status; if site_word is non-NULL it receives the first expired wait's

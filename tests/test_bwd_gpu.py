@@ -3,7 +3,7 @@
 Gates (the fp32 gradient outputs carry the stated tolerance; bf16 outputs add one rounding):
   fp32 dQ/dK/dV : max |err| <= 1e-2 and mean |err| / mean |ref| <= 2e-3
   bf16 dQ/dK/dV : per element |err| <= max(1e-2, one bf16 ulp of |ref|), and
-                  mean |err| / mean |ref| <= 3e-3 (bf16 rounding of the output alone is ~1.4e-3)
+                  mean |err| / mean |ref| <= 2e-3
 """
 import numpy as np
 import pytest
@@ -44,7 +44,7 @@ def check_bwd(oracle_mod, kind, bits, extra, scale=0.125, what="", with_lo=False
     what = "%s%s" % (what, " (Delta from O + O_lo)" if with_lo else "")
     for name, g, gb, r in zip(("dQ", "dK", "dV"), f32, bf, ref):
         assert_close(g, r, "%s %s %s fp32" % (what, kind, name), bf16_out=False)
-        assert_close(gb, r, "%s %s %s bf16" % (what, kind, name), mean_rel=3e-3)
+        assert_close(gb, r, "%s %s %s bf16" % (what, kind, name))
 
 
 def test_tiny_config_backward(oracle_mod):
@@ -154,7 +154,7 @@ def test_backward_operands_far_from_unit_range(oracle_mod, kind):
     for name, g, gb, r, f in zip(("dQ", "dK", "dV"), f32, bf, ref, factors):
         assert np.isfinite(g).all() and np.isfinite(gb).all()
         assert_close(g / f, r / f, "scaled %s %s fp32" % (kind, name), bf16_out=False)
-        assert_close(gb / f, r / f, "scaled %s %s bf16" % (kind, name), mean_rel=3e-3)
+        assert_close(gb / f, r / f, "scaled %s %s bf16" % (kind, name))
 
 
 @pytest.mark.parametrize("with_lo", [False, True])
@@ -175,3 +175,67 @@ def test_backward_is_deterministic(with_lo):
         for r in runs[1:]:
             for a, b in zip(runs[0][:3] + tuple(runs[0][3]), r[:3] + tuple(r[3])):
                 assert torch.equal(a, b), kind
+
+
+@pytest.mark.parametrize("kind", ["space", "time"])
+def test_backward_single_large_elements_in_v_and_dout(oracle_mod, kind):
+    """N(0,1) V and dO that each carry one element near 1e3-1e4: the power-of-two scales of
+    the fp16 products come from each tensor's largest magnitude, so one large element must not
+    push the typical dS values into fp16's subnormal range."""
+    B, T, S, Hq, Hkv, agent, window = 1, 10, 150, 8, 2, 149, 6
+    q, k, v, do = inputs(B, T, S, Hq, Hkv, seed=5150, with_dout=True)
+    vf, dof = synth.bf16_bits_to_f64(v), synth.bf16_bits_to_f64(do)
+    vf[0, 3, 17, 1, 5] = 3000.0
+    dof[0, 4, 40, 6, 9] = -7000.0
+    bits = (q, k, synth.f64_to_bf16_bits(vf), synth.f64_to_bf16_bits(dof))
+    extra = agent if kind == "space" else window
+    for with_lo in (False, True):
+        bf, f32, ref = run_bwd(oracle_mod, kind, bits, extra, with_lo=with_lo)
+        for name, g, gb, r in zip(("dQ", "dK", "dV"), f32, bf, ref):
+            # the reference gradients are large where the outliers act: judge relative to the
+            # tensor's scale (max err <= 1e-2 * max|ref| is the absolute gate at unit scale)
+            sc = max(1.0, float(np.abs(r).max()) / 10.0)
+            assert_close(g / sc, r / sc, "outliers %s %s fp32 (lo=%s)" % (kind, name, with_lo), bf16_out=False)
+            assert_close(gb / sc, r / sc, "outliers %s %s bf16 (lo=%s)" % (kind, name, with_lo))
+
+
+@pytest.mark.parametrize("kind", ["space", "time"])
+def test_plain_and_extended_calls_agree(kind):
+    """The plain forward/backward calls and the extended ones with every optional pointer
+    NULL run the same kernels: bit-identical O, LSE, dQ, dK, dV (called through the C ABI)."""
+    import ctypes
+    P = ctypes.c_void_p
+    lib = api.library()
+    B, T, S, Hq, Hkv, agent, window = 1, 9, 150, 8, 2, 149, 5
+    q, k, v, do = (to_dev(x) for x in inputs(B, T, S, Hq, Hkv, seed=8181, with_dout=True))
+    extra = agent if kind == "space" else window
+    stream = P(torch.cuda.current_stream().cuda_stream)
+    dims = (B, T, S, Hq, Hkv, 64)
+    ptr = lambda t: P(t.data_ptr())  # noqa: E731
+    res = []
+    for ex in (False, True):
+        o, lse = torch.empty_like(q), torch.empty((B, T, S, Hq), dtype=torch.float32, device="cuda")
+        if ex:
+            st = getattr(lib, "od_%s_attn_fwd_ex" % kind)(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), P(0),
+                                                          *dims, extra, 0.125, stream)
+        else:
+            st = getattr(lib, "od_%s_attn_fwd" % kind)(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), *dims,
+                                                       extra, 0.125, stream)
+        assert st == 0
+        ws = torch.empty(api.bwd_workspace_bytes(0 if kind == "space" else 1, B, T, S, Hq, Hkv),
+                         dtype=torch.uint8, device="cuda")
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        if ex:
+            st = getattr(lib, "od_%s_attn_bwd_ex" % kind)(
+                ptr(q), ptr(k), ptr(v), ptr(o), P(0), ptr(lse), ptr(do), ptr(dq), ptr(dk), ptr(dv),
+                P(0), P(0), P(0), *dims, extra, 0.125, ptr(ws), ws.numel(), stream)
+        else:
+            st = getattr(lib, "od_%s_attn_bwd" % kind)(
+                ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), ptr(do), ptr(dq), ptr(dk), ptr(dv), *dims,
+                extra, 0.125, ptr(ws), ws.numel(), stream)
+        assert st == 0
+        res.append((o, lse, dq, dk, dv))
+    torch.cuda.synchronize()
+    assert api.get_device_status() == 0
+    for name, a, b in zip(("O", "LSE", "dQ", "dK", "dV"), *res):
+        assert torch.equal(a, b), name

@@ -4,9 +4,12 @@ Some callers cannot allocate device memory -- an allocator-free runtime, or code
 where cudaMalloc is not allowed or would synchronise.  For them the library offers a space
 attention backward whose scratch lives in a fixed array inside the library.  These tests call
 it through the C ABI and check that it gives the same gradients as the regular entry point
-(with a caller-provided workspace), on two calls in a row, since every call reuses the same
-array; and that sizes beyond the fixed array are refused before anything runs.  This file is
-collected last on purpose.
+(with a caller-provided workspace) -- bit for bit, since both run the same deterministic
+kernels -- on two calls in a row, since every call reuses the same array, on both Delta routes
+(recomputed, and read from O + O_lo); and that sizes beyond the fixed array are refused before
+anything runs.  The tests build all their inputs themselves and assume nothing about what ran
+before them; the file name only makes pytest collect them last, so that a run that stops at
+the first failure has run every other test first.
 """
 import ctypes
 
@@ -26,38 +29,42 @@ def _ptr(t):
     return P(t.data_ptr()) if t is not None else P(0)
 
 
-def _static_ws_bwd(lib, Q, K, V, O, L, DO, agent, scale, stream):
+def _static_ws_bwd(lib, Q, K, V, O, L, DO, agent, scale, stream, O_lo=None):
     dq, dk, dv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     fq = torch.empty(Q.shape, dtype=torch.float32, device=Q.device)
     fk = torch.empty(K.shape, dtype=torch.float32, device=Q.device)
     fv = torch.empty(V.shape, dtype=torch.float32, device=Q.device)
     B, T, S, Hq, D = Q.shape
     st = lib.od_space_attn_bwd_static_ws(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), P(0), _ptr(L), _ptr(DO), _ptr(dq), _ptr(dk), _ptr(dv),
-        _ptr(fq), _ptr(fk), _ptr(fv), B, T, S, Hq, K.shape[3], D, agent, ctypes.c_float(scale),
-        P(stream.cuda_stream))
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(O_lo), _ptr(L), _ptr(DO), _ptr(dq), _ptr(dk),
+        _ptr(dv), _ptr(fq), _ptr(fk), _ptr(fv), B, T, S, Hq, K.shape[3], D, agent,
+        ctypes.c_float(scale), P(stream.cuda_stream))
     assert st == 0, api.STATUS.get(st, st)
     return (dq, dk, dv), (fq, fk, fv)
 
 
-def test_static_workspace_backward_matches_regular_entry_point():
+@pytest.mark.parametrize("with_lo", [False, True])
+def test_static_workspace_backward_matches_regular_entry_point(with_lo):
     lib = api.library()
     B, T, S, Hq, Hkv, agent, scale = 2, 6, 150, 12, 2, 149, 0.125
     Q, K, V, DO = (to_dev(x) for x in inputs(B, T, S, Hq, Hkv, seed=2024, with_dout=True))
     stream = torch.cuda.current_stream()
-    O, L = api.space_attn_fwd(Q, K, V, agent, scale)
-    ref_bf, ref_f32 = None, None
-    dq, dk, dv, (fq, fk, fv) = api.space_attn_bwd(Q, K, V, O, L, DO, agent, scale, fp32_grads=True)
-    ref_bf = [to_f64(t) for t in (dq, dk, dv)]
-    ref_f32 = [to_f64(t) for t in (fq, fk, fv)]
+    if with_lo:
+        O, L, O_lo = api.space_attn_fwd(Q, K, V, agent, scale, o_lo=True)
+    else:
+        (O, L), O_lo = api.space_attn_fwd(Q, K, V, agent, scale), None
+    dq, dk, dv, (fq, fk, fv) = api.space_attn_bwd(Q, K, V, O, L, DO, agent, scale, fp32_grads=True,
+                                                  o_lo=O_lo)
+    ref = (dq, dk, dv, fq, fk, fv)
     for call in range(2):   # the second call reuses the array the first one left behind
-        got_bf, got_f32 = _static_ws_bwd(lib, Q, K, V, O, L, DO, agent, scale, stream)
+        got_bf, got_f32 = _static_ws_bwd(lib, Q, K, V, O, L, DO, agent, scale, stream, O_lo)
         torch.cuda.synchronize()
         assert api.get_device_status() == 0
-        for name, g, r in zip(("dQ", "dK", "dV"), got_f32, ref_f32):
-            assert_close(to_f64(g), r, "call %d %s fp32" % (call, name), bf16_out=False)
-        for name, g, r in zip(("dQ", "dK", "dV"), got_bf, ref_bf):
-            assert_close(to_f64(g), r, "call %d %s bf16" % (call, name))
+        for name, g, r in zip(("dQ", "dK", "dV", "dQ fp32", "dK fp32", "dV fp32"),
+                              got_bf + got_f32, ref):
+            assert_close(to_f64(g), to_f64(r), "call %d %s" % (call, name),
+                         bf16_out=g.dtype == torch.bfloat16)
+            assert torch.equal(g, r), "call %d %s differs from the regular entry point" % (call, name)
 
 
 def test_static_workspace_refuses_sizes_beyond_the_fixed_array():
