@@ -235,6 +235,48 @@ def oracle_sample(w, nunits, with_bwd):
     return tot_flop, tot_s, nth, desc
 
 
+def oracle_full(w, with_bwd, chunk=48):
+    """Time the fp64 oracle on every unit of the workload (all B*T*Hkv space units and all
+    B*S*Hkv time units, `chunk` units per oracle call to bound host memory); returns
+    (flop, seconds, threads, description) like oracle_sample."""
+    import oracle
+    oracle.build()
+    if w.name not in _INPUTS:
+        _INPUTS[w.name] = synth.make_inputs(w, with_dout=True)
+    q, k, v, dout = _INPUTS[w.name]
+    G = w.G
+    X = oracle.from_bf16
+    f = flops(w)
+    units_space = [(b, t, h) for b in range(w.B) for t in range(w.T) for h in range(w.Hkv)]
+    units_time = [(b, s_, h) for b in range(w.B) for s_ in range(w.S) for h in range(w.Hkv)]
+    nth = oracle.num_threads(0)
+    tot_s = 0.0
+    for kind, units in (("space", units_space), ("time", units_time)):
+        for c0 in range(0, len(units), chunk):
+            part = units[c0:c0 + chunk]
+            if kind == "space":
+                sl = [(slice(b, b + 1), slice(t, t + 1), slice(None)) for b, t, h in part]
+            else:
+                sl = [(slice(b, b + 1), slice(None), slice(s_, s_ + 1)) for b, s_, h in part]
+            hs = [h for _, _, h in part]
+            cq = np.concatenate([X(q[a + (slice(h * G, (h + 1) * G),)]) for a, h in zip(sl, hs)])
+            ck = np.concatenate([X(k[a + (slice(h, h + 1),)]) for a, h in zip(sl, hs)])
+            cv = np.concatenate([X(v[a + (slice(h, h + 1),)]) for a, h in zip(sl, hs)])
+            cd = np.concatenate([X(dout[a + (slice(h * G, (h + 1) * G),)]) for a, h in zip(sl, hs)])
+            extra = w.agent if kind == "space" else w.window
+            t0 = time.perf_counter()
+            if with_bwd:
+                getattr(oracle, kind + "_bwd")(cq, ck, cv, cd, extra, w.scale)
+            else:
+                getattr(oracle, kind + "_fwd")(cq, ck, cv, extra, w.scale)
+            tot_s += time.perf_counter() - t0
+    ops = ["space_fwd", "time_fwd"] + (["space_bwd", "time_bwd"] if with_bwd else [])
+    tot_flop = sum(f[o] for o in ops)
+    desc = "the whole %s workload: %d space units + %d time units, %s" % (
+        w.name, len(units_space), len(units_time), "fwd+bwd" if with_bwd else "fwd")
+    return tot_flop, tot_s, nth, desc
+
+
 def run_reference(args, w, with_bwd):
     rank, world, _ = dist_info()
     if rank != 0:
@@ -244,7 +286,10 @@ def run_reference(args, w, with_bwd):
     for _ in range(args.warmup if args.warmup < 1 else 1):
         oracle_sample(w, max(1, nunits // 8), with_bwd)
     for _ in range(args.steps):
-        fl, s, nth, desc = oracle_sample(w, nunits, with_bwd)
+        if args.oracle_full:
+            fl, s, nth, desc = oracle_full(w, with_bwd)
+        else:
+            fl, s, nth, desc = oracle_sample(w, nunits, with_bwd)
         vals.append((fl, s))
     fl = sum(v[0] for v in vals)
     s = sum(v[1] for v in vals)
@@ -453,7 +498,10 @@ def run_ours(args, w, with_bwd):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.op:
-        fl, s, nth, desc = oracle_sample(w, args.ref_units, with_bwd)
+        if args.oracle_full:
+            fl, s, nth, desc = oracle_full(w, with_bwd)
+        else:
+            fl, s, nth, desc = oracle_sample(w, args.ref_units, with_bwd)
         cpu = {"value": fl / s / 1e12, "unit": UNIT, "cores": nth, "kind": "oracle", "sample": desc}
 
     launches_per_step = {"space_fwd": 1, "time_fwd": 1, "space_bwd": api.BWD_LAUNCHES,
@@ -832,6 +880,9 @@ def main():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--ref-units", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-full", action="store_true",
+                    help="time the oracle on the whole workload instead of a bounded sample "
+                         "(about a minute of host time for minecraft_fwd_bwd)")
     ap.add_argument("--varlen", action="store_true",
                     help="variable-length space attention (fwd+bwd) over seeded MAE block "
                          "lengths, e.g. with --workload tokenizer_enc")

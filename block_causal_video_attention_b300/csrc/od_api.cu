@@ -760,6 +760,11 @@ int od_trace_read(unsigned long long* dst, unsigned int* counts) {
   if (cudaMemcpyToSymbol(g_od_trace_n, zero, sizeof(zero)) != cudaSuccess) return -1;
   return 0;
 }
+// Profiling builds only: selects the kernel whose trace points record (0 forward, 1 dQ
+// pass, 2 dK/dV, 3 Delta pass).  Returns 0, or -1 on a CUDA error.
+int od_trace_select(int kernel) {
+  return cudaMemcpyToSymbol(g_od_trace_sel, &kernel, sizeof(int)) == cudaSuccess ? 0 : -1;
+}
 #endif
 
 }  // extern "C"

@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const bool resident = p.nkb <= kDqStages;
+  OD_TRACE_INIT(kDelta ? 3 : 1);
   // items of this CTA: a contiguous range (consecutive items of a unit share its K/V); for
   // variable-length blocks every gridDim.x-th item, so that items of unequal cost spread
   // over all CTAs
@@ -518,6 +519,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           }
           if (!__all_sync(0xffffffffu, wait_bar(&qb[x], qn & 1u, ctl, status, 14))) break;
           ++qn;
+          OD_TP(90, (int)i, 0);
           auto issue_s = [&](int bi) -> bool {
             const KvSlot ks = slot(bi);
             if (!__all_sync(0xffffffffu, wait_bar(&kb16[ks.stage], ks.parity, ctl, status, 15))) return false;
@@ -543,6 +545,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           for (int bi = 0; bi < nb && ok; ++bi) {
             if (!__all_sync(0xffffffffu, wait_bar(&sm.ds_full[x], jd & 1u, ctl, status, 16))) { ok = false; break; }
             ++jd;
+            OD_TP(91, (int)i, bi);
             tc_fence_after();
             const KvSlot ks = slot(bi);
             if (!kDelta) {
@@ -602,6 +605,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       // dQ pass: S carries 2^(eq + ek) (eq: this Q tile's); dS is written times 2^eds with eds
       // from the row's bound ||dO_i|| 8 max|V| + |Delta_i| on |dS|, and dQ undoes 2^(eds + ek)
       float slx = p.sl, c1 = 1.f, fq = dp.scale;
+      OD_TP(80, (int)i, 0);
       if (!kDelta) {
         ok = __all_sync(0xffffffffu, wait_bar(&sm.q16[x], jq & 1u, ctl, status, 9));
         if (!ok) break;
@@ -636,6 +640,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ++jS;
+        OD_TP(82, (int)i, bi);
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < n32; ++c) {
@@ -667,10 +672,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           }
           tmem_st16(tS + 16 * c, pk);   // dS (fp16 pairs, times 2^eds) over the scores already read
         }
+        OD_TP(83, (int)i, bi);
         if (!kDelta) tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.ds_full[x]);
+        OD_TP(84, (int)i, bi);
       }
       if (!ok) break;
       if (kDelta) {
@@ -686,6 +693,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ++jD;
+      OD_TP(85, (int)i, 0);
       tc_fence_after();
       float o[64];
       tmem_ld32(tQ, o);
@@ -739,6 +747,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
   }
 
+  OD_TRACE_END();
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -919,7 +928,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  OD_TRACE_INIT();
+  OD_TRACE_INIT(2);
 
   {  // tile rows that TMA never writes stay zero (after conversion too)
     const int pad = (kBM - p.rows) * 128;
@@ -1340,6 +1349,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     }
   }
 
+  OD_TRACE_END();
   __syncwarp();
   tc_fence_before();
   __syncthreads();

@@ -10,12 +10,14 @@
 #include "od_ptx.cuh"
 
 // Timeline trace points, compiled out unless OD_TRACE is defined.  A profiling build
-// (nvcc -DOD_TRACE) records, for the CTA with index OD_TRACE_CTA only and lane 0 of each warp,
-// one 64-bit record per trace point into that warp's own region of OD_TRACE_PER_WARP records:
-// the low 32 bits of the SM clock and a word (event << 18) | (a & 0x3FF) << 8 | (b & 0xFF).
-// The record count lives in a register (OD_TRACE_INIT declares it; OD_TRACE_END publishes
-// it), so a trace point costs a clock read and one store.  od_trace_read (C ABI, same build)
-// copies the regions out; the records show where each warp role waits.
+// (nvcc -DOD_TRACE) records, for one kernel at a time (g_od_trace_sel, set by
+// od_trace_select: 0 forward, 1 dQ pass, 2 dK/dV, 3 Delta pass), for the CTA with index
+// OD_TRACE_CTA only and lane 0 of each warp, one 64-bit record per trace point into that
+// warp's own region of OD_TRACE_PER_WARP records: the low 32 bits of the SM clock and a word
+// (event << 18) | (a & 0x3FF) << 8 | (b & 0xFF).  The record count lives in a register
+// (OD_TRACE_INIT declares it; OD_TRACE_END publishes it), so a trace point costs a clock read
+// and one store.  od_trace_read (C ABI, same build) copies the regions out; the records show
+// where each warp role waits.
 #ifdef OD_TRACE
 #ifndef OD_TRACE_CTA
 #define OD_TRACE_CTA 7
@@ -24,8 +26,9 @@
 #define OD_TRACE_PER_WARP 8192
 __device__ unsigned long long g_od_trace[OD_TRACE_WARPS * OD_TRACE_PER_WARP];
 __device__ unsigned int g_od_trace_n[OD_TRACE_WARPS];
-__device__ __forceinline__ void od_trace(unsigned int& n, int ev, int a, int b) {
-  if (blockIdx.x == OD_TRACE_CTA && (threadIdx.x & 31) == 0 && n < OD_TRACE_PER_WARP) {
+__device__ int g_od_trace_sel;
+__device__ __forceinline__ void od_trace(unsigned int& n, bool on, int ev, int a, int b) {
+  if (on && blockIdx.x == OD_TRACE_CTA && (threadIdx.x & 31) == 0 && n < OD_TRACE_PER_WARP) {
     const unsigned long long clk = static_cast<unsigned int>(clock64());
     const unsigned int w = (static_cast<unsigned int>(ev & 0xFF) << 18) |
                            (static_cast<unsigned int>(a & 0x3FF) << 8) | static_cast<unsigned int>(b & 0xFF);
@@ -33,16 +36,18 @@ __device__ __forceinline__ void od_trace(unsigned int& n, int ev, int a, int b) 
   }
   ++n;
 }
-#define OD_TP(ev, a, b) od_trace(od_tn, (ev), (a), (b))
-#define OD_TRACE_INIT() unsigned int od_tn = 0
+#define OD_TP(ev, a, b) od_trace(od_tn, od_ton, (ev), (a), (b))
+#define OD_TRACE_INIT(kid) \
+  unsigned int od_tn = 0;  \
+  const bool od_ton = g_od_trace_sel == (kid)
 #define OD_TRACE_END()                                                                   \
   do {                                                                                   \
-    if (blockIdx.x == OD_TRACE_CTA && (threadIdx.x & 31) == 0)                           \
+    if (od_ton && blockIdx.x == OD_TRACE_CTA && (threadIdx.x & 31) == 0)                 \
       g_od_trace_n[threadIdx.x >> 5] = od_tn < OD_TRACE_PER_WARP ? od_tn : OD_TRACE_PER_WARP; \
   } while (0)
 #else
 #define OD_TP(ev, a, b) ((void)0)
-#define OD_TRACE_INIT() ((void)0)
+#define OD_TRACE_INIT(kid) ((void)0)
 #define OD_TRACE_END() ((void)0)
 #endif
 

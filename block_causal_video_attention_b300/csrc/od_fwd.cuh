@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int istep = strided ? static_cast<int>(gridDim.x) : 1;
   const int i0 = strided ? static_cast<int>(blockIdx.x) : static_cast<int>((p.nitems * blockIdx.x) / gridDim.x);
   const int i1 = strided ? static_cast<int>(p.nitems) : static_cast<int>((p.nitems * (blockIdx.x + 1)) / gridDim.x);
-  OD_TRACE_INIT();
+  OD_TRACE_INIT(0);
 
   // Zero what TMA never writes: Q-tile rows >= p.rows, and K/V stage rows >= p.kvb (packed
   // tiles whose key blocks are shorter than 128 rows; the MMAs read up to 16-row multiples).
