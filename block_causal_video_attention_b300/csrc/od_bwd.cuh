@@ -773,17 +773,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // converter warps rewrite each Q/dO tile in place as scaled fp16 after its TMA load.
 // Warps: 0-3 half 0, 4-7 half 1 (elementwise, then the epilogue: dK by warps 0-3, dV by
 // warps 4-7), 8 TMA producer + per-row LSE/Delta copies, 9 TMEM allocator + MMA issuer
-// (whole warp, one elected lane issues), 10/11 converters (Q / dO).  K/V blocks are
-// double-buffered in shared memory across items; Q/dO tiles stream through kKvQSlots
-// slots.  CTA c takes items c, then 2*grid-1-c, then
-// 2*grid+c, ... so the items in flight at any time are consecutive (the key blocks of one
-// unit share its Q/dO tiles through L2) and alternate between cheaper and dearer blocks.
+// (whole warp, one elected lane issues), 10-15 converters (a third of Q or of dO each: with
+// two converter warps the conversion paced the kernel).  K/V blocks are double-buffered in
+// shared memory across items; Q/dO tiles stream through kKvQSlots slots.  CTA c takes items
+// c, then 2*grid-1-c, then 2*grid+c, ... so the items in flight at any time are consecutive
+// (the key blocks of one unit share its Q/dO tiles through L2) and alternate between cheaper
+// and dearer blocks.
 constexpr int kKvBN = 128;
-constexpr int kKvThreads = 384;
+constexpr int kKvThreads = 512;
+constexpr int kKvLaunchRegs = 128;   // 65536 registers / 512 threads
 constexpr int kKvQSlots = 4;
 constexpr int kKvProducerWarp = 8;
 constexpr int kKvMmaWarp = 9;
-constexpr int kKvConvWarp = 10;
+constexpr int kKvConvWarp = 10;   // warps 10-12 convert Q, 13-15 dO (a third of each tile)
+constexpr int kKvConvParts = 3;
 
 struct KvParams {
   FwdParams f;            // shapes (item fields unused)
@@ -821,8 +824,8 @@ constexpr size_t kKvTileBytes = size_t(4) * kTile + size_t(2 * kKvQSlots) * kTil
 constexpr size_t kKvSmemBytes = kKvTileBytes + 1024 + sizeof(KvSmem) + 64;
 static_assert(kKvSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kKvElemRegs = 176;   // elementwise warpgroups
-constexpr int kKvCtrlRegs = 152;   // producer, issuer, converters
-static_assert(2 * 128 * kKvElemRegs + 128 * kKvCtrlRegs == kKvThreads * kQsLaunchRegs,
+constexpr int kKvCtrlRegs = 80;    // producer, issuer, converters
+static_assert(2 * 128 * kKvElemRegs + 256 * kKvCtrlRegs == kKvThreads * kKvLaunchRegs,
               "register split must add up to the launch allocation");
 
 struct KvItem {
@@ -950,7 +953,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     }
     for (int q = 0; q < kKvQSlots; ++q) {
       mbar_init(&sm.q_full[q], 1 + 32);  // TMA issuer + the producer lanes' row copies
-      mbar_init(&sm.q16[q], 2);
+      mbar_init(&sm.q16[q], 2 * kKvConvParts);
       mbar_init(&sm.q_empty[q], 1);
     }
     mbar_init(&sm.acc_done, 1);
@@ -1168,10 +1171,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         drain_wait(&sm.drain, 0);
       }
     } else {
-      // ---------------------------------------------------------- converters (10: Q, 11: dO)
-      const int which = warp - kKvConvWarp;  // 0: Q, 1: dO
+      // ---------------------------------------------------------- converters (10-15)
+      // Warps 10-12 rewrite a third each of every Q tile's rows as fp16 times 2^eq, warps
+      // 13-15 the same of dO times 2^edo; warp 10 also turns the rows' raw LSE into
+      // -log2(e) LSE and warp 13 the raw Delta into -Delta (0 for rows outside the sequence).
+      const int which = (warp - kKvConvWarp) / kKvConvParts;  // 0: Q, 1: dO
+      const int part = (warp - kKvConvWarp) % kKvConvParts;
       const float sqd = ldexpf(1.f, which ? edo : eq);
       const float rowf = which ? -1.f : -1.4426950408889634f;
+      const int nch = p.rows * 8;                               // 16-byte chunks of a tile
+      const int c0 = (nch * part) / kKvConvParts, c1 = (nch * (part + 1)) / kKvConvParts;
+      int tok_of[4];                                            // (lane + 32 k) / G
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tok_of[k] = (lane + 32 * k) / p.G;
       KvSeq<kVarlen> seq;
       KvItem it;
       uint32_t n = 0, tau = 0;
@@ -1184,18 +1196,23 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           ok = __all_sync(0xffffffffu, wait_bar(&sm.q_full[q], (tau / kKvQSlots) & 1u, ctl, status, 36));
           if (!ok) break;
           OD_TP(71, (int)tau, 0);
-          to_fp16_scaled(sQD + (2 * q + which) * kTile, p.rows * 128, sqd, lane);
-          {  // rows of the tile: -log2(e) LSE (warp 10) or -Delta (warp 11); 0 elsewhere
+          to_fp16_scaled(sQD + (2 * q + which) * kTile + c0 * 16, (c1 - c0) * 16, sqd, lane);
+          OD_TP(72, (int)tau, 0);
+          if (part == 0) {  // rows of the tile: -log2(e) LSE (Q warp) or -Delta (dO warp); 0 elsewhere
             float* rowv = which ? sm.ndel[q] : sm.nlse2[q];
             const int t0 = tq * p.nTok;
-            for (int rr = lane; rr < 128; rr += 32) {
-              const bool valid = rr < p.rows && t0 + rr / p.G < (kVarlen ? it.L : p.L);
+            const int L = kVarlen ? it.L : p.L;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int rr = lane + 32 * k;
+              const bool valid = rr < p.rows && t0 + tok_of[k] < L;
               rowv[rr] = valid ? rowv[rr] * rowf : 0.f;
             }
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.q16[q]);
+          OD_TP(73, (int)tau, 0);
         }
       }
     }
@@ -1384,7 +1401,7 @@ inline cudaError_t bwd_setup_one() {
   if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncGetAttributes(&fa, od_bwd_dkdv_kernel<kVarlen>);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (fa.numRegs != kKvLaunchRegs) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 inline cudaError_t bwd_setup() {
