@@ -316,8 +316,39 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   f.resident = 0;
   f.seqlen = is_time ? nullptr : seqlen;
   f.status = dev->status;
+  f.pk = 0;
   if (f.nitems >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
   if (1LL * B * f.F * Hkv * ((f.L + od::kKvBN - 1) / od::kKvBN) >= (1LL << 31)) return OD_ERR_UNSUPPORTED;
+  // Short time sequences (G T <= 64) are packed: a Q tile holds pk token positions x all T
+  // frames (rows (t pk + sp) G + g) and its key block the same positions' frames.  The dQ
+  // passes take pk with pk T <= kBN keys per block, the dK/dV kernel pk with pk T G <= 128.
+  od::FwdParams fk = f;   // the dK/dV kernel's tiling
+  f.kvb = od::kBN;
+  fk.kvb = od::kKvBN;
+  const int Gq = Hq / Hkv;
+  if (is_time && Gq * T <= 64) {
+    const int pk_dq = od::kBM / (Gq * T) < od::kBN / T ? od::kBM / (Gq * T) : od::kBN / T;
+    if (pk_dq >= 2) {
+      f.pk = pk_dq;
+      f.F = (S + 2 * pk_dq - 1) / (2 * pk_dq);
+      f.nTok = T;
+      f.rows = pk_dq * T * Gq;
+      f.ntiles = 2;
+      f.npairs = 1;
+      f.nitems = 1LL * B * f.F * Hkv;
+      f.rcp_npairs = od::host_div_rcp(f.npairs);
+      f.rcp_f = od::host_div_rcp(f.F);
+      f.kvb = pk_dq * T;
+      f.nkb = 2;
+    }
+    const int pk_kv = od::kBM / (Gq * T);
+    fk.pk = pk_kv;
+    fk.F = (S + pk_kv - 1) / pk_kv;
+    fk.nTok = T;
+    fk.rows = pk_kv * T * Gq;
+    fk.ntiles = 1;
+    fk.kvb = pk_kv * T;
+  }
 
   float* delta = static_cast<float*>(workspace);
   float* amax = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
@@ -326,7 +357,8 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   int amax_slots = 0, dq_slots = 0;
   const uint32_t qbox_space[5] = {64, (uint32_t)f.G, (uint32_t)f.nTok, 1, 1};
   const uint32_t qbox_time[5] = {64, (uint32_t)f.G, 1, (uint32_t)f.nTok, 1};
-  const uint32_t* qbox = is_time ? qbox_time : qbox_space;
+  const uint32_t qbox_packed[5] = {64, (uint32_t)f.G, (uint32_t)f.pk, (uint32_t)T, 1};
+  const uint32_t* qbox = f.pk ? qbox_packed : (is_time ? qbox_time : qbox_space);
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tq, tdo, tk, tv;
@@ -337,7 +369,8 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   {
     const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kBN, 1, 1};
     const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kBN, 1};
-    const uint32_t* kbox = is_time ? kbox_time : kbox_space;
+    const uint32_t kbox_packed[5] = {64, 1, (uint32_t)f.pk, (uint32_t)T, 1};
+    const uint32_t* kbox = f.pk ? kbox_packed : (is_time ? kbox_time : kbox_space);
     if ((st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)) ||
         (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)))
       return st;
@@ -390,17 +423,29 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
   {
     const uint32_t kbox_space[5] = {64, 1, (uint32_t)od::kKvBN, 1, 1};
     const uint32_t kbox_time[5] = {64, 1, 1, (uint32_t)od::kKvBN, 1};
-    const uint32_t* kbox = is_time ? kbox_time : kbox_space;
+    const uint32_t kbox_packed[5] = {64, 1, (uint32_t)fk.pk, (uint32_t)T, 1};
+    const uint32_t* kbox = fk.pk ? kbox_packed : (is_time ? kbox_time : kbox_space);
     if ((st = make_map(&tk, k, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)) ||
         (st = make_map(&tv, v, bf, 2, B, T, S, Hkv, D, kbox, sw, kv_rows)))
       return st;
+    if (fk.pk) {   // Q/dO tiles of pk token positions x all T frames
+      const uint32_t qbox_kv[5] = {64, (uint32_t)fk.G, (uint32_t)fk.pk, (uint32_t)T, 1};
+      if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, qbox_kv, sw, q_rows)) ||
+          (st = make_map(&tdo, dout, bf, 2, B, T, S, Hq, D, qbox_kv, sw, Hq)))
+        return st;
+    } else if (f.pk) {   // the dQ passes used packed boxes: back to the forward's tiles
+      const uint32_t* qb = is_time ? qbox_time : qbox_space;
+      if ((st = make_map(&tq, q, bf, 2, B, T, S, Hq, D, qb, sw, q_rows)) ||
+          (st = make_map(&tdo, dout, bf, 2, B, T, S, Hq, D, qb, sw, Hq)))
+        return st;
+    }
     od::KvParams kp{};
-    kp.f = f;
+    kp.f = fk;
     kp.lse = lse;
     kp.delta = delta;
     kp.scale = scale;
-    kp.nkb = (f.L + od::kKvBN - 1) / od::kKvBN;
-    kp.nitems = 1LL * B * f.F * Hkv * kp.nkb;
+    kp.nkb = fk.pk ? 1 : (fk.L + od::kKvBN - 1) / od::kKvBN;
+    kp.nitems = 1LL * B * fk.F * Hkv * kp.nkb;
     kp.dk = static_cast<__nv_bfloat16*>(dk);
     kp.dv = static_cast<__nv_bfloat16*>(dv);
     kp.kv_rows = kv_rows;

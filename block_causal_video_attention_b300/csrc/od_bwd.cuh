@@ -215,13 +215,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const long long i0 = strided ? blockIdx.x : (p.nitems * blockIdx.x) / gridDim.x;
   const long long i1 = strided ? p.nitems : (p.nitems * (blockIdx.x + 1)) / gridDim.x;
 
-  {  // zero the tile rows TMA never writes
+  {  // zero the tile rows TMA never writes (and, packed, the K/V stage rows past pk T keys)
     const int pad = (kBM - p.rows) * 128;
     for (int x = tid * 16; x < pad; x += kDqThreads * 16)
       for (int t = 0; t < 2; ++t) {
         *reinterpret_cast<uint4*>(sQ[t] + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(sdO[t] + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
       }
+    const int kvpad = (kBN - p.kvb) * 128;
+    for (int x = tid * 16; x < kvpad; x += kDqThreads * 16)
+      for (int st = 0; st < 2 * kDqStages; ++st)
+        *reinterpret_cast<uint4*>(sK + st * kKVTile + p.kvb * 128 + x) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   if (tid == 0) {
@@ -395,34 +399,30 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
           const int nb = it.kb_hi - it.kb_lo + 1;
           auto load_kv = [&](int stage, int kb) {
+            // box start (s, t): packed time, time, space
             const int kp = kb * kBN;
-            (void)OD_TMA_OK(it.kvh, p.is_time ? it.fixed : kp, p.is_time ? kp : it.fixed, it.b, p.Hkv,
-                            p.S, p.T, p.B, status, 210);
-            mbar_arrive_expect_tx(&sm.k_full[stage], kKVTile);
-            mbar_arrive_expect_tx(&sm.v_full[stage], kKVTile);
-            if (p.is_time) {
-              tma_load_5d(sK + stage * kKVTile, &tm_k, &sm.k_full[stage], 0, it.kvh, it.fixed, kp, it.b);
-              tma_load_5d(sV + stage * kKVTile, &tm_v, &sm.v_full[stage], 0, it.kvh, it.fixed, kp, it.b);
-            } else {
-              tma_load_5d(sK + stage * kKVTile, &tm_k, &sm.k_full[stage], 0, it.kvh, kp, it.fixed, it.b);
-              tma_load_5d(sV + stage * kKVTile, &tm_v, &sm.v_full[stage], 0, it.kvh, kp, it.fixed, it.b);
-            }
+            const int cs = p.pk ? it.tok0[0] + kb * p.pk : (p.is_time ? it.fixed : kp);
+            const int ct = p.pk ? 0 : (p.is_time ? kp : it.fixed);
+            // (a packed unit without a tile B loads its second block from past the end on
+            // purpose: TMA fills it with zeros, and every stage's phase count stays equal)
+            if (!p.pk || kb == 0 || it.validB)
+              (void)OD_TMA_OK(it.kvh, cs, ct, it.b, p.Hkv, p.S, p.T, p.B, status, 210);
+            mbar_arrive_expect_tx(&sm.k_full[stage], p.kvb * 128);
+            mbar_arrive_expect_tx(&sm.v_full[stage], p.kvb * 128);
+            tma_load_5d(sK + stage * kKVTile, &tm_k, &sm.k_full[stage], 0, it.kvh, cs, ct, it.b);
+            tma_load_5d(sV + stage * kKVTile, &tm_v, &sm.v_full[stage], 0, it.kvh, cs, ct, it.b);
           };
           for (int x = 0; x < 2 && ok; ++x) {
             if (x == 1 && !it.validB) break;
             if (qn[x] > 0) ok = wait_bar(&sm.q_empty[x], (qn[x] - 1) & 1u, ctl, status, 1);
             if (!ok) break;
             const int t0 = x ? it.tok0[1] : it.tok0[0];
-            (void)OD_TMA_OK(it.kvh * p.G, p.is_time ? it.fixed : t0, p.is_time ? t0 : it.fixed, it.b,
-                            p.Hq, p.S, p.T, p.B, status, 211);
+            const int cs = p.pk ? t0 : (p.is_time ? it.fixed : t0);
+            const int ct = p.pk ? 0 : (p.is_time ? t0 : it.fixed);
+            (void)OD_TMA_OK(it.kvh * p.G, cs, ct, it.b, p.Hq, p.S, p.T, p.B, status, 211);
             mbar_arrive_expect_tx(&sm.q_full[x], 2 * p.rows * 128);
-            if (p.is_time) {
-              tma_load_5d(sQ[x], &tm_q, &sm.q_full[x], 0, it.kvh * p.G, it.fixed, t0, it.b);
-              tma_load_5d(sdO[x], &tm_do, &sm.q_full[x], 0, it.kvh * p.G, it.fixed, t0, it.b);
-            } else {
-              tma_load_5d(sQ[x], &tm_q, &sm.q_full[x], 0, it.kvh * p.G, t0, it.fixed, it.b);
-              tma_load_5d(sdO[x], &tm_do, &sm.q_full[x], 0, it.kvh * p.G, t0, it.fixed, it.b);
-            }
+            tma_load_5d(sQ[x], &tm_q, &sm.q_full[x], 0, it.kvh * p.G, cs, ct, it.b);
+            tma_load_5d(sdO[x], &tm_do, &sm.q_full[x], 0, it.kvh * p.G, cs, ct, it.b);
             ++qn[x];
           }
           if (!ok) break;
@@ -520,12 +520,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (!__all_sync(0xffffffffu, wait_bar(&qb[x], qn & 1u, ctl, status, 14))) break;
           ++qn;
           OD_TP(90, (int)i, 0);
+          // this tile's blocks (packed: its own block only; packed units are always resident)
+          const int b0 = (x ? it.blo[1] : it.blo[0]) - it.kb_lo, b1 = (x ? it.bhi[1] : it.bhi[0]) - it.kb_lo;
           auto issue_s = [&](int bi) -> bool {
             const KvSlot ks = slot(bi);
             if (!__all_sync(0xffffffffu, wait_bar(&kb16[ks.stage], ks.parity, ctl, status, 15))) return false;
             if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 15))) return false;
             tc_fence_after();
-            const int n = round16(block_ncols(it, it.kb_lo + bi, kBN));
+            const int n = round16(block_keys(p, it, it.kb_lo + bi, kBN));
             const uint32_t idesc = idesc_bf16(128, n, 0, 0);
             const uint32_t idesc_s = kDelta ? idesc : idesc_fp16(128, n, 0, 0);
             const uint64_t aq = sdesc_sw128(smem_u32(sQ[x]), 16, 1024);
@@ -538,24 +540,24 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             for (int k = 0; k < 4; ++k) mma_ss_w(tP, ado + 2 * k, bv + 2 * k, idesc, k > 0);
             mma_commit_w(&sm.s_full[x]);
             ++js;
-            if (bi == nb - 1) mma_commit_w(&sm.q_empty[x]);
+            if (bi == b1) mma_commit_w(&sm.q_empty[x]);
             return true;
           };
-          ok = issue_s(0);
-          for (int bi = 0; bi < nb && ok; ++bi) {
+          ok = issue_s(b0);
+          for (int bi = b0; bi <= b1 && ok; ++bi) {
             if (!__all_sync(0xffffffffu, wait_bar(&sm.ds_full[x], jd & 1u, ctl, status, 16))) { ok = false; break; }
             ++jd;
             OD_TP(91, (int)i, bi);
             tc_fence_after();
             const KvSlot ks = slot(bi);
             if (!kDelta) {
-              const int ksteps = round16(block_ncols(it, it.kb_lo + bi, kBN)) >> 4;
+              const int ksteps = round16(block_keys(p, it, it.kb_lo + bi, kBN)) >> 4;
               const uint64_t bk = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 1024, 1024);
               for (int k = 0; k < ksteps; ++k)
-                mma_ts_w(tQ, tS + 8 * k, bk + (2048 >> 4) * k, idesc_dq, (bi > 0 || k > 0));
+                mma_ts_w(tQ, tS + 8 * k, bk + (2048 >> 4) * k, idesc_dq, (bi > b0 || k > 0));
             }
             if (!resident) mma_commit_w(&sm.kv_empty[ks.stage]);
-            if (bi == nb - 1) {
+            if (bi == b1) {
               if (!kDelta) mma_commit_w(&sm.dq_done[x]);
             } else {
               ok = issue_s(bi + 1);
@@ -585,16 +587,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const FwdItem it = fwd_decode<kVarlen>(p, i);
       if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
       if (x == 1 && !it.validB) continue;
-      const int nb = it.kb_hi - it.kb_lo + 1;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
-      const int pos = mytok0 + tok;
+      // the row's sequence position pos (packed: its frame; sp its token within the tile)
+      const int pt = p.pk ? tok / p.pk : 0;
+      const int sp = p.pk ? tok - pt * p.pk : 0;
+      const int pos = p.pk ? pt : mytok0 + tok;
       long long row = 0;
       float lse2 = INFINITY, dl = 0.f;
       float dacc[4] = {0.f, 0.f, 0.f, 0.f};
-      bool row_ok = (r < p.rows) && (pos < (kVarlen ? it.L : p.L));
+      bool row_ok = (r < p.rows) && (p.pk ? mytok0 + sp < p.S : pos < (kVarlen ? it.L : p.L));
       if (row_ok) {
         const long long t_idx = p.is_time ? pos : it.fixed;
-        const long long s_idx = p.is_time ? it.fixed : pos;
+        const long long s_idx = p.pk ? mytok0 + sp : (p.is_time ? it.fixed : pos);
         row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + g;
         row_ok = OD_IN_RANGE(row, static_cast<long long>(p.B) * p.T * p.S * p.Hq, status, 212);
       }
@@ -622,12 +626,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const float ndl = -dl * c1;
       const float2 sl2 = make_float2(slx, slx), c12 = make_float2(c1, c1), nd2 = make_float2(ndl, ndl);
       const float2 nl2 = make_float2(-lse2, -lse2);
-      for (int bi = 0; bi < nb; ++bi) {
-        const int kbase = (it.kb_lo + bi) * kBN;
-        const int ncols = block_ncols(it, it.kb_lo + bi, kBN);
+      const int kb_first = x ? it.blo[1] : it.blo[0], kb_last = x ? it.bhi[1] : it.bhi[0];
+      for (int kb = kb_first; kb <= kb_last; ++kb) {
+        const int bi = kb - it.kb_lo;
+        const int kbase = kb * kBN;
+        const int ncols = block_keys(p, it, kb, kBN);
         const int n32 = (ncols + 31) >> 5;
         int lo, hi, ex;
-        if (p.is_time) {
+        if (p.pk) {   // frames [lo, hi] of the row's own token (see keep_bits_packed)
+          lo = max(0, pos - p.window + 1);
+          hi = pos;
+          ex = -1;
+        } else if (p.is_time) {
           lo = pos - p.window + 1 - kbase;
           hi = min(ncols, pos + 1 - kbase);
           ex = -1;
@@ -649,7 +659,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tmem_ld32(tP + 32 * c, pv);
           tmem_wait_ld_dep32(sv);
           tmem_wait_ld_dep32(pv);
-          const uint32_t keep = keep_bits32(32 * c, lo, hi, ex);
+          const uint32_t keep = p.pk ? keep_bits_packed(32 * c, p.pk, sp, lo, hi) : keep_bits32(32 * c, lo, hi, ex);
           if (kDelta) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -726,10 +736,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const int rt = (warp & 3) * 32 + rr;
           const int tk = rt / G;
           const int gg = rt - tk * G;
-          const int ps = mytok0 + tk;
-          if (rt < p.rows && ps < (kVarlen ? it.L : p.L)) {
+          const int tp = p.pk ? tk / p.pk : 0;                 // packed: frame and token
+          const int spp = p.pk ? tk - tp * p.pk : 0;
+          const int ps = p.pk ? tp : mytok0 + tk;
+          if (rt < p.rows && (p.pk ? mytok0 + spp < p.S : ps < (kVarlen ? it.L : p.L))) {
             const long long t_idx = p.is_time ? ps : it.fixed;
-            const long long s_idx = p.is_time ? it.fixed : ps;
+            const long long s_idx = p.pk ? mytok0 + spp : (p.is_time ? it.fixed : ps);
             const long long rw =
                 ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * dp.dq_rows + it.kvh * G + gg;
             const uint4 wv = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
@@ -846,6 +858,12 @@ __device__ __forceinline__ KvItem kv_decode(const KvParams& kp, long long i) {
   const uint32_t bq = r / static_cast<uint32_t>(p.F);
   it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
   it.b = static_cast<int>(bq);
+  if (p.pk) {  // packed time attention: `fixed` counts groups of pk token positions
+    it.L = p.L;
+    it.valid = 1;
+    it.t_lo = it.t_hi = 0;
+    return it;
+  }
   int L = p.L;
   if (kVarlen) L = min(max(__ldg(p.seqlen + static_cast<long long>(it.b) * p.T + it.fixed), 0), p.L);
   it.L = L;
@@ -938,6 +956,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     for (int x = tid * 16; x < pad; x += kKvThreads * 16)
       for (int t = 0; t < 2 * kKvQSlots; ++t)
         *reinterpret_cast<uint4*>(sQD + t * kTile + p.rows * 128 + x) = make_uint4(0, 0, 0, 0);
+    const int kvpad = (kKvBN - p.kvb) * 128;   // packed: K/V rows past the block's pk T keys
+    for (int x = tid * 16; x < kvpad; x += kKvThreads * 16)
+      for (int t = 0; t < 4; ++t)
+        *reinterpret_cast<uint4*>(sKV + t * kTile + p.kvb * 128 + x) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     for (int x = tid; x < kKvQSlots * 128; x += kKvThreads) {
       (&sm.nlse2[0][0])[x] = 0.f;
@@ -1005,19 +1027,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (!ok) break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.kv_full[slot], 2 * kKvBN * 128);
+          mbar_arrive_expect_tx(&sm.kv_full[slot], 2 * p.kvb * 128);
           const int k0 = it.kb * kKvBN;
-          (void)OD_TMA_OK(it.kvh, p.is_time ? it.fixed : k0, p.is_time ? k0 : it.fixed, it.b, p.Hkv,
-                          p.S, p.T, p.B, status, 220);
+          // box start (s, t): packed time, time, space
+          const int cs = p.pk ? it.fixed * p.pk : (p.is_time ? it.fixed : k0);
+          const int ct = p.pk ? 0 : (p.is_time ? k0 : it.fixed);
+          (void)OD_TMA_OK(it.kvh, cs, ct, it.b, p.Hkv, p.S, p.T, p.B, status, 220);
           uint8_t* dK = sKV + (2 * slot) * kTile;
           uint8_t* dV = sKV + (2 * slot + 1) * kTile;
-          if (p.is_time) {
-            tma_load_5d(dK, &tm_k, &sm.kv_full[slot], 0, it.kvh, it.fixed, k0, it.b);
-            tma_load_5d(dV, &tm_v, &sm.kv_full[slot], 0, it.kvh, it.fixed, k0, it.b);
-          } else {
-            tma_load_5d(dK, &tm_k, &sm.kv_full[slot], 0, it.kvh, k0, it.fixed, it.b);
-            tma_load_5d(dV, &tm_v, &sm.kv_full[slot], 0, it.kvh, k0, it.fixed, it.b);
-          }
+          tma_load_5d(dK, &tm_k, &sm.kv_full[slot], 0, it.kvh, cs, ct, it.b);
+          tma_load_5d(dV, &tm_v, &sm.kv_full[slot], 0, it.kvh, cs, ct, it.b);
         }
         ++n;
         for (int tq = it.t_lo; tq <= it.t_hi && ok; ++tq, ++tau) {
@@ -1029,29 +1048,28 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             if (!ok) break;
           }
           const int t0 = tq * p.nTok;
+          const int s0 = it.fixed * p.pk;   // packed: the block's first token position
           if (lane == 0) {
-            (void)OD_TMA_OK(it.kvh * p.G, p.is_time ? it.fixed : t0, p.is_time ? t0 : it.fixed, it.b,
-                            p.Hq, p.S, p.T, p.B, status, 221);
+            const int cs = p.pk ? s0 : (p.is_time ? it.fixed : t0);
+            const int ct = p.pk ? 0 : (p.is_time ? t0 : it.fixed);
+            (void)OD_TMA_OK(it.kvh * p.G, cs, ct, it.b, p.Hq, p.S, p.T, p.B, status, 221);
             uint8_t* dQ = sQD + (2 * q) * kTile;
             uint8_t* dO = sQD + (2 * q + 1) * kTile;
             mbar_arrive_expect_tx(&sm.q_full[q], 2 * p.rows * 128);
-            if (p.is_time) {
-              tma_load_5d(dQ, &tm_q, &sm.q_full[q], 0, it.kvh * p.G, it.fixed, t0, it.b);
-              tma_load_5d(dO, &tm_do, &sm.q_full[q], 0, it.kvh * p.G, it.fixed, t0, it.b);
-            } else {
-              tma_load_5d(dQ, &tm_q, &sm.q_full[q], 0, it.kvh * p.G, t0, it.fixed, it.b);
-              tma_load_5d(dO, &tm_do, &sm.q_full[q], 0, it.kvh * p.G, t0, it.fixed, it.b);
-            }
+            tma_load_5d(dQ, &tm_q, &sm.q_full[q], 0, it.kvh * p.G, cs, ct, it.b);
+            tma_load_5d(dO, &tm_do, &sm.q_full[q], 0, it.kvh * p.G, cs, ct, it.b);
           }
           // raw LSE and Delta of the tile's rows, copied asynchronously (the converters
           // rescale them); rows outside the sequence keep finite stale values, which only
           // ever meet the zero Q/dO rows of the tile
           for (int rr = lane; rr < p.rows; rr += 32) {
             const int tk = rr / p.G;
-            const int ps = t0 + tk;
-            if (ps < (kVarlen ? it.L : p.L)) {
+            const int tpk = p.pk ? tk / p.pk : 0;
+            const int sp = p.pk ? tk - tpk * p.pk : 0;
+            const int ps = p.pk ? tpk : t0 + tk;
+            if (p.pk ? s0 + sp < p.S : ps < (kVarlen ? it.L : p.L)) {
               const long long t_idx = p.is_time ? ps : it.fixed;
-              const long long s_idx = p.is_time ? it.fixed : ps;
+              const long long s_idx = p.pk ? s0 + sp : (p.is_time ? it.fixed : ps);
               const long long row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq +
                                     it.kvh * p.G + (rr - tk * p.G);
               cp_async4(&sm.nlse2[q][rr], kp.lse + row);
@@ -1183,7 +1201,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int c0 = (nch * part) / kKvConvParts, c1 = (nch * (part + 1)) / kKvConvParts;
       int tok_of[4];                                            // (lane + 32 k) / G
 #pragma unroll
-      for (int k = 0; k < 4; ++k) tok_of[k] = (lane + 32 * k) / p.G;
+      for (int k = 0; k < 4; ++k) {
+        tok_of[k] = (lane + 32 * k) / p.G;
+        if (p.pk) tok_of[k] %= p.pk;                            // packed: the row's token
+      }
       KvSeq<kVarlen> seq;
       KvItem it;
       uint32_t n = 0, tau = 0;
@@ -1205,7 +1226,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int rr = lane + 32 * k;
-              const bool valid = rr < p.rows && t0 + tok_of[k] < L;
+              const bool valid = rr < p.rows && (p.pk ? it.fixed * p.pk + tok_of[k] < p.S : t0 + tok_of[k] < L);
               rowv[rr] = valid ? rowv[rr] * rowf : 0.f;
             }
           }
@@ -1238,7 +1259,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     uint32_t n = 0, tau = 0;
     bool ok = true;
     while (ok && seq.next(kp, &it)) {
-      const int kpos = it.kb * kKvBN + j;
+      // the key's sequence position kpos (packed: its frame; spk its token within the block)
+      const int tkj = p.pk ? j / p.pk : 0;
+      const int spk = p.pk ? j - tkj * p.pk : 0;
+      const int kpos = p.pk ? tkj : it.kb * kKvBN + j;
+      const bool key_ok = p.pk ? (j < p.kvb && it.fixed * p.pk + spk < p.S) : kpos < (kVarlen ? it.L : p.L);
       {  // this key's K (half 0) or V (half 1) row -> scaled fp16 -> TMEM A operand columns.
          // The previous item's MMAs have all completed (its epilogue waited for them).
         const int slot = n & 1;
@@ -1304,7 +1329,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         for (int c = 0; c < 2; ++c) {
           const float* NL = &sm.nlse2[q][64 * h + 32 * c];
           const float* ND = &sm.ndel[q][64 * h + 32 * c];
-          const uint32_t keep = keep_bits32(64 * h + 32 * c, r_lo, r_hi, -1);
+          const uint32_t keep =
+              p.pk ? (key_ok ? keep_rows_packed(64 * h + 32 * c, p.G, p.pk, spk, kpos, min(p.L - 1, kpos + Weff - 1)) : 0u)
+                   : keep_bits32(64 * h + 32 * c, r_lo, r_hi, -1);
           uint32_t pk[16], dk[16];
           if (__any_sync(0xffffffffu, keep != 0xFFFFFFFFu))
             dkdv_chunk<true>(sv + 32 * c, dv + 32 * c, NL, ND, sl2, c12, sj2, keep, pk, dk);
@@ -1338,10 +1365,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.acc_free);
-      if (kpos < (kVarlen ? it.L : p.L)) {
+      if (key_ok) {
         const float f = h ? ldexpf(1.f, -edo) : kp.scale * ldexpf(1.f, -(eds + eq));
         const long long t_idx = p.is_time ? kpos : it.fixed;
-        const long long s_idx = p.is_time ? it.fixed : kpos;
+        const long long s_idx = p.pk ? it.fixed * p.pk + spk : (p.is_time ? it.fixed : kpos);
         const long long tok = (static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx;
         if (!OD_IN_RANGE(tok, static_cast<long long>(p.B) * p.T * p.S, status, 222)) continue;
         const long long row = tok * p.Hkv + it.kvh;

@@ -80,6 +80,13 @@ struct FwdParams {
   long long nitems;
   int bn;         // keys per key block
   int nkb;        // key blocks per unit
+  // packed time attention (short sequences, G T <= 64): a Q tile holds pk token positions x
+  // all T frames x G heads, rows (t pk + sp) G + g, and its key block the same positions'
+  // T frames, keys t pk + sp; query (t, sp) reads key (t', sp') iff sp' == sp and
+  // t - window < t' <= t.  A unit is (b, 2 pk positions, kv head): tile x holds positions
+  // [unit's first + x pk, + pk) and reads key block x only.  0: not packed.
+  int pk;
+  int kvb;        // keys a K/V block load brings in: bn, or pk T when packed
   int resident;   // nkb <= K/V stages: the unit's K/V stay in smem across its items
   // reciprocals for the item decode: floor(2^64 / d) + 1 for d = npairs, Hkv, F (0 when
   // d >= 2^16, where the plain division is used)
@@ -103,7 +110,8 @@ struct FwdItem {
   int validA;          // 0: tile A starts past the unit's length -- nothing to do
   int validB;
   int key_lo, key_hi;  // allowed key positions of the item lie in [key_lo, key_hi)
-  int kb_lo, kb_hi;    // inclusive key-block range
+  int kb_lo, kb_hi;    // inclusive key-block range of the item
+  int blo[2], bhi[2];  // inclusive key-block range of tile x
 };
 
 // n / d for n < 2^32 and 1 < d < 2^16 with rcp = floor(2^64 / d) + 1: the product's error
@@ -133,6 +141,20 @@ __device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
   const uint32_t bq = div_rcp(r, static_cast<uint32_t>(p.F), p.rcp_f);
   it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
   it.b = static_cast<int>(bq);
+  if (p.pk) {  // packed time attention: `fixed` counts groups of 2 pk token positions
+    it.L = p.L;
+    it.tok0[0] = it.fixed * 2 * p.pk;
+    it.tok0[1] = it.tok0[0] + p.pk;
+    it.validA = 1;
+    it.validB = it.tok0[1] < p.S;
+    it.key_lo = 0;
+    it.key_hi = 2 * p.kvb;
+    it.kb_lo = 0;
+    it.kb_hi = it.validB ? 1 : 0;
+    it.blo[0] = it.bhi[0] = 0;
+    it.blo[1] = it.bhi[1] = 1;
+    return it;
+  }
   int L = p.L;
   if (kVarlen) L = min(max(__ldg(p.seqlen + static_cast<long long>(it.b) * p.T + it.fixed), 0), p.L);
   it.L = L;
@@ -151,11 +173,42 @@ __device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
   }
   it.kb_lo = it.key_lo / p.bn;
   it.kb_hi = (!kVarlen || it.validA) ? (it.key_hi - 1) / p.bn : it.kb_lo - 1;  // none if skipped
+  it.blo[0] = it.blo[1] = it.kb_lo;
+  it.bhi[0] = it.bhi[1] = it.kb_hi;
   return it;
 }
 
 __device__ __forceinline__ int block_ncols(const FwdItem& it, int kb, int bn) {
   return min(bn, it.key_hi - kb * bn);
+}
+// Keys of block kb that the tile's rows may read (packed: the block's pk T keys).
+__device__ __forceinline__ int block_keys(const FwdParams& p, const FwdItem& it, int kb, int bn) {
+  return p.pk ? p.kvb : block_ncols(it, kb, bn);
+}
+
+// Packed time attention, one query row (frame t, position sp within the tile): bit j set
+// <=> key c0 + j = t' pk + sp with tlo <= t' <= thi.
+__device__ __forceinline__ uint32_t keep_bits_packed(int c0, int pk, int sp, int tlo, int thi) {
+  uint32_t m = 0u;
+  for (int tt = max(tlo, (c0 - sp + pk - 1) / pk); tt <= thi; ++tt) {
+    const int c = tt * pk + sp - c0;
+    if (c >= 32) break;
+    m |= 1u << c;
+  }
+  return m;
+}
+// Packed time attention, one key (frame t', position spk within the block): bit j set <=>
+// row r0 + j = (t pk + spk) G + g with tlo <= t <= thi and 0 <= g < G.
+__device__ __forceinline__ uint32_t keep_rows_packed(int r0, int G, int pk, int spk, int tlo, int thi) {
+  uint32_t m = 0u;
+  const int d = r0 / G - spk;   // frames before this one hold rows below r0
+  for (int tt = max(tlo, d > 0 ? d / pk : 0); tt <= thi; ++tt) {
+    const int c = (tt * pk + spk) * G - r0;   // the frame's G rows are [c, c + G)
+    if (c >= 32) break;
+    const int lo = max(c, 0), hi = min(c + G, 32);
+    if (lo < hi) m |= (hi == 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
+  }
+  return m;
 }
 __device__ __forceinline__ int round16(int x) { return (x + 15) & ~15; }
 

@@ -239,3 +239,27 @@ def test_plain_and_extended_calls_agree(kind):
     assert api.get_device_status() == 0
     for name, a, b in zip(("O", "LSE", "dQ", "dK", "dV"), *res):
         assert torch.equal(a, b), name
+
+
+# Short time sequences are packed in the backward (G T <= 64: several token positions per
+# tile, block-diagonal mask): T in {1, 3, 32, 33} x G in {1, 2}, S with a partial last group
+# of token positions, windows shorter than, equal to and longer than T.
+PACKED_SHAPES = [
+    # B, T, S, Hq, Hkv, window
+    (2, 1, 37, 2, 2, 1),
+    (1, 1, 130, 4, 2, 3),
+    (2, 3, 41, 2, 2, 2),
+    (1, 3, 50, 4, 2, 3),
+    (1, 32, 13, 2, 2, 7),
+    (2, 32, 9, 4, 2, 32),
+    (1, 33, 11, 2, 2, 40),
+    (1, 33, 7, 4, 2, 5),
+]
+
+
+@pytest.mark.parametrize("shape", PACKED_SHAPES)
+@pytest.mark.parametrize("with_lo", [False, True])
+def test_time_backward_short_sequences_packed(oracle_mod, shape, with_lo):
+    B, T, S, Hq, Hkv, window = shape
+    bits = inputs(B, T, S, Hq, Hkv, seed=700 + 7 * T + S, with_dout=True)
+    check_bwd(oracle_mod, "time", bits, window, 0.125, "packed %s" % (shape,), with_lo=with_lo)

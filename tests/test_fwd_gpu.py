@@ -207,3 +207,25 @@ def test_output_residual(oracle_mod, kind):
     e_hi = np.abs(hi - ro).mean() / np.abs(ro).mean()
     e_both = np.abs(both - ro).mean() / np.abs(ro).mean()
     assert e_both < 0.25 * e_hi and np.abs(both - ro).max() <= 2e-3, (e_hi, e_both)
+
+
+# Short time sequences are packed in the forward too (G T <= 64); every output element is
+# written (O and LSE start as NaN), including partial last groups of token positions.
+PACKED_TIME_SHAPES = [
+    # B, T, S, Hq, Hkv, window
+    (2, 1, 37, 2, 2, 1),
+    (1, 1, 130, 4, 2, 3),
+    (2, 3, 41, 2, 2, 2),
+    (1, 3, 50, 4, 2, 3),
+    (1, 32, 13, 2, 2, 7),
+    (2, 32, 9, 4, 2, 32),
+    (1, 33, 11, 2, 2, 40),
+    (1, 33, 7, 4, 2, 5),
+]
+
+
+@pytest.mark.parametrize("shape", PACKED_TIME_SHAPES)
+def test_time_forward_short_sequences_packed(oracle_mod, shape):
+    B, T, S, Hq, Hkv, window = shape
+    bits = inputs(B, T, S, Hq, Hkv, seed=500 + 7 * T + S)
+    check(oracle_mod, "time", bits, window, 0.125, "packed %s" % (shape,))
