@@ -72,7 +72,7 @@ od_status device_state(DeviceState** out) {
         reinterpret_cast<const void*>(od::od_attn_fwd_kernel<true, od::kModeSpace, false>),
         reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false, od::kModeTime, true>),
         reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false, od::kModeTime, false>),
-        reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false, od::kModeTimePacked, true>)};
+        reinterpret_cast<const void*>(od::od_attn_fwd_kernel<false, od::kModeTimePacked, false>)};
     for (const void* fn : fwd_fns) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(od::kFwdSmemBytes)) != cudaSuccess)
@@ -200,7 +200,7 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   p.rcp_npairs = od::host_div_rcp(p.npairs);
   p.rcp_hkv = od::host_div_rcp(p.Hkv);
   p.rcp_f = od::host_div_rcp(p.F);
-  p.resident = p.nkb <= od::kFwdStages;
+  p.resident = !packed && p.nkb <= od::kFwdStages;
   p.lse = lse;
   p.status = dev->status;
 
@@ -252,7 +252,9 @@ od_status launch_fwd(int is_time, const void* q, const void* k, const void* v, v
   } else if (p.mode == od::kModeTime) {
     if (res) OD_FWD_LAUNCH(false, od::kModeTime, true); else OD_FWD_LAUNCH(false, od::kModeTime, false);
   } else {
-    OD_FWD_LAUNCH(false, od::kModeTimePacked, true);  // packed units always fit (2 blocks)
+    // packed: every item is a new unit of 2 blocks; streaming them through the stages lets
+    // the next item's blocks load while this one computes
+    OD_FWD_LAUNCH(false, od::kModeTimePacked, false);
   }
 #undef OD_FWD_LAUNCH
   return cudaGetLastError() == cudaSuccess ? OD_OK : OD_ERR_CUDA;

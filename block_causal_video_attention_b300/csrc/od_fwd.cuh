@@ -175,6 +175,7 @@ struct FwdSlot {
   int stage;
   uint32_t parity;
 };
+// blk: the key block; s: its fill ordinal within the item (blk - ulo)
 template <bool kRes>
 __device__ __forceinline__ FwdSlot fwd_slot(int blk, int s, uint32_t unit_loads,
                                             uint32_t stream_base) {
@@ -540,7 +541,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll 1
           for (int s = 0; s < nb && ok; ++s) {
             const int blk = lo + s;
-            const FwdSlot f = fwd_slot<kRes>(blk, s, unit_loads, stream_cnt);
+            const FwdSlot f = fwd_slot<kRes>(blk, blk - it.ulo, unit_loads, stream_cnt);
             if (s == 0) {
               qs = qn & 1;
               ok = __all_sync(0xffffffffu, wait_bar(&sm.q_full[x][qs], (qn >> 1) & 1u, ctl, status, 12));
@@ -586,8 +587,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           if (!ok) break;
           if (!kRes) {
-            // fills of the item this tile did not use (no rows here): observe and release them
-            for (int s = nb; s < nload && ok; ++s) {
+            // fills of the item this tile did not use (no rows here, or, packed, the other
+            // tile's block): observe and release them
+            for (int s = 0; s < nload && ok; ++s) {
+              if (s >= lo - it.ulo && s < lo - it.ulo + nb) continue;
               const FwdSlot f = fwd_slot<kRes>(it.ulo + s, s, unit_loads, stream_cnt);
               ok = __all_sync(0xffffffffu, wait_bar(&sm.k_full[f.stage], f.parity, ctl, status, 15) &&
                                            wait_bar(&sm.v16_ready[f.stage], f.parity, ctl, status, 16));
@@ -798,7 +801,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         OD_TP(8, i, s);
         // the V stage's scale exponent (its keys hold fp16(v * 2^e)); O is kept in the
         // scale of the item's latest block and rescaled when that changes
-        const FwdSlot fs = fwd_slot<kRes>(blk, s, unit_loads, stream_cnt);
+        const FwdSlot fs = fwd_slot<kRes>(blk, blk - it.ulo, unit_loads, stream_cnt);
         ok = __all_sync(0xffffffffu, wait_bar(&sm.v16_ready[fs.stage], fs.parity, ctl, status, 22));
         if (!ok) break;
         const int ev = sm.vexp[fs.stage];
