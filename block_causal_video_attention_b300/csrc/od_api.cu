@@ -410,15 +410,19 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
       od::od_bwd_delta_o_kernel<<<(unsigned)dgrid, od::kDeltaOThreads, 0, strm>>>(d);
     } else {
       if (f.seqlen)
-        od::od_bwd_dq_kernel<true, true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+        od::od_bwd_dq_kernel<true, true, false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+      else if (f.pk)
+        od::od_bwd_dq_kernel<true, false, true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
       else
-        od::od_bwd_dq_kernel<true, false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+        od::od_bwd_dq_kernel<true, false, false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
     }
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
     if (f.seqlen)
-      od::od_bwd_dq_kernel<false, true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+      od::od_bwd_dq_kernel<false, true, false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+    else if (f.pk)
+      od::od_bwd_dq_kernel<false, false, true><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
     else
-      od::od_bwd_dq_kernel<false, false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
+      od::od_bwd_dq_kernel<false, false, false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
   }
   // 3. dK, dV
@@ -458,9 +462,11 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     kp.dq_slots = dq_slots;
     const long long grid = kp.nitems < num_ctas ? kp.nitems : num_ctas;
     if (f.seqlen)
-      od::od_bwd_dkdv_kernel<true><<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
+      od::od_bwd_dkdv_kernel<true, false><<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
+    else if (fk.pk)
+      od::od_bwd_dkdv_kernel<false, true><<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
     else
-      od::od_bwd_dkdv_kernel<false><<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
+      od::od_bwd_dkdv_kernel<false, false><<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);
     if (cudaGetLastError() != cudaSuccess) return OD_ERR_CUDA;
   }
   return OD_OK;

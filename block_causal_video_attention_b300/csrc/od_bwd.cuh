@@ -9,10 +9,10 @@
 // Three launches, no atomics, no zeroed workspace (results are deterministic):
 //   1. Delta per row in fp32 into the caller's workspace, and the operand ranges.  Given O's
 //        rounding residual O_lo from the forward: od_bwd_delta_o_kernel, Delta = <dO, O + O_lo>
-//        streamed from memory.  Otherwise od_bwd_dq_kernel<true>, Delta = sum_j P_j dP_j
+//        streamed from memory.  Otherwise od_bwd_dq_kernel<true, ...>, Delta = sum_j P_j dP_j
 //        (equal to <dO, O> for the exact O; the bf16 O alone would give Delta only to ~1e-2
 //        absolute, which the gradients inherit).
-//   2. od_bwd_dq_kernel<false>: Q-tile stationary (the forward's work items and warp roles):
+//   2. od_bwd_dq_kernel<false, ...>: Q-tile stationary (the forward's work items and warp roles):
 //        S = Q K^T and dP = dO V^T per 96-key block in TMEM; dS written in place over S as
 //        fp16 times 2^eds; dQ += dS K into one fp32 accumulator, written once per tile.  Q
 //        tiles and K blocks are rewritten as scaled fp16 in shared memory first (see "fp16
@@ -186,12 +186,15 @@ static_assert(kDqSmemBytes <= 227 * 1024, "shared memory budget");
 // kDelta = true: the Delta pass -- S and dP per key block, Delta = sum_j P_j dP_j accumulated
 // in fp32 per row and written to the workspace (no dS, no dQ).  This is <dO, O> for the exact
 // forward output, which the bf16 O given to the backward only approximates.
-template <bool kDelta, bool kVarlen>
+// kPacked: packed short time sequences (PK; see FwdParams), a separate instantiation so
+// that the other calls compile without its branches
+template <bool kDelta, bool kVarlen, bool kPacked>
 __global__ void __launch_bounds__(kDqThreads, 1)
     od_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DqParams dp) {
   const FwdParams& p = dp.f;
+  const int PK = kPacked ? p.pk : 0;   // packed: token positions per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         return true;
       };
       for (long long i = i0; i < i1 && ok; i += istep) {
-        const FwdItem it = fwd_decode<kVarlen>(p, i);
+        const FwdItem it = fwd_decode<kVarlen, kPacked>(p, i);
         if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
         const int nb = it.kb_hi - it.kb_lo + 1;
         for (int x = 0; x < 2 && ok; ++x) {
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
       bool ok = true;
       for (long long i = i0; i < i1 && ok; i += istep) {
-        const FwdItem it = fwd_decode<kVarlen>(p, i);
+        const FwdItem it = fwd_decode<kVarlen, kPacked>(p, i);
         if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
         const int nb = it.kb_hi - it.kb_lo + 1;
         for (int x = 0; x < 2 && ok; ++x) {
@@ -395,17 +398,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         uint32_t unit_loads = 0, sbase = 0, qn[2] = {0, 0};
         bool ok = true;
         for (long long i = i0; i < i1 && ok; i += istep) {
-          const FwdItem it = fwd_decode<kVarlen>(p, i);
+          const FwdItem it = fwd_decode<kVarlen, kPacked>(p, i);
           if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
           const int nb = it.kb_hi - it.kb_lo + 1;
           auto load_kv = [&](int stage, int kb) {
             // box start (s, t): packed time, time, space
             const int kp = kb * kBN;
-            const int cs = p.pk ? it.tok0[0] + kb * p.pk : (p.is_time ? it.fixed : kp);
-            const int ct = p.pk ? 0 : (p.is_time ? kp : it.fixed);
+            const int cs = PK ? it.tok0[0] + kb * PK : (p.is_time ? it.fixed : kp);
+            const int ct = PK ? 0 : (p.is_time ? kp : it.fixed);
             // (a packed unit without a tile B loads its second block from past the end on
             // purpose: TMA fills it with zeros, and every stage's phase count stays equal)
-            if (!p.pk || kb == 0 || it.validB)
+            if (!PK || kb == 0 || it.validB)
               (void)OD_TMA_OK(it.kvh, cs, ct, it.b, p.Hkv, p.S, p.T, p.B, status, 210);
             mbar_arrive_expect_tx(&sm.k_full[stage], p.kvb * 128);
             mbar_arrive_expect_tx(&sm.v_full[stage], p.kvb * 128);
@@ -417,8 +420,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (qn[x] > 0) ok = wait_bar(&sm.q_empty[x], (qn[x] - 1) & 1u, ctl, status, 1);
             if (!ok) break;
             const int t0 = x ? it.tok0[1] : it.tok0[0];
-            const int cs = p.pk ? t0 : (p.is_time ? it.fixed : t0);
-            const int ct = p.pk ? 0 : (p.is_time ? t0 : it.fixed);
+            const int cs = PK ? t0 : (p.is_time ? it.fixed : t0);
+            const int ct = PK ? 0 : (p.is_time ? t0 : it.fixed);
             (void)OD_TMA_OK(it.kvh * p.G, cs, ct, it.b, p.Hq, p.S, p.T, p.B, status, 211);
             mbar_arrive_expect_tx(&sm.q_full[x], 2 * p.rows * 128);
             tma_load_5d(sQ[x], &tm_q, &sm.q_full[x], 0, it.kvh * p.G, cs, ct, it.b);
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         long long prev_unit = -1;
         bool ok = true;
         for (long long i = i0; i < i1 && ok; i += istep) {
-          const FwdItem it = fwd_decode<kVarlen>(p, i);
+          const FwdItem it = fwd_decode<kVarlen, kPacked>(p, i);
           if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
           const int nb = it.kb_hi - it.kb_lo + 1;
           if (resident && it.unit != prev_unit) {
@@ -527,7 +530,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (!__all_sync(0xffffffffu, wait_bar(&kb16[ks.stage], ks.parity, ctl, status, 15))) return false;
             if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 15))) return false;
             tc_fence_after();
-            const int n = round16(block_keys(p, it, it.kb_lo + bi, kBN));
+            const int n = round16(block_keys<kPacked>(p, it, it.kb_lo + bi, kBN));
             const uint32_t idesc = idesc_bf16(128, n, 0, 0);
             const uint32_t idesc_s = kDelta ? idesc : idesc_fp16(128, n, 0, 0);
             const uint64_t aq = sdesc_sw128(smem_u32(sQ[x]), 16, 1024);
@@ -551,7 +554,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tc_fence_after();
             const KvSlot ks = slot(bi);
             if (!kDelta) {
-              const int ksteps = round16(block_keys(p, it, it.kb_lo + bi, kBN)) >> 4;
+              const int ksteps = round16(block_keys<kPacked>(p, it, it.kb_lo + bi, kBN)) >> 4;
               const uint64_t bk = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 1024, 1024);
               for (int k = 0; k < ksteps; ++k)
                 mma_ts_w(tQ, tS + 8 * k, bk + (2048 >> 4) * k, idesc_dq, (bi > b0 || k > 0));
@@ -584,21 +587,21 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint32_t dmax = 0u;  // Delta pass: max |Delta| of this thread's rows (float bits; NaN on top)
     bool ok = true;
     for (long long i = i0; i < i1 && ok; i += istep) {
-      const FwdItem it = fwd_decode<kVarlen>(p, i);
+      const FwdItem it = fwd_decode<kVarlen, kPacked>(p, i);
       if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
       if (x == 1 && !it.validB) continue;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
       // the row's sequence position pos (packed: its frame; sp its token within the tile)
-      const int pt = p.pk ? tok / p.pk : 0;
-      const int sp = p.pk ? tok - pt * p.pk : 0;
-      const int pos = p.pk ? pt : mytok0 + tok;
+      const int pt = PK ? tok / PK : 0;
+      const int sp = PK ? tok - pt * PK : 0;
+      const int pos = PK ? pt : mytok0 + tok;
       long long row = 0;
       float lse2 = INFINITY, dl = 0.f;
       float dacc[4] = {0.f, 0.f, 0.f, 0.f};
-      bool row_ok = (r < p.rows) && (p.pk ? mytok0 + sp < p.S : pos < (kVarlen ? it.L : p.L));
+      bool row_ok = (r < p.rows) && (PK ? mytok0 + sp < p.S : pos < (kVarlen ? it.L : p.L));
       if (row_ok) {
         const long long t_idx = p.is_time ? pos : it.fixed;
-        const long long s_idx = p.pk ? mytok0 + sp : (p.is_time ? it.fixed : pos);
+        const long long s_idx = PK ? mytok0 + sp : (p.is_time ? it.fixed : pos);
         row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + g;
         row_ok = OD_IN_RANGE(row, static_cast<long long>(p.B) * p.T * p.S * p.Hq, status, 212);
       }
@@ -630,10 +633,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       for (int kb = kb_first; kb <= kb_last; ++kb) {
         const int bi = kb - it.kb_lo;
         const int kbase = kb * kBN;
-        const int ncols = block_keys(p, it, kb, kBN);
+        const int ncols = block_keys<kPacked>(p, it, kb, kBN);
         const int n32 = (ncols + 31) >> 5;
         int lo, hi, ex;
-        if (p.pk) {   // frames [lo, hi] of the row's own token (see keep_bits_packed)
+        if (PK) {   // frames [lo, hi] of the row's own token (see keep_bits_packed)
           lo = max(0, pos - p.window + 1);
           hi = pos;
           ex = -1;
@@ -659,7 +662,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tmem_ld32(tP + 32 * c, pv);
           tmem_wait_ld_dep32(sv);
           tmem_wait_ld_dep32(pv);
-          const uint32_t keep = p.pk ? keep_bits_packed(32 * c, p.pk, sp, lo, hi) : keep_bits32(32 * c, lo, hi, ex);
+          const uint32_t keep = PK ? keep_bits_packed(32 * c, PK, sp, lo, hi) : keep_bits32(32 * c, lo, hi, ex);
           if (kDelta) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -736,12 +739,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const int rt = (warp & 3) * 32 + rr;
           const int tk = rt / G;
           const int gg = rt - tk * G;
-          const int tp = p.pk ? tk / p.pk : 0;                 // packed: frame and token
-          const int spp = p.pk ? tk - tp * p.pk : 0;
-          const int ps = p.pk ? tp : mytok0 + tk;
-          if (rt < p.rows && (p.pk ? mytok0 + spp < p.S : ps < (kVarlen ? it.L : p.L))) {
+          const int tp = PK ? tk / PK : 0;                 // packed: frame and token
+          const int spp = PK ? tk - tp * PK : 0;
+          const int ps = PK ? tp : mytok0 + tk;
+          if (rt < p.rows && (PK ? mytok0 + spp < p.S : ps < (kVarlen ? it.L : p.L))) {
             const long long t_idx = p.is_time ? ps : it.fixed;
-            const long long s_idx = p.pk ? mytok0 + spp : (p.is_time ? it.fixed : ps);
+            const long long s_idx = PK ? mytok0 + spp : (p.is_time ? it.fixed : ps);
             const long long rw =
                 ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * dp.dq_rows + it.kvh * G + gg;
             const uint4 wv = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
@@ -846,7 +849,7 @@ struct KvItem {
   int valid;       // 0: the key block starts past the unit's length (skipped by every role)
   int t_lo, t_hi;  // Q tiles [t_lo, t_hi] that can see the key block
 };
-template <bool kVarlen>
+template <bool kVarlen, bool kPacked>
 __device__ __forceinline__ KvItem kv_decode(const KvParams& kp, long long i) {
   const FwdParams& p = kp.f;
   KvItem it;
@@ -858,7 +861,7 @@ __device__ __forceinline__ KvItem kv_decode(const KvParams& kp, long long i) {
   const uint32_t bq = r / static_cast<uint32_t>(p.F);
   it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
   it.b = static_cast<int>(bq);
-  if (p.pk) {  // packed time attention: `fixed` counts groups of pk token positions
+  if (kPacked && p.pk) {  // packed time attention: `fixed` counts groups of pk positions
     it.L = p.L;
     it.valid = 1;
     it.t_lo = it.t_hi = 0;
@@ -881,7 +884,7 @@ __device__ __forceinline__ KvItem kv_decode(const KvParams& kp, long long i) {
 }
 
 // The CTA's item sequence: round r takes item r*grid + c (r even) or r*grid + grid-1-c.
-template <bool kVarlen>
+template <bool kVarlen, bool kPacked>
 struct KvSeq {
   long long round = 0;
   __device__ __forceinline__ bool next(const KvParams& kp, KvItem* it) {
@@ -892,7 +895,7 @@ struct KvSeq {
                                       : static_cast<long long>(blockIdx.x);
       ++round;
       if (base + c < kp.nitems) {
-        *it = kv_decode<kVarlen>(kp, base + c);
+        *it = kv_decode<kVarlen, kPacked>(kp, base + c);
         if (!kVarlen || it->valid) return true;  // blocks past the length: no role sees them
       }
     }
@@ -933,12 +936,13 @@ __device__ __forceinline__ void dkdv_chunk(const float* sv, const float* dv, con
 }
 
 
-template <bool kVarlen>
+template <bool kVarlen, bool kPacked>
 __global__ void __launch_bounds__(kKvThreads, 1)
     od_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const KvParams kp) {
   const FwdParams& p = kp.f;
+  const int PK = kPacked ? p.pk : 0;   // packed: token positions per key block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1016,7 +1020,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     regs_dec<kKvCtrlRegs>();
     if (warp == kKvProducerWarp) {
       // ---------------------------------------------------------- producer (whole warp)
-      KvSeq<kVarlen> seq;
+      KvSeq<kVarlen, kPacked> seq;
       KvItem it;
       uint32_t n = 0, tau = 0;
       bool ok = true;
@@ -1030,8 +1034,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mbar_arrive_expect_tx(&sm.kv_full[slot], 2 * p.kvb * 128);
           const int k0 = it.kb * kKvBN;
           // box start (s, t): packed time, time, space
-          const int cs = p.pk ? it.fixed * p.pk : (p.is_time ? it.fixed : k0);
-          const int ct = p.pk ? 0 : (p.is_time ? k0 : it.fixed);
+          const int cs = PK ? it.fixed * PK : (p.is_time ? it.fixed : k0);
+          const int ct = PK ? 0 : (p.is_time ? k0 : it.fixed);
           (void)OD_TMA_OK(it.kvh, cs, ct, it.b, p.Hkv, p.S, p.T, p.B, status, 220);
           uint8_t* dK = sKV + (2 * slot) * kTile;
           uint8_t* dV = sKV + (2 * slot + 1) * kTile;
@@ -1048,10 +1052,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             if (!ok) break;
           }
           const int t0 = tq * p.nTok;
-          const int s0 = it.fixed * p.pk;   // packed: the block's first token position
+          const int s0 = it.fixed * PK;   // packed: the block's first token position
           if (lane == 0) {
-            const int cs = p.pk ? s0 : (p.is_time ? it.fixed : t0);
-            const int ct = p.pk ? 0 : (p.is_time ? t0 : it.fixed);
+            const int cs = PK ? s0 : (p.is_time ? it.fixed : t0);
+            const int ct = PK ? 0 : (p.is_time ? t0 : it.fixed);
             (void)OD_TMA_OK(it.kvh * p.G, cs, ct, it.b, p.Hq, p.S, p.T, p.B, status, 221);
             uint8_t* dQ = sQD + (2 * q) * kTile;
             uint8_t* dO = sQD + (2 * q + 1) * kTile;
@@ -1064,12 +1068,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           // ever meet the zero Q/dO rows of the tile
           for (int rr = lane; rr < p.rows; rr += 32) {
             const int tk = rr / p.G;
-            const int tpk = p.pk ? tk / p.pk : 0;
-            const int sp = p.pk ? tk - tpk * p.pk : 0;
-            const int ps = p.pk ? tpk : t0 + tk;
-            if (p.pk ? s0 + sp < p.S : ps < (kVarlen ? it.L : p.L)) {
+            const int tpk = PK ? tk / PK : 0;
+            const int sp = PK ? tk - tpk * PK : 0;
+            const int ps = PK ? tpk : t0 + tk;
+            if (PK ? s0 + sp < p.S : ps < (kVarlen ? it.L : p.L)) {
               const long long t_idx = p.is_time ? ps : it.fixed;
-              const long long s_idx = p.pk ? s0 + sp : (p.is_time ? it.fixed : ps);
+              const long long s_idx = PK ? s0 + sp : (p.is_time ? it.fixed : ps);
               const long long row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq +
                                     it.kvh * p.G + (rr - tk * p.G);
               cp_async4(&sm.nlse2[q][rr], kp.lse + row);
@@ -1100,7 +1104,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const uint32_t idesc_sp = idesc_fp16(128, 64, 0, 0);   // M keys, N 64 tile rows
         const uint32_t idesc_acc = idesc_fp16(128, 64, 0, 1);  // M keys, N head dim, B MN-major
         const uint32_t tDK = tmem + 256, tDV = tmem + 320;
-        KvSeq<kVarlen> seq;
+        KvSeq<kVarlen, kPacked> seq;
         KvItem cur, nxt;
         bool ok = seq.next(kp, &cur);
         uint32_t n = 0, tau = 0;      // item and tile ordinals of the current tile
@@ -1203,9 +1207,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         tok_of[k] = (lane + 32 * k) / p.G;
-        if (p.pk) tok_of[k] %= p.pk;                            // packed: the row's token
+        if (PK) tok_of[k] %= PK;                            // packed: the row's token
       }
-      KvSeq<kVarlen> seq;
+      KvSeq<kVarlen, kPacked> seq;
       KvItem it;
       uint32_t n = 0, tau = 0;
       bool ok = true;
@@ -1226,7 +1230,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int rr = lane + 32 * k;
-              const bool valid = rr < p.rows && (p.pk ? it.fixed * p.pk + tok_of[k] < p.S : t0 + tok_of[k] < L);
+              const bool valid = rr < p.rows && (PK ? it.fixed * PK + tok_of[k] < p.S : t0 + tok_of[k] < L);
               rowv[rr] = valid ? rowv[rr] * rowf : 0.f;
             }
           }
@@ -1254,16 +1258,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     float2 sj2 = make_float2(1.f, 1.f);
     const int Weff = min(p.window, p.L);
     const float skv = ldexpf(1.f, h ? ev : ek);
-    KvSeq<kVarlen> seq;
+    KvSeq<kVarlen, kPacked> seq;
     KvItem it;
     uint32_t n = 0, tau = 0;
     bool ok = true;
     while (ok && seq.next(kp, &it)) {
       // the key's sequence position kpos (packed: its frame; spk its token within the block)
-      const int tkj = p.pk ? j / p.pk : 0;
-      const int spk = p.pk ? j - tkj * p.pk : 0;
-      const int kpos = p.pk ? tkj : it.kb * kKvBN + j;
-      const bool key_ok = p.pk ? (j < p.kvb && it.fixed * p.pk + spk < p.S) : kpos < (kVarlen ? it.L : p.L);
+      const int tkj = PK ? j / PK : 0;
+      const int spk = PK ? j - tkj * PK : 0;
+      const int kpos = PK ? tkj : it.kb * kKvBN + j;
+      const bool key_ok = PK ? (j < p.kvb && it.fixed * PK + spk < p.S) : kpos < (kVarlen ? it.L : p.L);
       {  // this key's K (half 0) or V (half 1) row -> scaled fp16 -> TMEM A operand columns.
          // The previous item's MMAs have all completed (its epilogue waited for them).
         const int slot = n & 1;
@@ -1330,7 +1334,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const float* NL = &sm.nlse2[q][64 * h + 32 * c];
           const float* ND = &sm.ndel[q][64 * h + 32 * c];
           const uint32_t keep =
-              p.pk ? (key_ok ? keep_rows_packed(64 * h + 32 * c, p.G, p.pk, spk, kpos, min(p.L - 1, kpos + Weff - 1)) : 0u)
+              PK ? (key_ok ? keep_rows_packed(64 * h + 32 * c, p.G, PK, spk, kpos, min(p.L - 1, kpos + Weff - 1)) : 0u)
                    : keep_bits32(64 * h + 32 * c, r_lo, r_hi, -1);
           uint32_t pk[16], dk[16];
           if (__any_sync(0xffffffffu, keep != 0xFFFFFFFFu))
@@ -1368,7 +1372,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (key_ok) {
         const float f = h ? ldexpf(1.f, -edo) : kp.scale * ldexpf(1.f, -(eds + eq));
         const long long t_idx = p.is_time ? kpos : it.fixed;
-        const long long s_idx = p.pk ? it.fixed * p.pk + spk : (p.is_time ? it.fixed : kpos);
+        const long long s_idx = PK ? it.fixed * PK + spk : (p.is_time ? it.fixed : kpos);
         const long long tok = (static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx;
         if (!OD_IN_RANGE(tok, static_cast<long long>(p.B) * p.T * p.S, status, 222)) continue;
         const long long row = tok * p.Hkv + it.kvh;
@@ -1404,36 +1408,37 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 }
 
 // ============================================================================ host side
-template <bool kVarlen>
+template <bool kVarlen, bool kPacked>
 inline cudaError_t bwd_setup_one() {
-  cudaError_t e = cudaFuncSetAttribute(od_bwd_dq_kernel<false, kVarlen>,
+  cudaError_t e = cudaFuncSetAttribute(od_bwd_dq_kernel<false, kVarlen, kPacked>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kDqSmemBytes));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(od_bwd_dq_kernel<true, kVarlen>,
+  e = cudaFuncSetAttribute(od_bwd_dq_kernel<true, kVarlen, kPacked>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kDqSmemBytes));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(od_bwd_dkdv_kernel<kVarlen>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(od_bwd_dkdv_kernel<kVarlen, kPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kKvSmemBytes));
   if (e != cudaSuccess) return e;
   // each kernel redistributes its launch registers between warpgroups (setmaxnreg); the split
   // is only valid for the register count it was designed for
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<false, kVarlen>);
+  e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<false, kVarlen, kPacked>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<true, kVarlen>);
+  e = cudaFuncGetAttributes(&fa, od_bwd_dq_kernel<true, kVarlen, kPacked>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kQsLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncGetAttributes(&fa, od_bwd_dkdv_kernel<kVarlen>);
+  e = cudaFuncGetAttributes(&fa, od_bwd_dkdv_kernel<kVarlen, kPacked>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kKvLaunchRegs) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 inline cudaError_t bwd_setup() {
-  cudaError_t e = bwd_setup_one<false>();
-  return e != cudaSuccess ? e : bwd_setup_one<true>();
+  cudaError_t e = bwd_setup_one<false, false>();
+  if (e == cudaSuccess) e = bwd_setup_one<true, false>();
+  return e != cudaSuccess ? e : bwd_setup_one<false, true>();
 }
 
 // ============================================================================ Delta from O

@@ -128,7 +128,7 @@ inline unsigned long long host_div_rcp(int d) {
 
 // kVarlen: space attention over variable-length blocks (p.seqlen); false compiles the
 // fixed-length decode with no trace of the per-unit length.
-template <bool kVarlen>
+template <bool kVarlen, bool kPacked = false>
 __device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
   // the host guarantees nitems < 2^31, so 32-bit unsigned division suffices
   FwdItem it;
@@ -141,7 +141,7 @@ __device__ __forceinline__ FwdItem fwd_decode(const FwdParams& p, long long i) {
   const uint32_t bq = div_rcp(r, static_cast<uint32_t>(p.F), p.rcp_f);
   it.fixed = static_cast<int>(r - bq * static_cast<uint32_t>(p.F));
   it.b = static_cast<int>(bq);
-  if (p.pk) {  // packed time attention: `fixed` counts groups of 2 pk token positions
+  if (kPacked && p.pk) {  // packed time attention: `fixed` counts groups of 2 pk positions
     it.L = p.L;
     it.tok0[0] = it.fixed * 2 * p.pk;
     it.tok0[1] = it.tok0[0] + p.pk;
@@ -182,8 +182,9 @@ __device__ __forceinline__ int block_ncols(const FwdItem& it, int kb, int bn) {
   return min(bn, it.key_hi - kb * bn);
 }
 // Keys of block kb that the tile's rows may read (packed: the block's pk T keys).
+template <bool kPacked>
 __device__ __forceinline__ int block_keys(const FwdParams& p, const FwdItem& it, int kb, int bn) {
-  return p.pk ? p.kvb : block_ncols(it, kb, bn);
+  return (kPacked && p.pk) ? p.kvb : block_ncols(it, kb, bn);
 }
 
 // Packed time attention, one query row (frame t, position sp within the tile): bit j set
