@@ -71,13 +71,13 @@ def bwd_bytes(w):
 # --metrics dram__bytes_read.sum,dram__bytes_write.sum (summary in profiles/).  They hold only
 # for the kernel sources they were measured on: any change to those sources voids them.
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "3ff18123058f3f120c1d5f148fccbd550af52b58f5367062bc56505c6811e471",
+    "csrc_sha256": "24bfc45e830631d77b72d77c5ced37b38398b13c33f90b10bcd02b769b45b853",
     "minecraft_fwd_bwd": {
         # forward with the O residual; backward: Delta from O + O_lo, dQ, dK/dV
-        "space_fwd": 927212800,
-        "time_fwd": 924575744,
-        "space_bwd": 2883645440,
-        "time_bwd": 2897797888,
+        "space_fwd": 919097088,
+        "time_fwd": 916945971,
+        "space_bwd": 2594633984,
+        "time_bwd": 2610208154,
     },
     # decode: 4-rollout capture (176.43 MB read, 5.53 MB written) scaled by the units (x4)
     "minecraft_decode": {"decode": 727837696},
