@@ -45,7 +45,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
-  int delta_o_ctas = 0;  // resident CTAs of the Delta-from-O kernel (one wave), <= kAmaxSlots
+  int range_ctas = 0;    // resident CTAs of the K/V range kernel (one wave), <= kAmaxSlots
   unsigned int* status = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
@@ -84,11 +84,11 @@ od_status device_state(DeviceState** out) {
     if (od::bwd_setup() != cudaSuccess) return OD_ERR_CUDA;
     {
       int per_sm = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, od::od_bwd_delta_o_kernel,
-                                                        od::kDeltaOThreads, 0) != cudaSuccess ||
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, od::od_bwd_kv_range_kernel,
+                                                        od::kKvRangeThreads, 0) != cudaSuccess ||
           per_sm < 1)
         return OD_ERR_CUDA;
-      d.delta_o_ctas = per_sm * d.num_sms < od::kAmaxSlots ? per_sm * d.num_sms : od::kAmaxSlots;
+      d.range_ctas = per_sm * d.num_sms < od::kAmaxSlots ? per_sm * d.num_sms : od::kAmaxSlots;
     }
     if (cudaFuncSetAttribute(od::od_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(od::kDecSmemBytes)) != cudaSuccess)
@@ -389,25 +389,22 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     amax_slots = static_cast<int>(grid);
     dq_slots = static_cast<int>(grid);
     dp.amax_slots = amax_slots;
-    // 1. Delta (from O and its residual when the forward wrote it, else the Delta pass),
-    // 2. dQ
+    // 1. the K/V ranges (the dQ pass forms Delta from O and its residual when the forward
+    // wrote it), else the Delta pass; 2. dQ
     if (o_lo) {
-      od::DeltaOParams d{};
-      d.o = static_cast<const __nv_bfloat16*>(o);
-      d.o_lo = static_cast<const __nv_bfloat16*>(o_lo);
-      d.dout = static_cast<const __nv_bfloat16*>(dout);
+      od::KvRangeParams d{};
       d.k = static_cast<const __nv_bfloat16*>(k);
       d.v = static_cast<const __nv_bfloat16*>(v);
       d.ntok = 1LL * B * T * S;
-      d.Hq = Hq; d.Hkv = Hkv; d.kv_rows = kv_rows;
-      d.delta = delta;
+      d.Hkv = Hkv; d.kv_rows = kv_rows;
       d.amax = amax;
-      d.status = f.status;
       // one wave of resident CTAs: every CTA streams an equal share
-      const long long dgrid = dev->delta_o_ctas;
+      const long long dgrid = dev->range_ctas;
       amax_slots = static_cast<int>(dgrid);
       dp.amax_slots = amax_slots;
-      od::od_bwd_delta_o_kernel<<<(unsigned)dgrid, od::kDeltaOThreads, 0, strm>>>(d);
+      dp.o = static_cast<const __nv_bfloat16*>(o);
+      dp.o_lo = static_cast<const __nv_bfloat16*>(o_lo);
+      od::od_bwd_kv_range_kernel<<<(unsigned)dgrid, od::kKvRangeThreads, 0, strm>>>(d);
     } else {
       if (f.seqlen)
         od::od_bwd_dq_kernel<true, true, false><<<(unsigned)grid, od::kDqThreads, od::kDqSmemBytes, strm>>>(tq, tdo, tk, tv, dp);
@@ -460,6 +457,7 @@ od_status launch_bwd(int is_time, const void* q, const void* k, const void* v, c
     kp.amax = amax;
     kp.amax_slots = amax_slots;
     kp.dq_slots = dq_slots;
+    kp.dd_slots = o_lo ? dq_slots : amax_slots;
     const long long grid = kp.nitems < num_ctas ? kp.nitems : num_ctas;
     if (f.seqlen)
       od::od_bwd_dkdv_kernel<true, false><<<(unsigned)grid, od::kKvThreads, od::kKvSmemBytes, strm>>>(tq, tdo, tk, tv, kp);

@@ -7,16 +7,18 @@
 // dV_j += P_j dO  (dK, dV summed over the G query heads of a KV head).
 //
 // Three launches, no atomics, no zeroed workspace (results are deterministic):
-//   1. Delta per row in fp32 into the caller's workspace, and the operand ranges.  Given O's
-//        rounding residual O_lo from the forward: od_bwd_delta_o_kernel, Delta = <dO, O + O_lo>
-//        streamed from memory.  Otherwise od_bwd_dq_kernel<true, ...>, Delta = sum_j P_j dP_j
-//        (equal to <dO, O> for the exact O; the bf16 O alone would give Delta only to ~1e-2
-//        absolute, which the gradients inherit).
+//   1. Operand ranges, and Delta unless the dQ pass can form it.  Given O's rounding residual
+//        O_lo from the forward: od_bwd_kv_range_kernel, max|K| and max|V| only (the dQ pass
+//        forms Delta = <dO, O + O_lo> from its dO tile).  Otherwise od_bwd_dq_kernel<true, ...>,
+//        Delta = sum_j P_j dP_j per row in fp32 into the caller's workspace (equal to <dO, O>
+//        for the exact O; the bf16 O alone would give Delta only to ~1e-2 absolute, which the
+//        gradients inherit).
 //   2. od_bwd_dq_kernel<false, ...>: Q-tile stationary (the forward's work items and warp roles):
 //        S = Q K^T and dP = dO V^T per 96-key block in TMEM; dS written in place over S as
 //        fp16 times 2^eds; dQ += dS K into one fp32 accumulator, written once per tile.  Q
 //        tiles and K blocks are rewritten as scaled fp16 in shared memory first (see "fp16
-//        operand scaling"), so S runs on exact fp16 operands and dQ on fp16.
+//        operand scaling"), so S runs on exact fp16 operands and dQ on fp16.  With O_lo it
+//        also writes Delta to the workspace for the next launch.
 //   3. od_bwd_dkdv_kernel:  key-block stationary: a CTA item is (unit, 128-key block);
 //        for every Q tile that can see the block, S^T = K Q^T and dP^T = V dO^T in TMEM
 //        (keys on TMEM lanes), P^T and dS^T written in place (scaled fp16), then
@@ -47,9 +49,10 @@ constexpr int kKVTile = kBN * 128;  // bytes of one K or V stage
 // (dK: ||dO_i|| <= 8 max|dO|, |Delta_i| <= max|Delta|).  A single large element of V or dO
 // then lowers the scale only of the rows or keys it can reach.
 // Operand ranges live in kAmaxSlots slots of kAmaxStride floats after the Delta array in the
-// workspace, one slot per CTA of the launch that wrote it: the Delta launch (Delta pass or
-// Delta from O) writes max|K|, max|V|, max|dO|, max|Delta|; the dQ pass writes max|Q| (it
-// scales each Q tile by the tile's own range and records the maximum for the dK/dV kernel).
+// workspace, one slot per CTA of the launch that wrote it: the first launch writes max|K| and
+// max|V|, and max|dO| and max|Delta| where it forms Delta (the Delta pass); the dQ pass writes
+// max|Q| (it scales each Q tile by the tile's own range and records the maximum for the
+// dK/dV kernel), and max|dO| and max|Delta| where it forms Delta from O.
 constexpr int kAmaxSlots = 1024;
 constexpr int kAmaxStride = 8;
 constexpr int kAmK = 0, kAmV = 1, kAmDo = 2, kAmDelta = 3, kAmQ = 4;
@@ -125,6 +128,26 @@ __device__ __forceinline__ float row_norm2(const uint8_t* tile, int row) {
   return acc.x + acc.y;
 }
 
+// Eight bf16 elements of dO (d) against the same elements of O (o) and its residual (l):
+// returns sum dO (o + o_lo) in fp32 and adds sum dO^2 to *n2.
+__device__ __forceinline__ float chunk_delta(const uint4& d, const uint4& o, const uint4& l, float* n2) {
+  const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+  const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+  const uint32_t lw[4] = {l.x, l.y, l.z, l.w};
+  float2 acc = make_float2(0.f, 0.f), nn = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const float2 f = make_float2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
+    const float2 ov = make_float2(__uint_as_float(ow[h] << 16) + __uint_as_float(lw[h] << 16),
+                                  __uint_as_float(ow[h] & 0xFFFF0000u) +
+                                      __uint_as_float(lw[h] & 0xFFFF0000u));
+    acc = __ffma2_rn(f, ov, acc);
+    nn = __ffma2_rn(f, f, nn);
+  }
+  *n2 += nn.x + nn.y;
+  return acc.x + acc.y;
+}
+
 // Rewrite `bytes` of packed bf16 pairs as fp16 pairs times 2^e, in place (one warp).
 __device__ __forceinline__ void to_fp16_scaled(uint8_t* buf, int bytes, float s, int lane) {
   uint4* p = reinterpret_cast<uint4*>(buf);
@@ -157,11 +180,16 @@ struct DqParams {
   float* delta;           // Delta per query row (written by the Delta pass, read otherwise)
   float* amax;            // operand-range slots: the Delta pass writes its CTA's max|K|, max|V|,
                           // max|dO|, max|Delta|; the dQ pass its CTA's max|Q|
-  int amax_slots;         // dQ pass: slots the Delta launch wrote (scales for the fp16 products)
+  int amax_slots;         // dQ pass: slots the first launch wrote (scales for the fp16 products)
   float scale;
   __nv_bfloat16* dq;
   int dq_rows;            // 64-element rows per token of dq (Hq, or Hq + 2 Hkv when packed)
   float* dq_f32;          // optional, contiguous [B,T,S,Hq,64]
+  // dQ pass, optional: O and its residual O_lo (contiguous [B,T,S,Hq,64]).  Given, the pass
+  // forms Delta = <dO_i, O_i> itself, writes it for the dK/dV kernel and records max|dO| and
+  // max|Delta| in its slots; otherwise it reads Delta from the workspace.
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* o_lo;
 };
 
 struct DqSmem {
@@ -174,9 +202,10 @@ struct DqSmem {
   Ctl ctl;
   int ek;                     // dQ pass: K's fp16 scale exponent
   float vn8;                  // dQ pass: 8 max|V| >= every ||v_j||
-  unsigned int dmax_bits;     // Delta pass: max |Delta| of the CTA's rows (float bits)
+  unsigned int dmax_bits;     // max |Delta| of the CTA's rows (float bits): Delta pass, or
+                              // the dQ pass when it forms Delta from O
+  unsigned int domax_bits;    // max |dO| of the CTA's tiles (float bits), idem
   int eqt[2];                 // dQ pass: scale exponent of Q tile x
-  float dn2[2][128];          // dQ pass: ||dO_i||^2 of tile x's rows
 };
 // smem: [Q0 Q1 dO0 dO1][K stages][V stages][dQ staging 8 x 4 KB][DqSmem]
 constexpr size_t kDqTileBytes = size_t(4) * kTile + size_t(2 * kDqStages) * kKVTile + 8 * 4096;
@@ -235,7 +264,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.q_full[x], 1);
       // Delta pass: MMA commit + the range scanner; dQ pass: MMA commit + the 4 dS warps of
-      // the tile, which read the fill's eq and row norms (so the slot is not refilled first)
+      // the tile, which read the fill's eq and dO rows (so the slot is not refilled first)
       mbar_init(&sm.q_empty[x], kDelta ? 2 : 5);
       mbar_init(&sm.q16[x], 1);
       mbar_init(&sm.s_full[x], 1);
@@ -251,10 +280,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     sm.ctl.abort = 0;
     sm.dmax_bits = 0u;
+    sm.domax_bits = 0u;
     fence_mbar_init();
   }
   if (!kDelta && warp == kQsProducerWarp) {
-    // operand ranges recorded by the Delta launch -> K's scale and the bound on ||v_j||
+    // operand ranges recorded by the first launch -> K's scale and the bound on ||v_j||
     const float ak = slots_max(dp.amax, dp.amax_slots, kAmK, lane);
     const float av = slots_max(dp.amax, dp.amax_slots, kAmV, lane);
     if (lane == 0) {
@@ -281,9 +311,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       // ---------------------------------------------------------- operand conversion
       // dQ pass: every Q tile is rewritten in place as fp16 times 2^eq (eq from the tile's own
       // largest magnitude) and every K block as fp16 times 2^ek (S then runs on fp16 operands
-      // -- exact, the scales fold into the exponent -- and dQ += dS K on fp16 dS); the rows'
-      // ||dO_i||^2 and the tile's eq go to the dS warpgroups.  Released to the MMA issuers
-      // and the dS warpgroups through q16 / k16.  Walks the producer's fills in its order.
+      // -- exact, the scales fold into the exponent -- and dQ += dS K on fp16 dS); the tile's
+      // eq goes to the dS warpgroups.  Released to the MMA issuers and the dS warpgroups
+      // through q16 / k16.  Walks the producer's fills in its order.
       const float sk = ldexpf(1.f, ek);
       uint32_t mq = 0;  // running max|Q| over the CTA's tiles (bf16 bit pairs)
       long long prev_unit = -1;
@@ -310,7 +340,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           mq = __vmaxu2(mq, mt);
           const int eqt = fp16_shift(amax_reduce(mt));
           to_fp16_scaled(sQ[x], p.rows * 128, ldexpf(1.f, eqt), lane);
-          for (int rr = lane; rr < p.rows; rr += 32) sm.dn2[x][rr] = row_norm2(sdO[x], rr);
           if (lane == 0) sm.eqt[x] = eqt;
           fence_proxy_async_smem();
           __syncwarp();
@@ -584,41 +613,118 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int g = r - tok * G;
     const float lg2e = 1.4426950408889634f;
     uint32_t jS = 0, jD = 0, jq = 0;
-    uint32_t dmax = 0u;  // Delta pass: max |Delta| of this thread's rows (float bits; NaN on top)
+    uint32_t dmax = 0u;  // max |Delta| of this thread's rows (float bits; NaN on top)
+    uint32_t mdo = 0u;   // dQ pass from O: max |dO| of this thread's tile rows (bf16 pairs)
+    const bool from_o = !kDelta && dp.o != nullptr;
+    // the row's sequence position (packed: pt its frame, sp its token within the tile)
+    const int pt = PK ? tok / PK : 0;
+    const int sp = PK ? tok - pt * PK : 0;
+    // this thread's query row of item `it` in [B,T,S,Hq] order, if the tile row exists
+    auto row_of = [&](const FwdItem& it, long long* rw) -> bool {
+      const int t0 = x ? it.tok0[1] : it.tok0[0];
+      const int ps = PK ? pt : t0 + tok;
+      if (!(r < p.rows && (PK ? t0 + sp < p.S : ps < (kVarlen ? it.L : p.L)))) return false;
+      const long long t_idx = p.is_time ? ps : it.fixed;
+      const long long s_idx = PK ? t0 + sp : (p.is_time ? it.fixed : ps);
+      *rw = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + g;
+      return true;
+    };
+    bool first = true;
     bool ok = true;
     for (long long i = i0; i < i1 && ok; i += istep) {
       const FwdItem it = fwd_decode<kVarlen, kPacked>(p, i);
       if (kVarlen && !it.validA) continue;  // past the unit's length: no role touches it
       if (x == 1 && !it.validB) continue;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
-      // the row's sequence position pos (packed: its frame; sp its token within the tile)
-      const int pt = PK ? tok / PK : 0;
-      const int sp = PK ? tok - pt * PK : 0;
       const int pos = PK ? pt : mytok0 + tok;
       long long row = 0;
       float lse2 = INFINITY, dl = 0.f;
       float dacc[4] = {0.f, 0.f, 0.f, 0.f};
-      bool row_ok = (r < p.rows) && (PK ? mytok0 + sp < p.S : pos < (kVarlen ? it.L : p.L));
-      if (row_ok) {
-        const long long t_idx = p.is_time ? pos : it.fixed;
-        const long long s_idx = PK ? mytok0 + sp : (p.is_time ? it.fixed : pos);
-        row = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + g;
-        row_ok = OD_IN_RANGE(row, static_cast<long long>(p.B) * p.T * p.S * p.Hq, status, 212);
-      }
+      bool row_ok = row_of(it, &row);
+      if (row_ok) row_ok = OD_IN_RANGE(row, static_cast<long long>(p.B) * p.T * p.S * p.Hq, status, 212);
       if (row_ok) {
         lse2 = dp.lse[row] * lg2e;
-        if (!kDelta) dl = dp.delta[row];
+        if (!kDelta && !from_o) dl = dp.delta[row];
       }
+      // from O: the row's O and O_lo lines are sent towards L2 one item ahead (the first
+      // item's now), so that the loads below, on the way to this item's first dS, hit L2
+      if (from_o) {
+        if (first && row_ok) {
+          prefetch_l2(dp.o + row * 64);
+          prefetch_l2(dp.o_lo + row * 64);
+        }
+        long long rn;
+        if (i + istep < i1) {
+          const FwdItem nx = fwd_decode<kVarlen, kPacked>(p, i + istep);
+          if (!(kVarlen && !nx.validA) && !(x == 1 && !nx.validB) && row_of(nx, &rn) &&
+              rn < static_cast<long long>(p.B) * p.T * p.S * p.Hq) {
+            prefetch_l2(dp.o + rn * 64);
+            prefetch_l2(dp.o_lo + rn * 64);
+          }
+        }
+      }
+      first = false;
       // dQ pass: S carries 2^(eq + ek) (eq: this Q tile's); dS is written times 2^eds with eds
       // from the row's bound ||dO_i|| 8 max|V| + |Delta_i| on |dS|, and dQ undoes 2^(eds + ek)
       float slx = p.sl, c1 = 1.f, fq = dp.scale;
       OD_TP(80, (int)i, 0);
       if (!kDelta) {
+        // the row's ||dO_i|| (and, from O, Delta_i) from the dO tile as loaded; every row of
+        // the tile counts towards max|dO|, which scales whole tiles in the dK/dV kernel
+        ok = __all_sync(0xffffffffu, wait_bar(&sm.q_full[x], jq & 1u, ctl, status, 7));
+        if (!ok) break;
+        OD_TP(86, (int)i, 0);
+        float dn2 = 0.f;
+        if (from_o) {
+          // the warp's 32 rows 4 at a time, 8 lanes x 16 bytes per 128-byte row (coalesced
+          // loads of O and O_lo); each row's sums go back to the row's own lane
+          const int sub = lane >> 3, ch = lane & 7;
+          uint4 ov[8], lv[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const long long rw = __shfl_sync(0xffffffffu, row, 4 * k + sub);
+            const bool rok = __shfl_sync(0xffffffffu, static_cast<int>(row_ok), 4 * k + sub) != 0;
+            ov[k] = rok ? __ldg(reinterpret_cast<const uint4*>(dp.o) + rw * 8 + ch) : make_uint4(0, 0, 0, 0);
+            lv[k] = rok ? __ldg(reinterpret_cast<const uint4*>(dp.o_lo) + rw * 8 + ch) : make_uint4(0, 0, 0, 0);
+          }
+          float dsel = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 32 * (warp & 3) + 4 * k + sub;   // tile row (zeros past p.rows)
+            const uint4 d = *reinterpret_cast<const uint4*>(sdO[x] + rr * 128 + ((ch ^ (rr & 7)) << 4));
+            mdo = __vmaxu2(mdo, d.x & 0x7FFF7FFFu);
+            mdo = __vmaxu2(mdo, d.y & 0x7FFF7FFFu);
+            mdo = __vmaxu2(mdo, d.z & 0x7FFF7FFFu);
+            mdo = __vmaxu2(mdo, d.w & 0x7FFF7FFFu);
+            float n = 0.f;
+            float a = chunk_delta(d, ov[k], lv[k], &n);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+              a += __shfl_xor_sync(0xffffffffu, a, o);
+              n += __shfl_xor_sync(0xffffffffu, n, o);
+            }
+            const float at = __shfl_sync(0xffffffffu, a, (lane & 3) * 8);   // row 4k + (lane & 3)
+            const float nt = __shfl_sync(0xffffffffu, n, (lane & 3) * 8);
+            if ((lane >> 2) == k) {
+              dsel = at;
+              dn2 = nt;
+            }
+          }
+          if (row_ok) {
+            dl = dsel;
+            dp.delta[row] = dsel;
+            dmax = max(dmax, __float_as_uint(fabsf(dsel)));
+          }
+        } else if (row_ok) {
+          dn2 = row_norm2(sdO[x], r);
+        }
+        OD_TP(87, (int)i, 0);
         ok = __all_sync(0xffffffffu, wait_bar(&sm.q16[x], jq & 1u, ctl, status, 9));
         if (!ok) break;
+        OD_TP(88, (int)i, 0);
         ++jq;
         const int eqt = sm.eqt[x];
-        const float dn = row_ok ? sqrtf(sm.dn2[x][r]) : 0.f;
+        const float dn = row_ok ? sqrtf(dn2) : 0.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.q_empty[x]);  // this warp is done with the fill's values
         const int eds = fp16_shift(fmaf(dn, vn8, fabsf(dl)));
@@ -755,10 +861,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         __syncwarp();
       }
     }
-    if (kDelta) {
+    if (kDelta || from_o) {
       __syncwarp();
       const uint32_t m = __reduce_max_sync(0xffffffffu, dmax);
-      if (lane == 0) atomicMax(&sm.dmax_bits, m);
+      const float md = amax_reduce(mdo);
+      if (lane == 0) {
+        atomicMax(&sm.dmax_bits, m);
+        atomicMax(&sm.domax_bits, __float_as_uint(md));
+      }
     }
   }
 
@@ -766,7 +876,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (kDelta && tid == 0) dp.amax[kAmaxStride * blockIdx.x + kAmDelta] = __uint_as_float(sm.dmax_bits);
+  if ((kDelta || dp.o != nullptr) && tid == 0) {
+    dp.amax[kAmaxStride * blockIdx.x + kAmDelta] = __uint_as_float(sm.dmax_bits);
+    if (!kDelta) dp.amax[kAmaxStride * blockIdx.x + kAmDo] = __uint_as_float(sm.domax_bits);
+  }
   if (warp == kQsMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -808,8 +921,10 @@ struct KvParams {
   const float* lse;
   const float* delta;
   const float* amax;      // operand-range slots (see "fp16 operand scaling")
-  int amax_slots;         // slots the Delta launch wrote
+  int amax_slots;         // slots the first launch wrote (max|K|, max|V|)
   int dq_slots;           // slots the dQ pass wrote (max|Q|)
+  int dd_slots;           // slots holding max|dO| and max|Delta| (the Delta pass's, or the
+                          // dQ pass's when it formed Delta from O)
   float scale;
   long long nitems;       // units x key blocks
   int nkb;                // 128-key blocks per unit
@@ -989,12 +1104,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     fence_mbar_init();
   }
   if (warp == kKvProducerWarp) {
-    // operand ranges recorded by the Delta launch and the dQ pass -> scale exponents
+    // operand ranges recorded by the first launch and the dQ pass -> scale exponents
     const float aq = slots_max(kp.amax, kp.dq_slots, kAmQ, lane);
     const float ak = slots_max(kp.amax, kp.amax_slots, kAmK, lane);
     const float av = slots_max(kp.amax, kp.amax_slots, kAmV, lane);
-    const float ado = slots_max(kp.amax, kp.amax_slots, kAmDo, lane);
-    const float adl = slots_max(kp.amax, kp.amax_slots, kAmDelta, lane);
+    const float ado = slots_max(kp.amax, kp.dd_slots, kAmDo, lane);
+    const float adl = slots_max(kp.amax, kp.dd_slots, kAmDelta, lane);
     if (lane == 0) {
       sm.eq = fp16_shift(aq);
       sm.ek = fp16_shift(ak);
@@ -1441,102 +1556,44 @@ inline cudaError_t bwd_setup() {
   return e != cudaSuccess ? e : bwd_setup_one<false, true>();
 }
 
-// ============================================================================ Delta from O
+// ============================================================================ K/V ranges
 // When the forward also wrote O's rounding residual O_lo (O ~ o + o_lo to about 16 significant
-// bits), Delta = <dO, O> is a row-wise dot product of tensors in HBM and needs no recompute of
-// P and dP: this streaming kernel replaces the Delta pass.  It also records the operand
-// ranges max|K|, max|V|, max|dO|, max|Delta| per CTA, in the slots the Delta pass would fill
-// (Q's range is taken per tile by the dQ pass, so Q is not read here).
-// One warp takes 4 query rows at a time (8 lanes x 16 bytes per 128-byte row); every byte of
-// dO, O, O_lo, K and V is read once.
-constexpr int kDeltaOThreads = 256;
+// bits), Delta = <dO, O> is a row-wise dot product that the dQ pass forms from its dO tile and
+// two row loads (no recompute of P and dP, no extra pass over dO).  The dQ pass then needs
+// only the ranges of K and V up front (for K's fp16 scale and the bound on ||v_j||); this
+// streaming kernel records max|K| and max|V| per CTA, in the slots the Delta pass would fill.
+constexpr int kKvRangeThreads = 256;
 
-struct DeltaOParams {
-  const __nv_bfloat16* o;       // [rows, 64] contiguous
-  const __nv_bfloat16* o_lo;    // [rows, 64] contiguous
-  const __nv_bfloat16* dout;    // [rows, 64] contiguous
+struct KvRangeParams {
   const __nv_bfloat16* k;       // views: token i starts at row i * kv_rows
   const __nv_bfloat16* v;
   long long ntok;               // B * T * S
-  int Hq, Hkv, kv_rows;
-  float* delta;                 // [rows]
+  int Hkv, kv_rows;
   float* amax;                  // one slot of kAmaxStride floats per CTA
-  unsigned int* status;         // device status word (range checks of debug builds)
 };
 
-__device__ __forceinline__ float bf16x2_dot3(uint32_t d, uint32_t o, uint32_t l, float acc) {
-  const float d0 = __uint_as_float(d << 16), d1 = __uint_as_float(d & 0xFFFF0000u);
-  const float o0 = __uint_as_float(o << 16) + __uint_as_float(l << 16);
-  const float o1 = __uint_as_float(o & 0xFFFF0000u) + __uint_as_float(l & 0xFFFF0000u);
-  return fmaf(d1, o1, fmaf(d0, o0, acc));
-}
-
-__global__ void __launch_bounds__(kDeltaOThreads)
-    od_bwd_delta_o_kernel(const DeltaOParams p) {
-  __shared__ float red[kDeltaOThreads / 32][4];  // per warp: K, V, dO, Delta
+__global__ void __launch_bounds__(kKvRangeThreads)
+    od_bwd_kv_range_kernel(const KvRangeParams p) {
+  __shared__ float red[kKvRangeThreads / 32][2];  // per warp: K, V
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long long gw = static_cast<long long>(blockIdx.x) * (kDeltaOThreads / 32) + warp;
-  const long long nw = static_cast<long long>(gridDim.x) * (kDeltaOThreads / 32);
-  const int sub = lane >> 3, ch = lane & 7;
-  uint32_t mk = 0, mv = 0, md = 0;
-  uint32_t mdl = 0u;  // max |Delta| (float bits; NaN on top)
-
-  // Delta: groups of 4 rows, four groups in flight per warp
-  const long long nrows = p.ntok * p.Hq;
-  const long long ngroups = (nrows + 3) >> 2;
-  const uint4* D4 = reinterpret_cast<const uint4*>(p.dout);
-  const uint4* O4 = reinterpret_cast<const uint4*>(p.o);
-  const uint4* L4 = reinterpret_cast<const uint4*>(p.o_lo);
-  for (long long g0 = gw; g0 < ngroups; g0 += 4 * nw) {
-    uint4 d[4], o[4], l[4];
-    long long r[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      r[u] = 4 * (g0 + u * nw) + sub;
-      if (g0 + u * nw < ngroups && r[u] < nrows) {
-        d[u] = __ldg(D4 + r[u] * 8 + ch);
-        o[u] = __ldg(O4 + r[u] * 8 + ch);
-        l[u] = __ldg(L4 + r[u] * 8 + ch);
-      } else {
-        d[u] = o[u] = l[u] = make_uint4(0, 0, 0, 0);
-        r[u] = -1;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      md = __vmaxu2(md, d[u].x & 0x7FFF7FFFu);
-      md = __vmaxu2(md, d[u].y & 0x7FFF7FFFu);
-      md = __vmaxu2(md, d[u].z & 0x7FFF7FFFu);
-      md = __vmaxu2(md, d[u].w & 0x7FFF7FFFu);
-      float acc = bf16x2_dot3(d[u].x, o[u].x, l[u].x, 0.f);
-      acc = bf16x2_dot3(d[u].y, o[u].y, l[u].y, acc);
-      acc = bf16x2_dot3(d[u].z, o[u].z, l[u].z, acc);
-      acc = bf16x2_dot3(d[u].w, o[u].w, l[u].w, acc);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      if (ch == 0 && r[u] >= 0 && OD_IN_RANGE(r[u], nrows, p.status, 230)) {
-        p.delta[r[u]] = acc;
-        mdl = max(mdl, __float_as_uint(fabsf(acc)));
-      }
-    }
-  }
-
-  // operand ranges of K and V.  A contiguous tensor is one flat array (four 16-byte loads in
-  // flight per thread); a packed view is walked token by token (the token's head rows are
-  // contiguous), again four loads in flight per lane.
+  const long long gw = static_cast<long long>(blockIdx.x) * (kKvRangeThreads / 32) + warp;
+  const long long nw = static_cast<long long>(gridDim.x) * (kKvRangeThreads / 32);
   auto vmax4 = [](uint32_t m, const uint4& x) {
     m = __vmaxu2(m, x.x & 0x7FFF7FFFu);
     m = __vmaxu2(m, x.y & 0x7FFF7FFFu);
     m = __vmaxu2(m, x.z & 0x7FFF7FFFu);
     return __vmaxu2(m, x.w & 0x7FFF7FFFu);
   };
-  auto scan = [&](const __nv_bfloat16* base, int rows_per_tok, int heads, uint32_t m) {
+  // A contiguous tensor is one flat array (four 16-byte loads in flight per thread); a packed
+  // view is walked token by token (the token's head rows are contiguous), again four loads in
+  // flight per lane.
+  auto scan = [&](const __nv_bfloat16* base) {
+    uint32_t m = 0;
     const uint4* src = reinterpret_cast<const uint4*>(base);
-    if (rows_per_tok == heads) {
-      const long long n = p.ntok * heads * 8;
-      const long long nt = static_cast<long long>(gridDim.x) * kDeltaOThreads;
-      const long long t0 = static_cast<long long>(blockIdx.x) * kDeltaOThreads + threadIdx.x;
+    if (p.kv_rows == p.Hkv) {
+      const long long n = p.ntok * p.Hkv * 8;
+      const long long nt = static_cast<long long>(gridDim.x) * kKvRangeThreads;
+      const long long t0 = static_cast<long long>(blockIdx.x) * kKvRangeThreads + threadIdx.x;
       for (long long c = t0; c < n; c += 4 * nt) {
         uint4 x[4];
 #pragma unroll
@@ -1546,9 +1603,9 @@ __global__ void __launch_bounds__(kDeltaOThreads)
         for (int u = 0; u < 4; ++u) m = vmax4(m, x[u]);
       }
     } else {
-      const int nchunk = heads * 8;
+      const int nchunk = p.Hkv * 8;
       for (long long t = gw; t < p.ntok; t += nw) {
-        const uint4* row = src + t * rows_per_tok * 8;
+        const uint4* row = src + t * p.kv_rows * 8;
         for (int c = lane; c < nchunk; c += 128) {
           uint4 x[4];
 #pragma unroll
@@ -1561,23 +1618,21 @@ __global__ void __launch_bounds__(kDeltaOThreads)
     }
     return m;
   };
-  mk = scan(p.k, p.kv_rows, p.Hkv, mk);
-  mv = scan(p.v, p.kv_rows, p.Hkv, mv);
-
-  const float a[4] = {amax_reduce(mk), amax_reduce(mv), amax_reduce(md),
-                      __uint_as_float(__reduce_max_sync(0xffffffffu, mdl))};
-  if (lane == 0)
-    for (int c = 0; c < 4; ++c) red[warp][c] = a[c];
+  const float a[2] = {amax_reduce(scan(p.k)), amax_reduce(scan(p.v))};
+  if (lane == 0) {
+    red[warp][0] = a[0];
+    red[warp][1] = a[1];
+  }
   __syncthreads();
-  if (threadIdx.x < 4) {
+  if (threadIdx.x < 2) {
     float m = 0.f;
     bool nan = false;
-    for (int w = 0; w < kDeltaOThreads / 32; ++w) {
+    for (int w = 0; w < kKvRangeThreads / 32; ++w) {
       const float x = red[w][threadIdx.x];
       nan |= !(x == x);
       m = fmaxf(m, x);
     }
-    static_assert(kAmK == 0 && kAmV == 1 && kAmDo == 2 && kAmDelta == 3, "slot fields in order");
+    static_assert(kAmK == 0 && kAmV == 1, "slot fields in order");
     p.amax[kAmaxStride * blockIdx.x + threadIdx.x] = nan ? __int_as_float(0x7fc00000) : m;
   }
 }

@@ -10,7 +10,7 @@ consecutive events of each warp, which is how waits are told apart from work.
     python -m block_causal_video_attention_b300.trace minecraft_fwd_bwd space dq
 
 Events (see OD_TP in the sources): forward softmax 1-9, MMA issuers 10-13 and 44-45, producer
-20-23, V converter 30; dQ pass dS warps 80-85 and MMA issuers 90-91; dK/dV elementwise 40-47,
+20-23, V converter 30; dQ pass dS warps 80-88 and MMA issuers 90-91; dK/dV elementwise 40-47,
 producer 50-51, MMA issuer 61-64, converters 70-73.  Clocks of different warps share a base,
 within a CTA.
 """
