@@ -619,14 +619,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // the row's sequence position (packed: pt its frame, sp its token within the tile)
     const int pt = PK ? tok / PK : 0;
     const int sp = PK ? tok - pt * PK : 0;
-    // this thread's query row of item `it` in [B,T,S,Hq] order, if the tile row exists
-    auto row_of = [&](const FwdItem& it, long long* rw) -> bool {
+    // this thread's token of item `it` ([B,T,S] order), if the tile row exists; its query
+    // row is token * Hq + kvh G + g
+    auto token_of = [&](const FwdItem& it, long long* ti) -> bool {
       const int t0 = x ? it.tok0[1] : it.tok0[0];
       const int ps = PK ? pt : t0 + tok;
       if (!(r < p.rows && (PK ? t0 + sp < p.S : ps < (kVarlen ? it.L : p.L)))) return false;
       const long long t_idx = p.is_time ? ps : it.fixed;
       const long long s_idx = PK ? t0 + sp : (p.is_time ? it.fixed : ps);
-      *rw = ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * p.Hq + it.kvh * G + g;
+      *ti = (static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx;
       return true;
     };
     bool first = true;
@@ -637,10 +638,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (x == 1 && !it.validB) continue;
       const int mytok0 = x ? it.tok0[1] : it.tok0[0];
       const int pos = PK ? pt : mytok0 + tok;
-      long long row = 0;
+      long long tix = 0, row = 0;
       float lse2 = INFINITY, dl = 0.f;
       float dacc[4] = {0.f, 0.f, 0.f, 0.f};
-      bool row_ok = row_of(it, &row);
+      bool row_ok = token_of(it, &tix);
+      row = tix * p.Hq + it.kvh * G + g;
       if (row_ok) row_ok = OD_IN_RANGE(row, static_cast<long long>(p.B) * p.T * p.S * p.Hq, status, 212);
       if (row_ok) {
         lse2 = dp.lse[row] * lg2e;
@@ -653,13 +655,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           prefetch_l2(dp.o + row * 64);
           prefetch_l2(dp.o_lo + row * 64);
         }
-        long long rn;
+        long long tn;
         if (i + istep < i1) {
           const FwdItem nx = fwd_decode<kVarlen, kPacked>(p, i + istep);
-          if (!(kVarlen && !nx.validA) && !(x == 1 && !nx.validB) && row_of(nx, &rn) &&
-              rn < static_cast<long long>(p.B) * p.T * p.S * p.Hq) {
-            prefetch_l2(dp.o + rn * 64);
-            prefetch_l2(dp.o_lo + rn * 64);
+          if (!(kVarlen && !nx.validA) && !(x == 1 && !nx.validB) && token_of(nx, &tn)) {
+            const long long rn = tn * p.Hq + nx.kvh * G + g;
+            if (rn < static_cast<long long>(p.B) * p.T * p.S * p.Hq) {
+              prefetch_l2(dp.o + rn * 64);
+              prefetch_l2(dp.o_lo + rn * 64);
+            }
           }
         }
       }
@@ -838,21 +842,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           *reinterpret_cast<uint4*>(stg + wr * 128 + ((c ^ (wr & 7)) << 4)) = wv;
         }
         __syncwarp();
+        // rows 4k + sub of the warp, 8 lanes x 16 bytes per row; each row's dQ row comes
+        // from the row's own lane (-1: no row)
         const int sub = lane >> 3, ch = lane & 7;
+        const long long rq = row_ok ? tix * dp.dq_rows + it.kvh * G + g : -1LL;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int rr = 4 * k + sub;
-          const int rt = (warp & 3) * 32 + rr;
-          const int tk = rt / G;
-          const int gg = rt - tk * G;
-          const int tp = PK ? tk / PK : 0;                 // packed: frame and token
-          const int spp = PK ? tk - tp * PK : 0;
-          const int ps = PK ? tp : mytok0 + tk;
-          if (rt < p.rows && (PK ? mytok0 + spp < p.S : ps < (kVarlen ? it.L : p.L))) {
-            const long long t_idx = p.is_time ? ps : it.fixed;
-            const long long s_idx = PK ? mytok0 + spp : (p.is_time ? it.fixed : ps);
-            const long long rw =
-                ((static_cast<long long>(it.b) * p.T + t_idx) * p.S + s_idx) * dp.dq_rows + it.kvh * G + gg;
+          const long long rw = __shfl_sync(0xffffffffu, rq, rr);
+          if (rw >= 0) {
             const uint4 wv = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
             if (OD_IN_RANGE(rw, static_cast<long long>(p.B) * p.T * p.S * dp.dq_rows, status, 213))
               reinterpret_cast<uint4*>(dp.dq + rw * 64)[ch] = wv;
