@@ -505,6 +505,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int x = warp - kQsMmaWarp;
         const uint32_t tS = tmem + 256u * x, tP = tS + 96u, tQ = tS + 192u;
         const uint32_t idesc_dq = idesc_fp16(128, 64, 0, 1);
+        // operand descriptors: this tile's Q and dO, stage 0's K and V (a stage's are these
+        // plus its offset in 16-byte units; every address stays below 2^18, the field's range)
+        const uint64_t d_q = sdesc_sw128(smem_u32(sQ[x]), 16, 1024);
+        const uint64_t d_do = sdesc_sw128(smem_u32(sdO[x]), 16, 1024);
+        const uint64_t d_k = sdesc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t d_v = sdesc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t d_kq = sdesc_sw128(smem_u32(sK), 1024, 1024);   // K as dQ's B (MN-major)
         // the dQ pass reads Q and K after their fp16 rewrite, the Delta pass as loaded
         uint64_t* const qb = kDelta ? sm.q_full : sm.q16;
         uint64_t* const kb16 = kDelta ? sm.k_full : sm.k16;
@@ -556,20 +563,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const int b0 = (x ? it.blo[1] : it.blo[0]) - it.kb_lo, b1 = (x ? it.bhi[1] : it.bhi[0]) - it.kb_lo;
           auto issue_s = [&](int bi) -> bool {
             const KvSlot ks = slot(bi);
-            if (!__all_sync(0xffffffffu, wait_bar(&kb16[ks.stage], ks.parity, ctl, status, 15))) return false;
-            if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 15))) return false;
-            tc_fence_after();
+            if (!resident) {   // (a resident unit's stages were all waited for at its start)
+              if (!__all_sync(0xffffffffu, wait_bar(&kb16[ks.stage], ks.parity, ctl, status, 15))) return false;
+              if (!__all_sync(0xffffffffu, wait_bar(&sm.v_full[ks.stage], ks.parity, ctl, status, 15))) return false;
+              tc_fence_after();
+            }
             const int n = round16(block_keys<kPacked>(p, it, it.kb_lo + bi, kBN));
             const uint32_t idesc = idesc_bf16(128, n, 0, 0);
             const uint32_t idesc_s = kDelta ? idesc : idesc_fp16(128, n, 0, 0);
-            const uint64_t aq = sdesc_sw128(smem_u32(sQ[x]), 16, 1024);
-            const uint64_t ado = sdesc_sw128(smem_u32(sdO[x]), 16, 1024);
-            const uint64_t bk = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 16, 1024);
-            const uint64_t bv = sdesc_sw128(smem_u32(sV + ks.stage * kKVTile), 16, 1024);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss_w(tS, aq + 2 * k, bk + 2 * k, idesc_s, k > 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss_w(tP, ado + 2 * k, bv + 2 * k, idesc, k > 0);
+            const uint64_t so = static_cast<uint64_t>((ks.stage * kKVTile) >> 4);
+            mma_ss_k64_w(tS, d_q, d_k + so, idesc_s);
+            mma_ss_k64_w(tP, d_do, d_v + so, idesc);
             mma_commit_w(&sm.s_full[x]);
             ++js;
             if (bi == b1) mma_commit_w(&sm.q_empty[x]);
@@ -584,9 +588,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             const KvSlot ks = slot(bi);
             if (!kDelta) {
               const int ksteps = round16(block_keys<kPacked>(p, it, it.kb_lo + bi, kBN)) >> 4;
-              const uint64_t bk = sdesc_sw128(smem_u32(sK + ks.stage * kKVTile), 1024, 1024);
-              for (int k = 0; k < ksteps; ++k)
-                mma_ts_w(tQ, tS + 8 * k, bk + (2048 >> 4) * k, idesc_dq, (bi > b0 || k > 0));
+              const uint64_t so = static_cast<uint64_t>((ks.stage * kKVTile) >> 4);
+              mma_ts_kn6_w(tQ, tS, d_kq + so, idesc_dq, bi > b0 ? 1u : 0u, static_cast<uint32_t>(ksteps));
             }
             if (!resident) mma_commit_w(&sm.kv_empty[ks.stage]);
             if (bi == b1) {
@@ -1228,10 +1231,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const uint64_t bo = sdesc_sw128(smem_u32(sQD + (2 * q + 1) * kTile + h * 8192), 16, 1024);
           const uint32_t dS = tmem + 128u * h, dP = dS + 64u;
           const uint32_t aK = tmem + 384u, aV = tmem + 416u;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_ts_w(dS, aK + 8 * kk, bq + 2 * kk, idesc_sp, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_ts_w(dP, aV + 8 * kk, bo + 2 * kk, idesc_sp, kk > 0);
+          mma_ts_k64_kb_w(dS, aK, bq, idesc_sp);
+          mma_ts_k64_kb_w(dP, aV, bo, idesc_sp);
           mma_commit_w(&sm.sp_full[h]);
         };
         auto issue_dkv = [&](int h, uint32_t t, bool first) {
@@ -1239,11 +1240,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const uint64_t bq = sdesc_sw128(smem_u32(sQD + (2 * q) * kTile + h * 8192), 1024, 1024);
           const uint64_t bo = sdesc_sw128(smem_u32(sQD + (2 * q + 1) * kTile + h * 8192), 1024, 1024);
           const uint32_t aP = tmem + 128u * h, aD = aP + 64u;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_ts_w(tDV, aP + 8 * kk, bo + (2048 >> 4) * kk, idesc_acc, !(first && kk == 0));
-            mma_ts_w(tDK, aD + 8 * kk, bq + (2048 >> 4) * kk, idesc_acc, !(first && kk == 0));
-          }
+          mma_ts_k64_w(tDV, aP, bo, idesc_acc, first ? 0u : 1u);
+          mma_ts_k64_w(tDK, aD, bq, idesc_acc, first ? 0u : 1u);
         };
         // waits for the operands of tile t (item ordinal item_n, new item or not)
         auto wait_operands = [&](uint32_t t, uint32_t item_n, bool new_item) -> bool {

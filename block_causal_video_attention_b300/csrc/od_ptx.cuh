@@ -327,6 +327,48 @@ __device__ __forceinline__ void mma_ts_k64_w(uint32_t d_tmem, uint32_t a_tmem, u
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] B[smem] over K = 64 with B K-major: four k-steps of 16 (A advanced by
+// 8 columns, B by 32 bytes); the first overwrites D.
+__device__ __forceinline__ void mma_ts_k64_kb_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e, t, f;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "setp.eq.u32 t, %3, %3;\n\tsetp.ne.u32 f, %3, %3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, f;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] B[smem] over the first 16 nsteps (1 <= nsteps <= 6) rows of B: k-steps
+// of 16 (A advanced by 8 columns, B by 2048 bytes); the first accumulates only if `accumulate`.
+__device__ __forceinline__ void mma_ts_kn6_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate, uint32_t nsteps) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t, e1, e2, e3, e4, e5;\n\t.reg .b32 a1, a2, a3, a4, a5;\n\t"
+      ".reg .b64 b1, b2, b3, b4, b5;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.u32 a4, %1, 32;\n\tadd.u32 a5, %1, 40;\n\t"
+      "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\t"
+      "add.s64 b4, %2, 512;\n\tadd.s64 b5, %2, 640;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, %3, %3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.gt.and.u32 e1, %5, 1, e;\n\tsetp.gt.and.u32 e2, %5, 2, e;\n\t"
+      "setp.gt.and.u32 e3, %5, 3, e;\n\tsetp.gt.and.u32 e4, %5, 4, e;\n\t"
+      "setp.gt.and.u32 e5, %5, 5, e;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e1 tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "@e2 tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "@e3 tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t"
+      "@e4 tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n\t"
+      "@e5 tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(nsteps)
+      : "memory");
+}
 // tcgen05.commit from the same elected lane (the lowest active one) that issued the MMAs.
 __device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
   asm volatile(
