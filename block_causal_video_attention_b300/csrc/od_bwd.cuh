@@ -1225,10 +1225,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         bool ok = seq.next(kp, &cur);
         uint32_t n = 0, tau = 0;      // item and tile ordinals of the current tile
         int k = 0;                    // tile within the current item
+        // descriptors of slot 0's Q tile (K-major, and MN-major for the dK/dV products); a
+        // half tile of a slot is these plus its offset in 16-byte units (addresses < 2^18)
+        const uint64_t d_qk = sdesc_sw128(smem_u32(sQD), 16, 1024);
+        const uint64_t d_qm = sdesc_sw128(smem_u32(sQD), 1024, 1024);
+        auto half_off = [&](uint32_t t, int which, int h) -> uint64_t {
+          const uint32_t q = t % kKvQSlots;
+          return static_cast<uint64_t>(((2 * q + which) * kTile + h * 8192) >> 4);
+        };
         auto issue_sp = [&](int h, uint32_t t) {
-          const int q = static_cast<int>(t % kKvQSlots);
-          const uint64_t bq = sdesc_sw128(smem_u32(sQD + (2 * q) * kTile + h * 8192), 16, 1024);
-          const uint64_t bo = sdesc_sw128(smem_u32(sQD + (2 * q + 1) * kTile + h * 8192), 16, 1024);
+          const uint64_t bq = d_qk + half_off(t, 0, h);
+          const uint64_t bo = d_qk + half_off(t, 1, h);
           const uint32_t dS = tmem + 128u * h, dP = dS + 64u;
           const uint32_t aK = tmem + 384u, aV = tmem + 416u;
           mma_ts_k64_kb_w(dS, aK, bq, idesc_sp);
@@ -1236,9 +1243,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mma_commit_w(&sm.sp_full[h]);
         };
         auto issue_dkv = [&](int h, uint32_t t, bool first) {
-          const int q = static_cast<int>(t % kKvQSlots);
-          const uint64_t bq = sdesc_sw128(smem_u32(sQD + (2 * q) * kTile + h * 8192), 1024, 1024);
-          const uint64_t bo = sdesc_sw128(smem_u32(sQD + (2 * q + 1) * kTile + h * 8192), 1024, 1024);
+          const uint64_t bq = d_qm + half_off(t, 0, h);
+          const uint64_t bo = d_qm + half_off(t, 1, h);
           const uint32_t aP = tmem + 128u * h, aD = aP + 64u;
           mma_ts_k64_w(tDV, aP, bo, idesc_acc, first ? 0u : 1u);
           mma_ts_k64_w(tDK, aD, bq, idesc_acc, first ? 0u : 1u);
