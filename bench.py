@@ -71,13 +71,13 @@ def bwd_bytes(w):
 # --metrics dram__bytes_read.sum,dram__bytes_write.sum (summary in profiles/).  They hold only
 # for the kernel sources they were measured on: any change to those sources voids them.
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "0bae16a6040ebf5f758dd6cd59a09e268dce40d02df623c0da43792f324a45c8",
+    "csrc_sha256": "b29992100f34d1f880ba643fa686fda5fbfca8a18080bb95f125251b173e2a8e",
     "minecraft_fwd_bwd": {
         # forward with the O residual; backward: K/V ranges, dQ (with Delta from O + O_lo), dK/dV
-        "space_fwd": 919379866,
-        "time_fwd": 917104026,
-        "space_bwd": 2311540275,
-        "time_bwd": 2317447680,
+        "space_fwd": 919118131,
+        "time_fwd": 917009408,
+        "space_bwd": 2311719270,
+        "time_bwd": 2317537485,
     },
     # decode: 4-rollout capture (176.42 MB read, 2.57 MB written, mean of 5 calls) scaled by
     # the units (x4); taken on sources whose decode kernel (od_decode.cuh and the helpers it
