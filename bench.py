@@ -279,6 +279,17 @@ def oracle_full(w, with_bwd, chunk=48):
     return tot_flop, tot_s, nth, desc
 
 
+def fwd_bwd_config(args, w, with_bwd, world, ops):
+    """The `config` object of a fwd/bwd line; both arms print the same one."""
+    return {"workload": w.name, "B": w.B, "T": w.T, "S": w.S, "Hq": w.Hq,
+            "Hkv": w.Hkv, "head_dim": w.D, "window": w.window, "agent": w.agent,
+            "ops": ops, "delta": ("recomputed from P and dP" if (not with_bwd or args.no_residual)
+                                  else "from O + O_lo (forward writes the residual)"),
+            "qkv": "packed [B,T,S,Hq+2Hkv,D]" if args.packed else "separate",
+            "l2": "inputs larger than L2 (Q alone %.0f MB)" % (w.B * w.T * w.S * w.Hq * w.D * 2 / 1e6),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args, w, with_bwd):
     rank, world, _ = dist_info()
     if rank != 0:
@@ -299,7 +310,9 @@ def run_reference(args, w, with_bwd):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name},
+            "data": "synthetic",
+            "config": fwd_bwd_config(args, w, with_bwd, world,
+                                     ["space_fwd", "time_fwd"] + (["space_bwd", "time_bwd"] if with_bwd else [])),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": nth, "kind": "oracle",
                              "sample": desc + " per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -513,14 +526,7 @@ def run_ours(args, w, with_bwd):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": w.name, "B": w.B, "T": w.T, "S": w.S, "Hq": w.Hq,
-                           "Hkv": w.Hkv, "head_dim": w.D, "window": w.window, "agent": w.agent,
-                           "ops": ops, "delta": ("recomputed from P and dP" if (not with_bwd or args.no_residual)
-                                                 else "from O + O_lo (forward writes the residual)"),
-                           "qkv": "packed [B,T,S,Hq+2Hkv,D]" if packed else "separate",
-                           "l2": "inputs larger than L2 (Q alone %.0f MB)" %
-                           (w.B * w.T * w.S * w.Hq * w.D * 2 / 1e6),
-                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "config": fwd_bwd_config(args, w, with_bwd, world, ops),
                 "per_op": per_op, "roofline": roof, "cpu_baseline": cpu,
                 "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
