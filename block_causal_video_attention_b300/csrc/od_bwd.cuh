@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const FwdParams& p = dp.f;
   const int PK = kPacked ? p.pk : 0;   // packed: token positions per tile
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned start of the dynamic shared memory, formed by pointer arithmetic on the
+  // __shared__ array (not through an integer) so that every tile is addressed as shared memory
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ[2] = {base, base + kTile};
   uint8_t* sdO[2] = {base + 2 * kTile, base + 3 * kTile};
   uint8_t* sK = base + 4 * kTile;
@@ -1060,8 +1061,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const FwdParams& p = kp.f;
   const int PK = kPacked ? p.pk : 0;   // packed: token positions per key block
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned start of the dynamic shared memory, formed by pointer arithmetic on the
+  // __shared__ array (not through an integer) so that every tile is addressed as shared memory
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sKV = base;                     // slot s: K at 2s*kTile, V at (2s+1)*kTile
   uint8_t* sQD = base + 4 * kTile;         // slot q: Q at 2q*kTile, dO at (2q+1)*kTile
   KvSmem& sm = *reinterpret_cast<KvSmem*>(base + kKvTileBytes);

@@ -257,8 +257,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                        const __grid_constant__ CUtensorMap tm_o,
                        const __grid_constant__ CUtensorMap tm_lo, const AttnFwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned start of the dynamic shared memory, formed by pointer arithmetic on the
+  // __shared__ array (not through an integer) so that every tile is addressed as shared memory
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = base;  // tile x, slot s at (2x + s) * kTile
   uint8_t* sK = base + 4 * kTile;
   uint8_t* sV = sK + kFwdStages * kFwdKVTile;
