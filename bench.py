@@ -71,13 +71,13 @@ def bwd_bytes(w):
 # --metrics dram__bytes_read.sum,dram__bytes_write.sum (summary in profiles/).  They hold only
 # for the kernel sources they were measured on: any change to those sources voids them.
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "b29992100f34d1f880ba643fa686fda5fbfca8a18080bb95f125251b173e2a8e",
+    "csrc_sha256": "5621d56d5edc540aca42aa831a0c4027c0d688e687a7903a7590dae10fdbfd00",
     "minecraft_fwd_bwd": {
         # forward with the O residual; backward: K/V ranges, dQ (with Delta from O + O_lo), dK/dV
-        "space_fwd": 919118131,
-        "time_fwd": 917009408,
-        "space_bwd": 2311719270,
-        "time_bwd": 2317537485,
+        "space_fwd": 919082189,
+        "time_fwd": 915951053,
+        "space_bwd": 2311614208,
+        "time_bwd": 2317548902,
     },
     # decode: 4-rollout capture (176.42 MB read, 2.57 MB written, mean of 5 calls) scaled by
     # the units (x4); taken on sources whose decode kernel (od_decode.cuh and the helpers it
