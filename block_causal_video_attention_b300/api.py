@@ -35,7 +35,8 @@ _lib = None
 _debug_lib = None
 _override = None   # set inside debug_build(): the binding's calls go to that library
 
-# kernels one backward call launches (row statistics, main kernel, dQ conversion)
+# kernels one backward call launches: the K/V range kernel (with O_lo) or the Delta pass, the
+# dQ pass, the dK/dV kernel
 BWD_LAUNCHES = 3
 
 STATUS = {0: "OD_OK", 1: "OD_ERR_INVALID_ARG", 2: "OD_ERR_UNSUPPORTED", 3: "OD_ERR_CUDA",
