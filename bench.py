@@ -279,6 +279,16 @@ def oracle_full(w, with_bwd, chunk=48):
     return tot_flop, tot_s, nth, desc
 
 
+def varlen_config(w, lengths):
+    """The `config` object of a variable-length line; both arms print the same one."""
+    return {"workload": w.name + "_varlen", "B": w.B, "T": w.T, "S_max": w.S,
+            "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D,
+            "tokens_per_block": {"mean": float(lengths.mean()),
+                                 "min": int(lengths.min()), "max": int(lengths.max())},
+            "ops": ["space_fwd", "space_bwd"], "l2": "inputs larger than L2",
+            "parallelism": "single GPU"}
+
+
 def fwd_bwd_config(args, w, with_bwd, world, ops):
     """The `config` object of a fwd/bwd line; both arms print the same one."""
     return {"workload": w.name, "B": w.B, "T": w.T, "S": w.S, "Hq": w.Hq,
@@ -584,7 +594,7 @@ def run_varlen(args, w):
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * sum(v_[1] for v_ in vals) / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f64", "data": "synthetic", "config": {"workload": w.name + "_varlen"},
+                "dtype": "f64", "data": "synthetic", "config": varlen_config(w, lengths),
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(0),
                                  "kind": "oracle", "sample": "one whole timestep block per step"},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -694,12 +704,7 @@ def run_varlen(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name + "_varlen", "B": w.B, "T": w.T, "S_max": w.S,
-                       "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D,
-                       "tokens_per_block": {"mean": float(lengths.mean()),
-                                            "min": int(lengths.min()), "max": int(lengths.max())},
-                       "ops": ["space_fwd", "space_bwd"], "l2": "inputs larger than L2",
-                       "parallelism": "single GPU"},
+            "config": varlen_config(w, lengths),
             "per_op": {"space_fwd": {"ms": fwd_ms, "tflops": fl_f / (fwd_ms * 1e-3) / 1e12},
                        "space_bwd": {"ms": bwd_ms, "tflops": bwd_tf}},
             "dense": {"ms_per_step": dense_ms, "fwd_ms": dense_fwd, "bwd_ms": dense_bwd,
@@ -745,6 +750,16 @@ def decode_oracle_sample(w, rollouts, inputs=None):
             rollouts, w.B, w.name, w.S, w.Hkv))
 
 
+def decode_config(w, world):
+    """The `config` object of a decode line; both arms print the same one (the step decodes
+    frame w.T - 1: every step reads a full window)."""
+    return {"workload": w.name, "rollouts": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
+            "head_dim": w.D, "window": w.window, "frame_index": w.T - 1,
+            "l2": "inputs larger than L2 (KV cache %.0f MB)" %
+            (2 * w.B * w.window * w.S * w.Hkv * w.D * 2 / 1e6),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_decode(args, w):
     import torch
     import torch.distributed as dist
@@ -763,7 +778,7 @@ def run_decode(args, w):
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * s / args.steps, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": w.name},
+                "config": decode_config(w, world),
                 "cpu_baseline": {"value": value, "unit": "GB/s", "cores": vals[0][2],
                                  "kind": "oracle", "sample": vals[0][3] + " per step"},
                 "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -784,7 +799,7 @@ def run_decode(args, w):
     stream = torch.cuda.current_stream()
     o = torch.empty_like(dq)
     lse = torch.empty(dq.shape[:3], dtype=torch.float32, device=dev)
-    t0 = w.T - 1  # steady state: every step reads a full window
+    t0 = w.T - 1  # steady state: every step reads a full window (decode_config says so)
 
     def step(i, Q=dq, KN=dkn, VN=dvn):
         api.time_attn_decode(Q, KN, VN, dkc, dvc, t0 + i, w.scale, o, lse, stream)
@@ -862,11 +877,7 @@ def run_decode(args, w):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": w.name, "rollouts": w.B, "S": w.S, "Hq": w.Hq,
-                           "Hkv": w.Hkv, "head_dim": w.D, "window": w.window,
-                           "frame_index": t0, "l2": "inputs larger than L2 (KV cache %.0f MB)" %
-                           (2 * w.B * w.window * w.S * w.Hkv * w.D * 2 / 1e6),
-                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "config": decode_config(w, world),
                 "tflops": decode_flops(w) / (kern_ms * 1e-3) / 1e12,
                 "roofline": roof, "cpu_baseline": cpu,
                 "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d,
